@@ -1,0 +1,518 @@
+#!/usr/bin/env python3
+"""Benchmark: Q4_0 x Q8_0 ggml_mul_mat on GB300.
+
+One step = one pass of the whole hot path over the workload's projection set:
+for every weight matrix, the activations are quantized to Q8_0 and multiplied
+by the resident Q4_0 weights (one q4q_mul_mat call per matrix, captured once in
+a CUDA graph and replayed).  Weight quantization (Q4_0 encode) happens once
+before timing, as a model load would do it, and is timed separately.
+
+Default workload: GPT-2 117M decode-step weight set at 1 token (12 layers x
+{768->2304, 768->768, 768->3072, 3072->768} + lm_head 768->50257), seed 1.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+Prints one JSON line (rank 0).  `value` is weight GB/s (Q4_0 weight bytes
+streamed per second, all ranks).  With torchrun (N > 1) every rank runs its own
+replica of the workload (the path has no exchange step): weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "Q4_0 mul_mat weight GB/s vs HBM peak (1 tok); int8 TOPS at 512 tok"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# --------------------------------------------------------------- helpers ----
+
+def _env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+def _measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _profile_traffic(kernel_file: str, summary: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel source is
+    unchanged since it was taken (the summary records the source's sha256)."""
+    try:
+        with open(os.path.join(ROOT, "profiles", summary), encoding="utf-8") as f:
+            text = f.read()
+        src = open(os.path.join(ROOT, "q4_quantized_matmul_gb300", "csrc", kernel_file), "rb").read()
+        sha = hashlib.sha256(src).hexdigest()[:16]
+        m_sha = re.search(r"source_sha256_16:\s*([0-9a-f]+)", text)
+        m_tr = re.search(r"dram_bytes_per_step:\s*([0-9.eE+]+)", text)
+        if m_sha and m_tr and m_sha.group(1) == sha:
+            return float(m_tr.group(1))
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the GPU is busy."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int, period_ms: int = 100):
+        self.index = index
+        self.proc = None
+        self.period_ms = period_ms
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY, "--format=csv,noheader,nounits",
+                 "-lms", str(self.period_ms)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), sm_max=float(parts[2]), power=float(parts[3]),
+                                 hw=parts[5], hw_thermal=parts[6], sw_thermal=parts[7], sw_power=parts[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                              ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows), "sm_max_mhz": max(r["sm_max"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(r["power"] for r in rows)}
+
+
+# --------------------------------------------------------------- the arms ---
+
+def _weights_bytes(shapes):
+    return sum(n * (k // 32) * 18 for k, n in shapes)
+
+
+def _workload(name):
+    from q4_quantized_matmul_gb300 import workloads
+    return workloads.WORKLOADS[name]
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import q4_quantized_matmul_gb300 as q4q
+    from q4_quantized_matmul_gb300 import workloads
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl = _workload(args.workload)
+    ne11 = args.ne11 or wl.ne11[0]
+    shapes = list(wl.shapes)
+    nmat = len(shapes)
+
+    # ---- set-up (untimed): fp32 weights -> Q4_0 on the GPU, activations resident
+    t_q = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    wq, xs, dsts = [], [], []
+    quant_ms, quant_in_bytes = 0.0, 0
+    for i, (ne00, ne01) in enumerate(shapes):
+        w, x = workloads.problem(args.workload, i, ne11)
+        wd = torch.from_numpy(w).to(dev)
+        t_q[0].record()
+        wq.append(q4q.q4q_quantize_q4_0(wd))
+        t_q[1].record()
+        torch.cuda.synchronize()
+        quant_ms += t_q[0].elapsed_time(t_q[1])
+        quant_in_bytes += w.nbytes
+        del wd
+        xs.append(torch.from_numpy(x).to(dev))
+        dsts.append(torch.empty((ne11, ne01), dtype=torch.float32, device=dev))
+    wbytes = _weights_bytes(shapes)
+    # rotate weight copies so that every step reads its weights from HBM, not L2
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    copies = max(1, -(-3 * l2 // wbytes)) if wbytes < 3 * l2 else 1
+    copies = max(copies, 2)
+    wsets = [wq] + [[t.clone() for t in wq] for _ in range(copies - 1)]
+    ws_bytes = max(q4q.q4q_mul_mat_workspace_size(k, n, ne11) for k, n in shapes)
+    workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(c):
+        for i, (ne00, ne01) in enumerate(shapes):
+            q4q.q4q_mul_mat(wsets[c][i], ne00, ne01, xs[i], dst=dsts[i], workspace=workspace)
+
+    with torch.cuda.stream(stream):
+        for c in range(copies):         # first calls outside capture (one-time set-up per kernel)
+            step(c)
+    torch.cuda.synchronize()
+    graphs = []
+    for c in range(copies):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step(c)
+        graphs.append(g)
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    # untimed soak so the clock sampler sees the GPU under load, then the warm-up steps
+    t_end = time.time() + args.soak
+    n = 0
+    with torch.cuda.stream(stream):
+        while time.time() < t_end:
+            graphs[n % copies].replay()
+            n += 1
+            if n % 200 == 0:
+                stream.synchronize()
+        for k in range(args.warmup):
+            graphs[k % copies].replay()
+    torch.cuda.synchronize()
+
+    # ---- timed region: exactly K steps
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for k in range(args.steps):
+            graphs[k % copies].replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    clocks = sampler.stop() if sampler else None
+
+    ms_per_step = ms / args.steps
+    value = world * wbytes * args.steps / (ms * 1e-3) / 1e9
+
+    # ---- per-launch durations of the mul_mat kernel (same calls, event-bracketed, L2-cold copies)
+    per_ms = []
+    with torch.cuda.stream(stream):
+        evs = []
+        for k in range(max(3, min(args.steps, 20))):
+            c = k % copies
+            for i, (ne00, ne01) in enumerate(shapes):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                q4q.q4q_mul_mat(wsets[c][i], ne00, ne01, xs[i], dst=dsts[i], workspace=workspace)
+                b.record(stream)
+                evs.append((i, a, b))
+    torch.cuda.synchronize()
+    for i, a, b in evs:
+        per_ms.append(a.elapsed_time(b))
+    reps = len(per_ms) // nmat
+    kern_ms_per_step = sum(per_ms) / reps
+    act_bytes = sum(4 * k * ne11 for k, n in shapes)
+    out_bytes = sum(4 * n * ne11 for k, n in shapes)
+    alg_bytes_step = wbytes + act_bytes + out_bytes
+    peak, peak_kind = _measured_peaks()
+    achieved = alg_bytes_step / (kern_ms_per_step * 1e-3) / 1e9
+    traffic_step = _profile_traffic("q4q_gemv.cu", "gemv_q4_0_%s.md" % args.workload) if ne11 < 8 else None
+
+    # ---- end to end through the public API with host buffers (pinned), graph-captured
+    xh = torch.empty(act_bytes // 4, dtype=torch.float32).pin_memory()
+    oh = torch.empty(out_bytes // 4, dtype=torch.float32).pin_memory()
+    off = 0
+    for i, (k, n) in enumerate(shapes):
+        xh[off:off + k * ne11].copy_(xs[i].reshape(-1).cpu())
+        off += k * ne11
+    xd = torch.empty_like(xh, device=dev)
+    od = torch.empty_like(oh, device=dev)
+    xviews, oviews = [], []
+    off_x = off_o = 0
+    for (k, n) in shapes:
+        xviews.append(xd[off_x:off_x + k * ne11].view(ne11, k))
+        oviews.append(od[off_o:off_o + n * ne11].view(ne11, n))
+        off_x += k * ne11
+        off_o += n * ne11
+
+    def e2e_step(c):
+        xd.copy_(xh, non_blocking=True)
+        for i, (ne00, ne01) in enumerate(shapes):
+            q4q.q4q_mul_mat(wsets[c][i], ne00, ne01, xviews[i], dst=oviews[i], workspace=workspace)
+        oh.copy_(od, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        e2e_step(0)
+    torch.cuda.synchronize()
+    egraphs = []
+    for c in range(copies):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            e2e_step(c)
+        egraphs.append(g)
+    with torch.cuda.stream(stream):
+        for k in range(args.warmup):
+            egraphs[k % copies].replay()
+    torch.cuda.synchronize()
+    barrier()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for k in range(args.steps):
+            egraphs[k % copies].replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ems = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ems], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ems = float(t.item())
+    e2e_value = world * wbytes * args.steps / (ems * 1e-3) / 1e9
+
+    # ---- CPU baseline: the oracle on this host's cores, bounded sample
+    cpu = cpu_baseline(args.workload, ne11, budget_s=args.cpu_seconds) if (rank == 0 and args.cpu_seconds > 0) else None
+
+    assert q4q.q4q_device_status() == 0, "device-side error recorded during the benchmark"
+    if rank != 0:
+        return None
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "i8",
+        "data": "synthetic",
+        "config": {
+            "workload": args.workload,
+            "description": wl.description,
+            "ne11": ne11,
+            "matrices": nmat,
+            "q4_0_weight_bytes_per_step": wbytes,
+            "l2_policy": "inputs larger than L2: %d rotating copies of the Q4_0 weights (%.0f MB, L2 %.0f MB)" % (
+                copies, copies * wbytes / 1e6, l2 / 1e6),
+            "launch": "one CUDA graph per weight copy, %d q4q_mul_mat calls per step" % nmat,
+            "parallelism": "replicas" if world > 1 else "single GPU",
+        },
+        "gpu_launches": nmat * args.steps,
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "gemv_q4_0_kernel (fused Q8_0 activation quantize + Q4_0 GEMV)" if ne11 < 8 else "mul_mat",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "peak_kind": peak_kind,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": (traffic_step / nmat) if traffic_step else None,
+            "algorithmic_bytes_per_launch": alg_bytes_step / nmat,
+            "avg_launch_us": round(kern_ms_per_step * 1e3 / nmat, 3),
+            "note": "achieved = algorithmic bytes (Q4_0 weights + fp32 activations + fp32 outputs) of the "
+                    "step's launches / their summed CUDA-event durations (each launch bracketed by events, "
+                    "L2-cold weight copies)",
+        },
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": act_bytes,
+                "d2h_bytes_per_step": out_bytes,
+                "how": "CUDA graph per step: pinned-host -> device copy of all activations, %d q4q_mul_mat "
+                       "calls, device -> pinned-host copy of all outputs" % nmat},
+        "weight_quantize": {"gb_per_s_fp32_in": round(quant_in_bytes / (quant_ms * 1e-3) / 1e9, 1),
+                            "ms": round(quant_ms, 3), "note": "q4q_quantize_q4_0 over the set, once, per matrix"},
+        "cpu_baseline": cpu,
+        "clocks": clocks,
+    }
+    return line
+
+
+def cpu_baseline(workload, ne11, budget_s=10.0, reps_min=1):
+    """The oracle (as it stands) on this host's cores, timed on a bounded sample:
+    all matrices of the workload, a seeded subset of rows when the full set would
+    take longer than the budget.  Returns the same metric (weight GB/s)."""
+    import oracle
+    from q4_quantized_matmul_gb300 import workloads
+    wl = workloads.WORKLOADS[workload]
+    threads = os.cpu_count() or 1
+    # prepare the sample: every matrix, rows subsampled to at most `cap` per matrix
+    cap = 4096
+    items = []
+    for i, (ne00, ne01) in enumerate(wl.shapes):
+        if workload == "gpt2_decode_step" and i >= 4 and i < len(wl.shapes) - 1:
+            items.append(items[i % 4])      # the 12 layers repeat 4 shapes; reuse the data
+            continue
+        w, x = workloads.problem(workload, i, ne11)
+        rows = np.arange(ne01) if ne01 <= cap else np.sort(np.random.default_rng(i).choice(ne01, cap, replace=False))
+        wq = oracle.quantize_q4_0(w[rows])
+        items.append((ne00, rows.size, wq, x))
+    done_bytes = 0
+    t0 = time.perf_counter()
+    passes = 0
+    while True:
+        for ne00, nr, wq, x in items:
+            oracle.mul_mat(wq, ne00, nr, x, nthreads=threads, with_scale=False)
+            done_bytes += nr * (ne00 // 32) * 18
+        passes += 1
+        el = time.perf_counter() - t0
+        if passes >= reps_min and el >= budget_s:
+            break
+        if el > 3 * budget_s:
+            break
+    el = time.perf_counter() - t0
+    sampled = sum(nr * (k // 32) for k, nr, _, _ in items) * 18
+    full = _weights_bytes(wl.shapes)
+    return {"value": round(done_bytes / el / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": "%d passes over all %d matrices of %s at %d token(s), rows capped at %d per matrix "
+                      "(%.1f%% of the weight bytes), incl. Q8_0 quantization of the activations; %.1f s wall"
+                      % (passes, len(items), workload, ne11, cap, 100.0 * sampled / full, el)}
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle, as it stands, on this host's cores."""
+    if rank != 0:
+        return None
+    import oracle
+    from q4_quantized_matmul_gb300 import workloads
+    wl = workloads.WORKLOADS[args.workload]
+    ne11 = args.ne11 or wl.ne11[0]
+    threads = os.cpu_count() or 1
+    # one step = the oracle over every matrix of the workload on a seeded row sample
+    frac = 1.0
+    items = []
+    for i, (ne00, ne01) in enumerate(wl.shapes):
+        if args.workload == "gpt2_decode_step" and 4 <= i < len(wl.shapes) - 1:
+            items.append(items[i % 4])
+            continue
+        w, x = workloads.problem(args.workload, i, ne11)
+        items.append((ne00, ne01, oracle.quantize_q4_0(w), x))
+
+    def one_step(fr):
+        nbytes = 0
+        for ne00, ne01, wq, x in items:
+            nr = max(1, int(round(ne01 * fr)))
+            oracle.mul_mat(wq[:nr], ne00, nr, x, nthreads=threads, with_scale=False)
+            nbytes += nr * (ne00 // 32) * 18
+        return nbytes
+
+    t0 = time.perf_counter()
+    one_step(frac)
+    t1 = time.perf_counter() - t0
+    budget = 120.0
+    total_steps = args.steps + args.warmup
+    if t1 * total_steps > budget:
+        frac = max(1e-4, budget / (t1 * total_steps))
+    for _ in range(args.warmup):
+        one_step(frac)
+    t0 = time.perf_counter()
+    nbytes = 0
+    for _ in range(args.steps):
+        nbytes += one_step(frac)
+    el = time.perf_counter() - t0
+    value = nbytes / el / 1e9
+    sample = ("each step: the oracle over all %d matrices of %s at %d token(s), first %.4g%% of each "
+              "matrix's rows, incl. Q8_0 quantization of the activations" % (len(items), args.workload, ne11,
+                                                                             100 * frac))
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(el * 1e3 / args.steps, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "i8",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "ne11": ne11, "matrices": len(items)},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="gpt2_decode_step")
+    ap.add_argument("--ne11", type=int, default=0, help="override the workload's token count")
+    ap.add_argument("--soak", type=float, default=1.5, help="seconds of untimed load before warm-up")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline budget (0 = skip)")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = _env_int("WORLD_SIZE", 1)
+    rank = _env_int("RANK", 0)
+    local_rank = _env_int("LOCAL_RANK", 0)
+
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+
+    import __graft_entry__
+    if rank == 0 or world == 1:
+        __graft_entry__.build()
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+        dist.barrier()
+        if rank != 0:
+            __graft_entry__.build()
+    line = run_ours(args, rank, world, local_rank)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,142 @@
+/*
+ * q4q.h -- C ABI of the GB300 (sm_103a) Q4_0 x Q8_0 quantized matmul library
+ * (libq4q.so).
+ *
+ * The operation is ggml's quantized weight matmul as described in
+ * "llama.cpp 深度解读" (luoboask.github.io):
+ *   §2 "量化数据结构 — Q4_0 格式详解"  -- the 18-byte Q4_0 block and its encode/decode,
+ *   §3 "量化矩阵乘法 — 核心算子"        -- ggml_vec_dot_q4_0_q8_0, with activations
+ *                                         quantized to Q8_0 so that the inner sum is integer.
+ * Operand convention (ggml, ne[0] innermost, all buffers contiguous):
+ *   src0  Q4_0   [ne00, ne01]  ne01 rows of ne00/32 blocks (weights)
+ *   src1  F32    [ne10, ne11]  ne11 rows (tokens) of ne10 = ne00 floats
+ *   dst   F32    [ne01, ne11]  dst[i11 * ne01 + i01]
+ * as in the same page §3 and "ggml GPT-2 117M inference walkthrough"
+ * (aicoding.csdn.net) §3.2 "QKV 线性投影" (c_attn_attn_w [768, 2304] x cur [768, N]
+ * -> [2304, N]).
+ *
+ * Conventions shared by every call:
+ *  - Memory: every pointer is DEVICE memory (cudaMalloc / a torch CUDA tensor)
+ *    owned by the caller.  The library never allocates device memory and never
+ *    frees caller memory; scratch space is passed in as `workspace`.
+ *  - Streams: every call enqueues work on `stream` (a cudaStream_t; NULL = the
+ *    legacy default stream) and returns without synchronizing.  Outputs are
+ *    valid once the stream has reached the call.
+ *  - Errors: argument errors are detected on the host, returned synchronously,
+ *    and nothing is launched.  A failed launch returns Q4Q_ERR_CUDA.  Kernels
+ *    that wait on asynchronous copies bound every wait (about one second); a
+ *    wait that runs out records Q4Q_ERR_TIMEOUT in a device status word that
+ *    q4q_device_status() returns (and clears), and the kernel returns early.
+ *  - Empty problems (ne01 == 0 or ne11 == 0, or nrows == 0) are valid and launch
+ *    nothing.
+ *  - Out of contract (not checked): non-finite inputs, and inputs whose block
+ *    scale overflows fp16 (|x| > 65504 * 8 for Q4_0, 65504 * 127 for Q8_0).
+ *  - Thread safety: calls may be made from several host threads; calls that
+ *    overlap on the GPU must not share output or workspace buffers.
+ */
+#ifndef Q4Q_H
+#define Q4Q_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define Q4Q_API __attribute__((visibility("default")))
+#else
+#define Q4Q_API
+#endif
+
+typedef struct CUstream_st* q4q_stream_t;   /* identical to cudaStream_t */
+
+typedef enum {
+    Q4Q_OK = 0,
+    Q4Q_ERR_NULL = 1,       /* a required pointer is NULL                          */
+    Q4Q_ERR_SHAPE = 2,      /* ne00 <= 0, ne00 % 32 != 0, ne10 != ne00, size < 0,
+                               or a size beyond the documented limits              */
+    Q4Q_ERR_ALIGN = 3,      /* a pointer is not aligned as the call requires       */
+    Q4Q_ERR_WORKSPACE = 4,  /* workspace smaller than q4q_mul_mat_workspace_size   */
+    Q4Q_ERR_CUDA = 5,       /* a CUDA runtime call or kernel launch failed          */
+    Q4Q_ERR_TIMEOUT = 6,    /* a bounded device wait ran out (see q4q_device_status) */
+    Q4Q_ERR_ARG = 7         /* any other invalid argument (e.g. unknown path)       */
+} q4q_status;
+
+#define Q4Q_QK 32                    /* weights per block                          */
+#define Q4Q_BLOCK_Q4_0_BYTES 18      /* fp16 d + 16 bytes of nibbles               */
+#define Q4Q_BLOCK_Q8_0_BYTES 34      /* fp16 d + 32 int8                           */
+
+/* Block layouts (little endian; `d` is the IEEE binary16 bit pattern).
+ * Q4_0 (§2): qs[j] holds element 2j in its low nibble and element 2j+1 in its
+ * high nibble; element value = (nibble - 8) * d.
+ * Q8_0: qs[k] is element k; element value = qs[k] * d. */
+typedef struct { uint16_t d; uint8_t qs[16]; } q4q_block_q4_0;
+typedef struct { uint16_t d; int8_t  qs[32]; } q4q_block_q8_0;
+
+/* Q4_0 encode (§2 "编码过程"): for each 32-element block of each row,
+ *   amax = max |w|, d32 = amax / 8 (fp32, IEEE division),
+ *   q = clamp(round_half_away(w / d32), -8, 7) + 8   (all 8 when d32 == 0),
+ *   qs[j] = q[2j] | q[2j+1] << 4,  d = fp16_round_to_nearest_even(d32).
+ * src: fp32 [nrows][ncols] row-major, device; dst: nrows * ncols/32 blocks
+ * (18 bytes each, contiguous, no padding), device.
+ * Requires ncols > 0, ncols % 32 == 0, nrows >= 0, ncols * nrows < 2^40.
+ * Any alignment is accepted; 16-byte aligned src and dst take the fast path. */
+Q4Q_API q4q_status q4q_quantize_q4_0(const float* src, void* dst, int64_t ncols, int64_t nrows,
+                             q4q_stream_t stream);
+
+/* Q8_0 encode: the same recipe on the signed 8-bit range (the activation side
+ * of §3's dot product; the pages name the type but do not print its encoder):
+ *   d32 = amax / 127, q = clamp(round_half_away(x / d32), -127, 127), d = fp16(d32).
+ * Layout, requirements and alignment as q4q_quantize_q4_0; 34-byte blocks. */
+Q4Q_API q4q_status q4q_quantize_q8_0(const float* src, void* dst, int64_t ncols, int64_t nrows,
+                             q4q_stream_t stream);
+
+/* Bytes of device workspace q4q_mul_mat needs for this problem (0 when the
+ * chosen kernel needs none).  The answer depends only on the shapes and on
+ * the current device; it never exceeds ne11 * (2 * ne00 + 4 * ne00 / 32) + 4096. */
+Q4Q_API q4q_status q4q_mul_mat_workspace_size(int64_t ne00, int64_t ne01, int64_t ne11, size_t* bytes);
+
+/* ggml_mul_mat(src0 Q4_0 [ne00, ne01], src1 F32 [ne10, ne11]) -> dst F32 [ne01, ne11]
+ * (§3): each src1 row is quantized to Q8_0 (as q4q_quantize_q8_0 does), then
+ *   dst[i11*ne01 + i01] = sum_b fp32(d_w[i01,b] * d_x[i11,b]) * isum(i01, i11, b),
+ *   isum = sum_{j<16} (lo_j - 8) * q[2j] + (hi_j - 8) * q[2j+1]   (exact int32).
+ * The block sums are exact; the fp32 sum over blocks may be taken in any order
+ * (results differ from a serial sum by rounding only).
+ * src0: device, 2-byte aligned; src1 / dst: device, 4-byte aligned.
+ * ne11 < 8 streams the weights once through a fused GEMV (no workspace);
+ * ne11 >= 8 runs the tensor-core GEMM, which needs
+ * q4q_mul_mat_workspace_size(...) bytes of 256-byte-aligned workspace.
+ * Limits: 0 < ne00 < 2^20 (ne00 % 32 == 0), 0 <= ne01 < 2^31, 0 <= ne11 < 2^20. */
+Q4Q_API q4q_status q4q_mul_mat(const void* src0, int64_t ne00, int64_t ne01,
+                       const float* src1, int64_t ne10, int64_t ne11,
+                       float* dst, void* workspace, size_t workspace_bytes,
+                       q4q_stream_t stream);
+
+/* Debug: per-block integer sums isum(i01, i11, b) (§3's `sumi`) of Q4_0 weights
+ * and already-quantized Q8_0 activations, computed by the device routine of the
+ * chosen path: path 0 = the GEMV block-dot routine, path 1 = the tensor-core
+ * GEMM (one 32-wide K slab per MMA accumulator).
+ * src0: ne01 rows x ne00/32 Q4_0 blocks; src1_q8_0: ne11 rows x ne00/32 Q8_0
+ * blocks; out: int32 [ne11][ne01][ne00/32].  All device memory.
+ * Path 0 requires ne00 % 64 == 0; path 1 requires ne00 % 256 == 0.
+ * Meant for small shapes (tests); it is not optimized. */
+Q4Q_API q4q_status q4q_debug_block_isums(const void* src0, const void* src1_q8_0,
+                                 int64_t ne00, int64_t ne01, int64_t ne11, int path,
+                                 int32_t* out, q4q_stream_t stream);
+
+/* Synchronizes the device, returns (in *status) the first device-side error
+ * recorded since the last call (Q4Q_OK if none) and clears it. */
+Q4Q_API q4q_status q4q_device_status(q4q_status* status);
+
+/* Static string for a status code. */
+Q4Q_API const char* q4q_status_string(q4q_status status);
+
+/* Library ABI version: (major << 16) | minor. */
+Q4Q_API int q4q_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* Q4Q_H */

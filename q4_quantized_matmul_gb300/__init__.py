@@ -1,0 +1,158 @@
+"""Q4_0 x Q8_0 quantized matmul for GB300 (sm_103a).
+
+A thin binding over the C ABI of libq4q.so (include/q4q.h).  Each function has
+the name of the C entry point it calls and only marshals arguments: torch CUDA
+tensors in, pointers and sizes out, the current torch CUDA stream as the
+stream.  Every step of the computation runs in the library's CUDA kernels.
+
+The operation is ggml_mul_mat(Q4_0 weights, F32 activations) as described in
+"llama.cpp 深度解读" (luoboask.github.io) §2 and §3.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+import torch
+
+from . import _lib
+
+__all__ = [
+    "Q4QError", "q4q_quantize_q4_0", "q4q_quantize_q8_0", "q4q_mul_mat_workspace_size",
+    "q4q_mul_mat", "q4q_debug_block_isums", "q4q_device_status", "q4q_status_string",
+    "q4q_version", "q4_0_row_bytes", "q8_0_row_bytes", "mul_mat_host",
+]
+
+QK = 32
+Q4_0_BYTES = 18
+Q8_0_BYTES = 34
+
+STATUS_NAMES = {0: "Q4Q_OK", 1: "Q4Q_ERR_NULL", 2: "Q4Q_ERR_SHAPE", 3: "Q4Q_ERR_ALIGN",
+                4: "Q4Q_ERR_WORKSPACE", 5: "Q4Q_ERR_CUDA", 6: "Q4Q_ERR_TIMEOUT", 7: "Q4Q_ERR_ARG"}
+
+
+class Q4QError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__("%s failed: %s (%s)" % (fn, STATUS_NAMES.get(status, status), q4q_status_string(status)))
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise Q4QError(fn, status)
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream or None
+    return stream
+
+
+def _dev(t: torch.Tensor, name: str):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def q4_0_row_bytes(ne00: int) -> int:
+    return ne00 // QK * Q4_0_BYTES
+
+
+def q8_0_row_bytes(ne00: int) -> int:
+    return ne00 // QK * Q8_0_BYTES
+
+
+def q4q_version() -> int:
+    return int(_lib.load().q4q_version())
+
+
+def q4q_status_string(status: int) -> str:
+    return _lib.load().q4q_status_string(int(status)).decode()
+
+
+def _quantize(fn: str, src: torch.Tensor, dst: Optional[torch.Tensor], row_bytes, stream):
+    if src.dtype != torch.float32 or src.dim() != 2:
+        raise TypeError("src must be a 2-D float32 tensor")
+    nrows, ncols = src.shape
+    if dst is None:
+        dst = torch.empty((nrows, row_bytes(ncols)), dtype=torch.uint8, device=src.device)
+    _check(fn, getattr(_lib.load(), fn)(_dev(src, "src"), _dev(dst, "dst"), ncols, nrows, _stream(stream)))
+    return dst
+
+
+def q4q_quantize_q4_0(src: torch.Tensor, dst: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """fp32 [nrows, ncols] -> uint8 [nrows, ncols/32*18] Q4_0 blocks."""
+    return _quantize("q4q_quantize_q4_0", src, dst, q4_0_row_bytes, stream)
+
+
+def q4q_quantize_q8_0(src: torch.Tensor, dst: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """fp32 [nrows, ncols] -> uint8 [nrows, ncols/32*34] Q8_0 blocks."""
+    return _quantize("q4q_quantize_q8_0", src, dst, q8_0_row_bytes, stream)
+
+
+def q4q_mul_mat_workspace_size(ne00: int, ne01: int, ne11: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check("q4q_mul_mat_workspace_size", _lib.load().q4q_mul_mat_workspace_size(ne00, ne01, ne11, ctypes.byref(n)))
+    return int(n.value)
+
+
+def q4q_mul_mat(src0: torch.Tensor, ne00: int, ne01: int, src1: torch.Tensor,
+                dst: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                stream=None) -> torch.Tensor:
+    """ggml_mul_mat(Q4_0 src0 [ne00, ne01], F32 src1 [ne00, ne11]) -> F32 [ne11, ne01].
+
+    src0: uint8 CUDA tensor holding ne01 * ne00/32 Q4_0 blocks; src1: float32
+    [ne11, ne00]; dst (optional): float32 [ne11, ne01]; workspace (optional):
+    uint8 tensor of at least q4q_mul_mat_workspace_size(ne00, ne01, ne11) bytes.
+    """
+    if src1.dtype != torch.float32:
+        raise TypeError("src1 must be float32")
+    x = src1.reshape(-1, src1.shape[-1]) if src1.dim() != 2 else src1
+    ne11, ne10 = x.shape
+    if dst is None:
+        dst = torch.empty((ne11, ne01), dtype=torch.float32, device=x.device)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is None:
+        need = q4q_mul_mat_workspace_size(ne00, ne01, ne11) if ne01 * ne11 > 0 else 0
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    if workspace is not None and workspace.numel() > 0:
+        ws_ptr, ws_bytes = _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
+    if ne01 * ne11 == 0:
+        return dst
+    _check("q4q_mul_mat", _lib.load().q4q_mul_mat(_dev(src0, "src0"), ne00, ne01, _dev(x, "src1"), ne10, ne11,
+                                                 _dev(dst, "dst"), ws_ptr, ws_bytes, _stream(stream)))
+    return dst
+
+
+def q4q_debug_block_isums(src0: torch.Tensor, src1_q8_0: torch.Tensor, ne00: int, ne01: int, ne11: int,
+                          path: int = 0, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """int32 [ne11, ne01, ne00/32] per-block integer sums from the device routine of `path`."""
+    if out is None:
+        out = torch.empty((ne11, ne01, ne00 // QK), dtype=torch.int32, device=src0.device)
+    _check("q4q_debug_block_isums",
+           _lib.load().q4q_debug_block_isums(_dev(src0, "src0"), _dev(src1_q8_0, "src1_q8_0"), ne00, ne01, ne11,
+                                             int(path), _dev(out, "out"), _stream(stream)))
+    return out
+
+
+def q4q_device_status() -> int:
+    """Synchronize the device and return (and clear) the device-side status word."""
+    st = ctypes.c_int(0)
+    _check("q4q_device_status", _lib.load().q4q_device_status(ctypes.byref(st)))
+    return int(st.value)
+
+
+def mul_mat_host(src0: torch.Tensor, ne00: int, ne01: int, src1_host: torch.Tensor, dst_host: torch.Tensor,
+                 src1_dev: torch.Tensor, dst_dev: torch.Tensor, workspace: Optional[torch.Tensor] = None,
+                 stream=None) -> torch.Tensor:
+    """q4q_mul_mat with host activations and a host result: pinned host -> device
+    copy of src1, the C-ABI call, device -> pinned host copy of dst, all on one stream."""
+    src1_dev.copy_(src1_host, non_blocking=True)
+    q4q_mul_mat(src0, ne00, ne01, src1_dev, dst=dst_dev, workspace=workspace, stream=stream)
+    dst_host.copy_(dst_dev, non_blocking=True)
+    return dst_host

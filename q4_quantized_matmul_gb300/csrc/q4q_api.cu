@@ -1,0 +1,136 @@
+// q4q_api.cu -- host side of the C ABI: argument checks, path choice, status.
+//
+// ggml_mul_mat(Q4_0 src0 [ne00, ne01], F32 src1 [ne10, ne11]) -> F32 [ne01, ne11]
+// ("llama.cpp 深度解读" §3 "量化矩阵乘法 — 核心算子").  Paths:
+//   ne11 < 8, ne00 % 256 == 0, 16-byte aligned src0/src1  -> fused GEMV (q4q_gemv.cu)
+//   ne11 >= 8 and the tensor-core GEMM accepts the shape    -> q4q_mma.cu
+//   anything else                                           -> generic two-kernel path
+#include <mutex>
+
+#include "q4q_common.cuh"
+#include "q4q_internal.h"
+
+namespace q4q {
+
+namespace {
+constexpr int MAX_DEVICES = 64;
+std::mutex g_info_mutex;
+DeviceInfo g_info[MAX_DEVICES];
+bool g_info_valid[MAX_DEVICES] = {};
+}  // namespace
+
+q4q_status current_device_info(DeviceInfo* info) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return Q4Q_ERR_CUDA;
+    if (dev < 0 || dev >= MAX_DEVICES) return Q4Q_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_info_mutex);
+    if (!g_info_valid[dev]) {
+        DeviceInfo d{};
+        d.device = dev;
+        if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return Q4Q_ERR_CUDA;
+        g_info[dev] = d;
+        g_info_valid[dev] = true;
+    }
+    *info = g_info[dev];
+    return Q4Q_OK;
+}
+
+q4q_status launch_status() {
+    return cudaGetLastError() == cudaSuccess ? Q4Q_OK : Q4Q_ERR_CUDA;
+}
+
+namespace {
+
+q4q_status check_mul_mat_shapes(int64_t ne00, int64_t ne01, int64_t ne10, int64_t ne11) {
+    if (ne00 <= 0 || ne00 % QK != 0 || ne00 >= (1 << 20)) return Q4Q_ERR_SHAPE;
+    if (ne10 != ne00) return Q4Q_ERR_SHAPE;
+    if (ne01 < 0 || ne01 >= (1ll << 31) || ne11 < 0 || ne11 >= (1 << 20)) return Q4Q_ERR_SHAPE;
+    return Q4Q_OK;
+}
+
+}  // namespace
+}  // namespace q4q
+
+using namespace q4q;
+
+extern "C" q4q_status q4q_mul_mat_workspace_size(int64_t ne00, int64_t ne01, int64_t ne11, size_t* bytes) {
+    if (!bytes) return Q4Q_ERR_NULL;
+    q4q_status st = check_mul_mat_shapes(ne00, ne01, ne00, ne11);
+    if (st != Q4Q_OK) return st;
+    size_t need = generic_workspace_bytes(ne00, ne11);
+    if (ne11 >= 8) {
+        DeviceInfo info;
+        if ((st = current_device_info(&info)) != Q4Q_OK) return st;
+        if (mma_supported(ne00, ne01, ne11, info)) need = std::max(need, mma_workspace_bytes(ne00, ne11));
+    }
+    *bytes = need;
+    return Q4Q_OK;
+}
+
+extern "C" q4q_status q4q_mul_mat(const void* src0, int64_t ne00, int64_t ne01,
+                                  const float* src1, int64_t ne10, int64_t ne11,
+                                  float* dst, void* workspace, size_t workspace_bytes,
+                                  q4q_stream_t stream_) {
+    q4q_status st = check_mul_mat_shapes(ne00, ne01, ne10, ne11);
+    if (st != Q4Q_OK) return st;
+    if (ne01 == 0 || ne11 == 0) return Q4Q_OK;
+    if (!src0 || !src1 || !dst) return Q4Q_ERR_NULL;
+    if (!aligned(src0, 2) || !aligned(src1, 4) || !aligned(dst, 4)) return Q4Q_ERR_ALIGN;
+    DeviceInfo info;
+    if ((st = current_device_info(&info)) != Q4Q_OK) return st;
+    cudaStream_t stream = (cudaStream_t)stream_;
+    if (ne11 < 8 && gemv_supported(src0, ne00, ne01, src1, ne11, info))
+        return gemv_mul_mat(src0, ne00, ne01, src1, ne11, dst, stream, info);
+    if (ne11 >= 8 && mma_supported(ne00, ne01, ne11, info) && aligned(src0, 16) && aligned(src1, 16)) {
+        if (workspace_bytes < mma_workspace_bytes(ne00, ne11)) return Q4Q_ERR_WORKSPACE;
+        if (!workspace) return Q4Q_ERR_NULL;
+        if (!aligned(workspace, 256)) return Q4Q_ERR_ALIGN;
+        return mma_mul_mat(src0, ne00, ne01, src1, ne11, dst, workspace, workspace_bytes, stream, info);
+    }
+    return generic_mul_mat(src0, ne00, ne01, src1, ne11, dst, workspace, workspace_bytes, stream, info);
+}
+
+extern "C" q4q_status q4q_debug_block_isums(const void* src0, const void* src1_q8_0,
+                                            int64_t ne00, int64_t ne01, int64_t ne11, int path,
+                                            int32_t* out, q4q_stream_t stream_) {
+    q4q_status st = check_mul_mat_shapes(ne00, ne01, ne00, ne11);
+    if (st != Q4Q_OK) return st;
+    if (path != 0 && path != 1) return Q4Q_ERR_ARG;
+    if (ne01 == 0 || ne11 == 0) return Q4Q_OK;
+    if (!src0 || !src1_q8_0 || !out) return Q4Q_ERR_NULL;
+    if (!aligned(src0, 2) || !aligned(src1_q8_0, 2) || !aligned(out, 4)) return Q4Q_ERR_ALIGN;
+    DeviceInfo info;
+    if ((st = current_device_info(&info)) != Q4Q_OK) return st;
+    cudaStream_t stream = (cudaStream_t)stream_;
+    if (path == 0) return gemv_debug_isums(src0, src1_q8_0, ne00, ne01, ne11, out, stream, info);
+    return mma_debug_isums(src0, src1_q8_0, ne00, ne01, ne11, out, stream, info);
+}
+
+extern "C" q4q_status q4q_device_status(q4q_status* status) {
+    if (!status) return Q4Q_ERR_NULL;
+    if (cudaDeviceSynchronize() != cudaSuccess) return Q4Q_ERR_CUDA;
+    unsigned int a = gemv_take_device_status();
+    unsigned int b = mma_take_device_status();
+    *status = (q4q_status)(a ? a : b);
+    return Q4Q_OK;
+}
+
+extern "C" const char* q4q_status_string(q4q_status s) {
+    switch (s) {
+        case Q4Q_OK: return "ok";
+        case Q4Q_ERR_NULL: return "null pointer";
+        case Q4Q_ERR_SHAPE: return "invalid shape";
+        case Q4Q_ERR_ALIGN: return "misaligned pointer";
+        case Q4Q_ERR_WORKSPACE: return "workspace too small";
+        case Q4Q_ERR_CUDA: return "CUDA error";
+        case Q4Q_ERR_TIMEOUT: return "device wait timed out";
+        case Q4Q_ERR_ARG: return "invalid argument";
+    }
+    return "unknown status";
+}
+
+extern "C" int q4q_version(void) { return (1 << 16) | 0; }

@@ -1,0 +1,133 @@
+// q4q_common.cuh -- device helpers shared by the CUDA kernels of libq4q.
+//
+// Block quantization follows "llama.cpp 深度解读" (luoboask.github.io) §2
+// "量化数据结构 — Q4_0 格式详解": per 32-element block, amax -> fp32 scale ->
+// round(x / scale) -> clamp -> fp16 scale stored.  Rounding is half away from
+// zero (roundf), the division is IEEE (__fdiv_rn), the fp16 store rounds to
+// nearest even (__float2half_rn).  No fast-math anywhere in this library.
+#pragma once
+
+#include <cstdint>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/q4q.h"
+
+namespace q4q {
+
+constexpr int QK = 32;
+constexpr int Q4_0_BYTES = 18;
+constexpr int Q8_0_BYTES = 34;
+
+// device status codes (stored in a per-library status word, first error wins)
+constexpr unsigned int DEV_OK = 0;
+constexpr unsigned int DEV_TIMEOUT = Q4Q_ERR_TIMEOUT;
+
+// ------------------------------------------------------------ quantization --
+
+__device__ __forceinline__ float warp_max4(float v) {
+    // max over the 4 consecutive lanes that hold one 32-element block
+    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+    return v;
+}
+
+__device__ __forceinline__ int warp_sum4(int v) {
+    v += __shfl_xor_sync(0xffffffffu, v, 1);
+    v += __shfl_xor_sync(0xffffffffu, v, 2);
+    return v;
+}
+
+// q = clamp(round_half_away(x / d), lo, hi); 0 when d == 0
+__device__ __forceinline__ int quant_one(float x, float d, float lo, float hi) {
+    if (d == 0.0f) return 0;
+    float r = roundf(__fdiv_rn(x, d));
+    r = fminf(fmaxf(r, lo), hi);
+    return (int)r;
+}
+
+__device__ __forceinline__ uint16_t fp16_bits(float d) {
+    return __half_as_ushort(__float2half_rn(d));
+}
+
+__device__ __forceinline__ float fp16_to_f32(uint32_t bits16) {
+    return __half2float(__ushort_as_half((unsigned short)(bits16 & 0xffffu)));
+}
+
+// Eight consecutive elements of one block -> one 32-bit word of Q4_0 nibbles.
+// Byte j of the block's qs holds element 2j (low) and 2j+1 (high), so the 8
+// elements e = 0..7 of this word land at bit 4e.
+__device__ __forceinline__ uint32_t pack_q4_word(const float (&v)[8], float d) {
+    uint32_t w = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        int q = quant_one(v[e], d, -8.0f, 7.0f) + 8;
+        w |= (uint32_t)q << (4 * e);
+    }
+    return w;
+}
+
+// ------------------------------------------------------------- async copy --
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for phase `parity` of an mbarrier, for at most `limit_ns` nanoseconds.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    uint64_t t0 = global_timer_ns();
+    while (true) {
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// 1-D bulk copy global -> shared (TMA engine), completion counted on `bar`.
+// dst, src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void record_error(unsigned int* word, unsigned int code) {
+    atomicCAS(word, 0u, code);
+}
+
+constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;   // one second
+
+}  // namespace q4q

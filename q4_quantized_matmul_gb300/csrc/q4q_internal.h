@@ -1,0 +1,56 @@
+// q4q_internal.h -- host-side helpers shared by the translation units of libq4q.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/q4q.h"
+
+namespace q4q {
+
+struct DeviceInfo {
+    int device;
+    int sm_count;
+    int max_smem_optin;    // bytes of dynamic shared memory a CTA may opt into
+    int cc_major, cc_minor;
+};
+
+// Cached properties of the current device (queried once per device).
+q4q_status current_device_info(DeviceInfo* info);
+
+// Map the result of the last launch to a status (consumes cudaGetLastError).
+q4q_status launch_status();
+
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// device status words of the translation units that wait on async copies
+unsigned int gemv_take_device_status();
+unsigned int mma_take_device_status();
+
+// tensor-core path (q4q_mma.cu)
+bool mma_supported(int64_t ne00, int64_t ne01, int64_t ne11, const DeviceInfo& info);
+size_t mma_workspace_bytes(int64_t ne00, int64_t ne11);
+q4q_status mma_mul_mat(const void* src0, int64_t ne00, int64_t ne01, const float* src1, int64_t ne11,
+                       float* dst, void* workspace, size_t workspace_bytes, cudaStream_t stream,
+                       const DeviceInfo& info);
+q4q_status mma_debug_isums(const void* src0, const void* src1_q8_0, int64_t ne00, int64_t ne01,
+                           int64_t ne11, int32_t* out, cudaStream_t stream, const DeviceInfo& info);
+
+// GEMV path (q4q_gemv.cu)
+bool gemv_supported(const void* src0, int64_t ne00, int64_t ne01, const float* src1, int64_t ne11,
+                    const DeviceInfo& info);
+q4q_status gemv_mul_mat(const void* src0, int64_t ne00, int64_t ne01, const float* src1, int64_t ne11,
+                        float* dst, cudaStream_t stream, const DeviceInfo& info);
+size_t generic_workspace_bytes(int64_t ne00, int64_t ne11);
+q4q_status generic_mul_mat(const void* src0, int64_t ne00, int64_t ne01, const float* src1, int64_t ne11,
+                           float* dst, void* workspace, size_t workspace_bytes, cudaStream_t stream,
+                           const DeviceInfo& info);
+q4q_status gemv_debug_isums(const void* src0, const void* src1_q8_0, int64_t ne00, int64_t ne01,
+                            int64_t ne11, int32_t* out, cudaStream_t stream, const DeviceInfo& info);
+
+// quantizers (q4q_quant.cu), also used by the GEMM / generic paths
+q4q_status launch_quantize(bool q4, const float* src, void* dst, int64_t ncols, int64_t nrows,
+                           cudaStream_t stream, const DeviceInfo& info);
+
+}  // namespace q4q

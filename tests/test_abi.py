@@ -1,0 +1,109 @@
+"""The C-ABI library builds, loads and exports what include/q4q.h declares (CPU).
+
+Also checks the host-side argument validation, which returns before any CUDA
+call and therefore runs without a GPU.
+"""
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    from q4_quantized_matmul_gb300 import _lib
+    return _lib.load()
+
+
+def test_header_declares_the_boundary():
+    from q4_quantized_matmul_gb300 import _lib
+    names = set(_lib.declared_entry_points())
+    assert {"q4q_quantize_q4_0", "q4q_quantize_q8_0", "q4q_mul_mat", "q4q_mul_mat_workspace_size",
+            "q4q_debug_block_isums", "q4q_device_status", "q4q_status_string", "q4q_version"} <= names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from q4_quantized_matmul_gb300 import _lib
+    out = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    for name in _lib.declared_entry_points():
+        assert name in exported, name
+        assert hasattr(lib, name)
+    # nothing else leaks out under the q4q_ prefix
+    assert {n for n in exported if n.startswith("q4q_")} == set(_lib.declared_entry_points())
+
+
+def test_header_compiles_as_c():
+    src = '#include "q4q.h"\nint main(void){ return (int)sizeof(q4q_block_q4_0) + (int)sizeof(q4q_block_q8_0); }\n'
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        "-x", "c", "-", "-o", "/dev/null"], input=src, text=True, capture_output=True)
+    assert r.returncode == 0, r.stderr
+
+
+def test_block_struct_sizes():
+    src = ('#include "q4q.h"\n#include <stdio.h>\nint main(void){ printf("%d %d", (int)sizeof(q4q_block_q4_0),'
+           ' (int)sizeof(q4q_block_q8_0)); return 0; }\n')
+    exe = "/tmp/q4q_sizes_%d" % os.getpid()
+    subprocess.run(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), "-x", "c", "-", "-o", exe],
+                   input=src, text=True, check=True)
+    try:
+        out = subprocess.run([exe], capture_output=True, text=True, check=True).stdout
+    finally:
+        os.unlink(exe)
+    assert out == "18 34"
+
+
+def test_version_and_strings(lib):
+    assert lib.q4q_version() >> 16 == 1
+    assert lib.q4q_status_string(0) == b"ok"
+    assert lib.q4q_status_string(3) == b"misaligned pointer"
+    assert lib.q4q_status_string(99) == b"unknown status"
+
+
+def test_argument_errors_need_no_gpu(lib):
+    P = ctypes.c_void_p
+    fake = P(0x1000)
+    # ne00 not a multiple of 32
+    assert lib.q4q_mul_mat(fake, 33, 4, fake, 33, 1, fake, None, 0, None) == 2
+    # ne10 != ne00
+    assert lib.q4q_mul_mat(fake, 64, 4, fake, 96, 1, fake, None, 0, None) == 2
+    # negative sizes
+    assert lib.q4q_mul_mat(fake, 64, -1, fake, 64, 1, fake, None, 0, None) == 2
+    assert lib.q4q_mul_mat(fake, 64, 4, fake, 64, -1, fake, None, 0, None) == 2
+    # empty problems are valid and launch nothing
+    assert lib.q4q_mul_mat(None, 64, 0, None, 64, 3, None, None, 0, None) == 0
+    assert lib.q4q_mul_mat(None, 64, 5, None, 64, 0, None, None, 0, None) == 0
+    # null pointers
+    assert lib.q4q_mul_mat(None, 64, 4, fake, 64, 1, fake, None, 0, None) == 1
+    assert lib.q4q_mul_mat(fake, 64, 4, fake, 64, 1, None, None, 0, None) == 1
+    # misaligned pointers
+    assert lib.q4q_mul_mat(P(0x1001), 64, 4, fake, 64, 1, fake, None, 0, None) == 3
+    assert lib.q4q_mul_mat(fake, 64, 4, P(0x1002), 64, 1, fake, None, 0, None) == 3
+    # quantizers
+    assert lib.q4q_quantize_q4_0(fake, fake, 31, 2, None) == 2
+    assert lib.q4q_quantize_q8_0(fake, fake, 0, 2, None) == 2
+    assert lib.q4q_quantize_q4_0(fake, fake, 32, 0, None) == 0
+    assert lib.q4q_quantize_q4_0(None, fake, 32, 1, None) == 1
+    assert lib.q4q_quantize_q8_0(P(0x1002), fake, 32, 1, None) == 3
+    # debug entry
+    assert lib.q4q_debug_block_isums(fake, fake, 64, 2, 1, 5, fake, None) == 7
+    assert lib.q4q_debug_block_isums(fake, fake, 64, 0, 1, 0, fake, None) == 0
+    # workspace query
+    n = ctypes.c_size_t(123)
+    assert lib.q4q_mul_mat_workspace_size(64, 4, 1, None) == 1
+    assert lib.q4q_mul_mat_workspace_size(48, 4, 1, ctypes.byref(n)) == 2
+    assert lib.q4q_mul_mat_workspace_size(64, 4, 3, ctypes.byref(n)) == 0
+    assert n.value == 3 * 2 * 34
+
+
+def test_binding_fails_loudly_without_cuda_tensors(lib):
+    import torch
+    import q4_quantized_matmul_gb300 as q4q
+    with pytest.raises(TypeError):
+        q4q.q4q_quantize_q4_0(torch.zeros(2, 32))

@@ -1,0 +1,239 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Bit-exact: every Q4_0 / Q8_0 byte and every per-block int32 sum.
+Outputs: |gpu - oracle| <= 1e-5 * sum_b |fp32(d_w d_x) isum_b| per element,
+exactly zero where that sum is zero.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from q4_quantized_matmul_gb300 import workloads
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-5
+
+
+@pytest.fixture(scope="module")
+def q4q():
+    import __graft_entry__
+    __graft_entry__.build()
+    import q4_quantized_matmul_gb300 as m
+    assert torch.cuda.is_available(), "GPU tests need CUDA"
+    torch.cuda.set_device(0)
+    return m
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def assert_close(got, ref, scale):
+    got = np.asarray(got, dtype=np.float32)
+    assert got.shape == ref.shape
+    err = np.abs(got.astype(np.float64) - ref.astype(np.float64))
+    bad = err > TOL * scale
+    assert not bad.any(), "%d of %d outside tolerance; worst err %g at scale %g" % (
+        bad.sum(), bad.size, err[bad].max(), scale[bad][np.argmax(err[bad])])
+    zero = scale == 0
+    assert np.all(got[zero] == 0)
+
+
+def _special_weights(rng, ne01, ne00):
+    w = (rng.standard_normal((ne01, ne00)) * 0.02).astype(np.float32)
+    blocks = w.reshape(-1, 32)
+    nb = blocks.shape[0]
+    blocks[rng.integers(0, nb, size=max(1, nb // 10))] = 0.0                     # d = 0
+    c = rng.integers(0, nb, size=max(1, nb // 10))
+    blocks[c] = blocks[c, :1]                                                    # constant
+    t = rng.integers(0, nb, size=max(1, nb // 10))
+    k = rng.integers(-16, 16, size=(t.size, 32)).astype(np.float32)
+    k[:, 0] = -16.0
+    blocks[t] = k * np.float32(0.125) / 2                                         # exact .5 ties
+    return w
+
+
+# ---------------------------------------------------------------- quantizers --
+
+@pytest.mark.parametrize("nrows,ncols", [(1, 32), (5, 96), (3, 768), (37, 4096), (2304, 768), (11, 14336)])
+@pytest.mark.parametrize("kind", ["q4_0", "q8_0"])
+def test_quantize_bit_exact(q4q, nrows, ncols, kind):
+    rng = np.random.default_rng([nrows, ncols])
+    w = _special_weights(rng, nrows, ncols)
+    if kind == "q8_0":
+        w = w * np.float32(50.0)
+    fn = q4q.q4q_quantize_q4_0 if kind == "q4_0" else q4q.q4q_quantize_q8_0
+    ref = oracle.quantize_q4_0(w) if kind == "q4_0" else oracle.quantize_q8_0(w)
+    got = fn(dev(w)).cpu().numpy()
+    np.testing.assert_array_equal(got, ref)
+
+
+@pytest.mark.parametrize("kind", ["q4_0", "q8_0"])
+def test_quantize_misaligned_buffers(q4q, kind):
+    # src offset by one float, dst by one byte: the generic (scalar) kernel
+    rng = np.random.default_rng(77)
+    nrows, ncols = 9, 320
+    w = _special_weights(rng, nrows, ncols)
+    src = torch.zeros(nrows * ncols + 1, dtype=torch.float32, device="cuda")
+    src[1:] = dev(w.reshape(-1))
+    bpr = ncols // 32 * (18 if kind == "q4_0" else 34)
+    dst = torch.zeros(nrows * bpr + 1, dtype=torch.uint8, device="cuda")
+    lib = q4q._lib.load()
+    fn = lib.q4q_quantize_q4_0 if kind == "q4_0" else lib.q4q_quantize_q8_0
+    import ctypes
+    st = fn(ctypes.c_void_p(src.data_ptr() + 4), ctypes.c_void_p(dst.data_ptr() + 1), ncols, nrows,
+            ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0
+    ref = oracle.quantize_q4_0(w) if kind == "q4_0" else oracle.quantize_q8_0(w)
+    np.testing.assert_array_equal(dst[1:].cpu().numpy().reshape(nrows, bpr), ref)
+    assert dst[0].item() == 0
+
+
+def test_quantize_hand_block(q4q):
+    w = ((np.arange(32) - 16) * 0.25).astype(np.float32).reshape(1, 32)
+    got = q4q.q4q_quantize_q4_0(dev(w)).cpu().numpy()
+    assert bytes(got[0]) == bytes.fromhex("0038001122334455667798a9bacbdcedfeff")
+
+
+# ------------------------------------------------------------ block int sums --
+
+@pytest.mark.parametrize("ne00,ne01,ne11", [(64, 1, 1), (256, 5, 3), (768, 37, 2), (4096, 9, 1), (160 * 2, 4, 4)])
+def test_block_isums_gemv_routine(q4q, ne00, ne01, ne11):
+    rng = np.random.default_rng([ne00, ne01, ne11, 1])
+    w = _special_weights(rng, ne01, ne00)
+    x = rng.standard_normal((ne11, ne00)).astype(np.float32)
+    x[:, ::7] *= 30
+    wq = oracle.quantize_q4_0(w)
+    xq = oracle.quantize_q8_0(x)
+    ref = oracle.block_isums(wq, xq, ne00, ne01, ne11)
+    got = q4q.q4q_debug_block_isums(dev(wq), dev(xq), ne00, ne01, ne11, path=0).cpu().numpy()
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_block_isums_extremes(q4q):
+    # nibble 0 (-8) against -127 and nibble 15 (+7) against +127 in every position
+    ne00, ne01, ne11 = 64, 2, 2
+    wq = np.zeros((ne01, 2 * 18), np.uint8)
+    wq[0, 2:18] = 0x00
+    wq[0, 20:36] = 0xFF
+    wq[1, 2:18] = 0xF0
+    wq[1, 20:36] = 0x0F
+    xq = np.zeros((ne11, 2 * 34), np.uint8)
+    xq[0, 2:34] = np.int8(-127).view(np.uint8)
+    xq[0, 36:68] = np.int8(127).view(np.uint8)
+    xq[1, 2:34] = np.int8(127).view(np.uint8)
+    xq[1, 36:68] = np.int8(-127).view(np.uint8)
+    ref = oracle.block_isums(wq, xq, ne00, ne01, ne11)
+    assert ref[0, 0, 0] == 32 * 8 * 127
+    got = q4q.q4q_debug_block_isums(dev(wq), dev(xq), ne00, ne01, ne11, path=0).cpu().numpy()
+    np.testing.assert_array_equal(got, ref)
+
+
+# ------------------------------------------------------------------- mul_mat --
+
+GEMV_SHAPES = [(256, 1), (256, 3), (768, 2304), (768, 1000), (3072, 768), (4096, 1024), (14336, 64),
+               (512, 33), (1024, 4099)]
+
+
+@pytest.mark.parametrize("ne00,ne01", GEMV_SHAPES)
+@pytest.mark.parametrize("ne11", [1, 2, 7])
+def test_mul_mat_gemv(q4q, ne00, ne01, ne11):
+    rng = np.random.default_rng([ne00, ne01, ne11, 2])
+    w = _special_weights(rng, ne01, ne00)
+    x = rng.standard_normal((ne11, ne00)).astype(np.float32)
+    wq_d = q4q.q4q_quantize_q4_0(dev(w))
+    got = q4q.q4q_mul_mat(wq_d, ne00, ne01, dev(x)).cpu().numpy()
+    ref, scale = oracle.mul_mat(oracle.quantize_q4_0(w), ne00, ne01, x, nthreads=8)
+    assert_close(got, ref, scale)
+
+
+@pytest.mark.parametrize("ne00,ne01,ne11", [(32, 3, 1), (96, 17, 2), (800, 65, 5), (160, 40, 9), (256, 70, 8),
+                                            (768, 130, 17), (4096, 64, 16)])
+def test_mul_mat_other_paths(q4q, ne00, ne01, ne11):
+    # ne00 % 256 != 0 (generic path) and ne11 >= 8 (GEMM path where it applies)
+    rng = np.random.default_rng([ne00, ne01, ne11, 3])
+    w = _special_weights(rng, ne01, ne00)
+    x = rng.standard_normal((ne11, ne00)).astype(np.float32)
+    got = q4q.q4q_mul_mat(q4q.q4q_quantize_q4_0(dev(w)), ne00, ne01, dev(x)).cpu().numpy()
+    ref, scale = oracle.mul_mat(oracle.quantize_q4_0(w), ne00, ne01, x, nthreads=8)
+    assert_close(got, ref, scale)
+
+
+def test_mul_mat_misaligned_weights_take_generic_path(q4q):
+    ne00, ne01, ne11 = 512, 40, 1
+    rng = np.random.default_rng(5)
+    w = _special_weights(rng, ne01, ne00)
+    x = rng.standard_normal((ne11, ne00)).astype(np.float32)
+    wq = oracle.quantize_q4_0(w)
+    buf = torch.zeros(wq.size + 2, dtype=torch.uint8, device="cuda")
+    buf[2:] = dev(wq.reshape(-1))
+    src0 = buf[2:]
+    assert src0.data_ptr() % 16 != 0
+    got = q4q.q4q_mul_mat(src0, ne00, ne01, dev(x)).cpu().numpy()
+    ref, scale = oracle.mul_mat(wq, ne00, ne01, x)
+    assert_close(got, ref, scale)
+
+
+def test_mul_mat_zero_rows_and_tokens(q4q):
+    ne00, ne01, ne11 = 1024, 50, 3
+    rng = np.random.default_rng(6)
+    w = _special_weights(rng, ne01, ne00)
+    w[7] = 0.0
+    x = rng.standard_normal((ne11, ne00)).astype(np.float32)
+    x[1] = 0.0
+    got = q4q.q4q_mul_mat(q4q.q4q_quantize_q4_0(dev(w)), ne00, ne01, dev(x)).cpu().numpy()
+    ref, scale = oracle.mul_mat(oracle.quantize_q4_0(w), ne00, ne01, x)
+    assert np.all(got[1] == 0) and np.all(got[:, 7] == 0)
+    assert_close(got, ref, scale)
+
+
+def test_mul_mat_hand_block(q4q):
+    w = ((np.arange(32) - 16) * 0.25).astype(np.float32)
+    w = np.tile(w, 8).reshape(1, 256)
+    x = np.ones((1, 256), np.float32)
+    got = q4q.q4q_mul_mat(q4q.q4q_quantize_q4_0(dev(w)), 256, 1, dev(x)).cpu().numpy()
+    assert got[0, 0] == np.float32(8 * -4.499725341796875)
+
+
+def test_mul_mat_empty(q4q):
+    wq = torch.zeros(18 * 8, dtype=torch.uint8, device="cuda")
+    out = q4q.q4q_mul_mat(wq, 256, 0, torch.zeros(3, 256, device="cuda"))
+    assert out.shape == (3, 0)
+    out = q4q.q4q_mul_mat(wq, 256, 1, torch.zeros(0, 256, device="cuda"))
+    assert out.shape == (0, 1)
+
+
+def test_no_device_errors_recorded(q4q):
+    assert q4q.q4q_device_status() == 0
+
+
+# ---------------------------------------------------- full-size workloads ----
+
+def _sample_rows(ne01, n, seed):
+    rng = np.random.default_rng(seed)
+    rows = np.unique(np.concatenate([rng.choice(ne01, size=min(n, ne01), replace=False), [0, ne01 - 1]]))
+    return rows
+
+
+@pytest.mark.parametrize("name", ["gpt2_c_attn_1tok", "gpt2_decode_step", "llama3_8b_decode"])
+def test_full_size_decode_workloads(q4q, name):
+    """Every distinct matrix of the workload at full size, in the launch
+    configuration the benchmark times: Q4_0 bytes bit-exact and outputs within
+    tolerance on up to 4096 sampled rows (plus the first and last) for every token."""
+    wl = workloads.WORKLOADS[name]
+    seen = set()
+    for i, (ne00, ne01) in enumerate(wl.shapes):
+        if name == "gpt2_decode_step" and (ne00, ne01) in seen:
+            continue           # the 12 layers repeat 4 shapes; one of each + lm_head
+        seen.add((ne00, ne01))
+        w, x = workloads.problem(name, i)
+        wq_d = q4q.q4q_quantize_q4_0(dev(w))
+        got = q4q.q4q_mul_mat(wq_d, ne00, ne01, dev(x)).cpu().numpy()
+        rows = _sample_rows(ne01, 4096, i)
+        wq_rows = oracle.quantize_q4_0(w[rows])
+        np.testing.assert_array_equal(wq_d.view(ne01, -1)[torch.from_numpy(rows).cuda()].cpu().numpy(), wq_rows)
+        ref, scale = oracle.mul_mat(wq_rows, ne00, rows.size, x, nthreads=8)
+        assert_close(got[:, rows], ref, scale)
+    assert q4q.q4q_device_status() == 0
