@@ -114,17 +114,39 @@ Q4Q_API q4q_status q4q_mul_mat(const void* src0, int64_t ne00, int64_t ne01,
                        float* dst, void* workspace, size_t workspace_bytes,
                        q4q_stream_t stream);
 
+/* Bytes of workspace q4q_debug_block_isums needs for `path` (0 for path 0). */
+Q4Q_API q4q_status q4q_debug_workspace_size(int64_t ne00, int64_t ne11, int path, size_t* bytes);
+
+/* Launch flags of q4q_mul_mat_ex. */
+#define Q4Q_MUL_MAT_PDL 1u   /* programmatic dependent launch (see below) */
+
+/* q4q_mul_mat with launch flags (0 = exactly q4q_mul_mat).
+ * Q4Q_MUL_MAT_PDL: the kernel is launched with programmatic dependent launch, so
+ * that it can be scheduled, set up and start streaming src0 while the work queued
+ * before it on `stream` is still running; it waits for that work to complete
+ * before it reads src1 or writes dst.  Valid only when no work still in flight on
+ * the stream writes src0 (true for resident model weights).  Used by chains of
+ * decode-step projections; honoured by the ne11 < 8 path, ignored by the others. */
+Q4Q_API q4q_status q4q_mul_mat_ex(const void* src0, int64_t ne00, int64_t ne01,
+                          const float* src1, int64_t ne10, int64_t ne11,
+                          float* dst, void* workspace, size_t workspace_bytes,
+                          unsigned int flags, q4q_stream_t stream);
+
 /* Debug: per-block integer sums isum(i01, i11, b) (§3's `sumi`) of Q4_0 weights
  * and already-quantized Q8_0 activations, computed by the device routine of the
- * chosen path: path 0 = the GEMV block-dot routine, path 1 = the tensor-core
- * GEMM (one 32-wide K slab per MMA accumulator).
+ * chosen path: path 0 = the GEMV block-dot routine (dp4a on nibble words),
+ * path 1 = the tensor-core GEMM (one 32-wide K block per fresh TMEM accumulator,
+ * read back exactly as fp32 and converted to int32).
  * src0: ne01 rows x ne00/32 Q4_0 blocks; src1_q8_0: ne11 rows x ne00/32 Q8_0
  * blocks; out: int32 [ne11][ne01][ne00/32].  All device memory.
- * Path 0 requires ne00 % 64 == 0; path 1 requires ne00 % 256 == 0.
+ * Path 0 requires ne00 % 64 == 0 and 2-byte aligned inputs; path 1 requires
+ * ne00 % 256 == 0, a 16-byte aligned src0 and q4q_debug_workspace_size bytes of
+ * 256-byte aligned workspace (path 0 ignores workspace).
  * Meant for small shapes (tests); it is not optimized. */
 Q4Q_API q4q_status q4q_debug_block_isums(const void* src0, const void* src1_q8_0,
                                  int64_t ne00, int64_t ne01, int64_t ne11, int path,
-                                 int32_t* out, q4q_stream_t stream);
+                                 int32_t* out, void* workspace, size_t workspace_bytes,
+                                 q4q_stream_t stream);
 
 /* Synchronizes the device, returns (in *status) the first device-side error
  * recorded since the last call (Q4Q_OK if none) and clears it. */

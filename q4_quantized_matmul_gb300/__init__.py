@@ -19,7 +19,7 @@ from . import _lib
 
 __all__ = [
     "Q4QError", "q4q_quantize_q4_0", "q4q_quantize_q8_0", "q4q_mul_mat_workspace_size",
-    "q4q_mul_mat", "q4q_debug_block_isums", "q4q_device_status", "q4q_status_string",
+    "q4q_mul_mat", "q4q_debug_block_isums", "q4q_debug_workspace_size", "Q4Q_MUL_MAT_PDL", "q4q_device_status", "q4q_status_string",
     "q4q_version", "q4_0_row_bytes", "q8_0_row_bytes", "mul_mat_host",
 ]
 
@@ -102,12 +102,13 @@ def q4q_mul_mat_workspace_size(ne00: int, ne01: int, ne11: int) -> int:
 
 def q4q_mul_mat(src0: torch.Tensor, ne00: int, ne01: int, src1: torch.Tensor,
                 dst: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-                stream=None) -> torch.Tensor:
+                stream=None, flags: int = 0) -> torch.Tensor:
     """ggml_mul_mat(Q4_0 src0 [ne00, ne01], F32 src1 [ne00, ne11]) -> F32 [ne11, ne01].
 
     src0: uint8 CUDA tensor holding ne01 * ne00/32 Q4_0 blocks; src1: float32
     [ne11, ne00]; dst (optional): float32 [ne11, ne01]; workspace (optional):
     uint8 tensor of at least q4q_mul_mat_workspace_size(ne00, ne01, ne11) bytes.
+    flags != 0 calls q4q_mul_mat_ex (Q4Q_MUL_MAT_PDL = 1).
     """
     if src1.dtype != torch.float32:
         raise TypeError("src1 must be float32")
@@ -124,19 +125,39 @@ def q4q_mul_mat(src0: torch.Tensor, ne00: int, ne01: int, src1: torch.Tensor,
         ws_ptr, ws_bytes = _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
     if ne01 * ne11 == 0:
         return dst
-    _check("q4q_mul_mat", _lib.load().q4q_mul_mat(_dev(src0, "src0"), ne00, ne01, _dev(x, "src1"), ne10, ne11,
-                                                 _dev(dst, "dst"), ws_ptr, ws_bytes, _stream(stream)))
+    lib = _lib.load()
+    if flags:
+        _check("q4q_mul_mat_ex", lib.q4q_mul_mat_ex(_dev(src0, "src0"), ne00, ne01, _dev(x, "src1"), ne10, ne11,
+                                                   _dev(dst, "dst"), ws_ptr, ws_bytes, int(flags), _stream(stream)))
+    else:
+        _check("q4q_mul_mat", lib.q4q_mul_mat(_dev(src0, "src0"), ne00, ne01, _dev(x, "src1"), ne10, ne11,
+                                             _dev(dst, "dst"), ws_ptr, ws_bytes, _stream(stream)))
     return dst
 
 
+Q4Q_MUL_MAT_PDL = 1
+
+
+def q4q_debug_workspace_size(ne00: int, ne11: int, path: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check("q4q_debug_workspace_size", _lib.load().q4q_debug_workspace_size(ne00, ne11, int(path), ctypes.byref(n)))
+    return int(n.value)
+
+
 def q4q_debug_block_isums(src0: torch.Tensor, src1_q8_0: torch.Tensor, ne00: int, ne01: int, ne11: int,
-                          path: int = 0, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+                          path: int = 0, out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                          stream=None) -> torch.Tensor:
     """int32 [ne11, ne01, ne00/32] per-block integer sums from the device routine of `path`."""
     if out is None:
         out = torch.empty((ne11, ne01, ne00 // QK), dtype=torch.int32, device=src0.device)
+    need = q4q_debug_workspace_size(ne00, ne11, path)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=src0.device)
+    ws_ptr = _dev(workspace, "workspace") if workspace is not None else None
+    ws_bytes = workspace.numel() if workspace is not None else 0
     _check("q4q_debug_block_isums",
            _lib.load().q4q_debug_block_isums(_dev(src0, "src0"), _dev(src1_q8_0, "src1_q8_0"), ne00, ne01, ne11,
-                                             int(path), _dev(out, "out"), _stream(stream)))
+                                             int(path), _dev(out, "out"), ws_ptr, ws_bytes, _stream(stream)))
     return out
 
 

@@ -75,6 +75,14 @@ extern "C" q4q_status q4q_mul_mat(const void* src0, int64_t ne00, int64_t ne01,
                                   const float* src1, int64_t ne10, int64_t ne11,
                                   float* dst, void* workspace, size_t workspace_bytes,
                                   q4q_stream_t stream_) {
+    return q4q_mul_mat_ex(src0, ne00, ne01, src1, ne10, ne11, dst, workspace, workspace_bytes, 0u, stream_);
+}
+
+extern "C" q4q_status q4q_mul_mat_ex(const void* src0, int64_t ne00, int64_t ne01,
+                                     const float* src1, int64_t ne10, int64_t ne11,
+                                     float* dst, void* workspace, size_t workspace_bytes,
+                                     unsigned int flags, q4q_stream_t stream_) {
+    if (flags & ~Q4Q_MUL_MAT_PDL) return Q4Q_ERR_ARG;
     q4q_status st = check_mul_mat_shapes(ne00, ne01, ne10, ne11);
     if (st != Q4Q_OK) return st;
     if (ne01 == 0 || ne11 == 0) return Q4Q_OK;
@@ -84,7 +92,7 @@ extern "C" q4q_status q4q_mul_mat(const void* src0, int64_t ne00, int64_t ne01,
     if ((st = current_device_info(&info)) != Q4Q_OK) return st;
     cudaStream_t stream = (cudaStream_t)stream_;
     if (ne11 < 8 && gemv_supported(src0, ne00, ne01, src1, ne11, info))
-        return gemv_mul_mat(src0, ne00, ne01, src1, ne11, dst, stream, info);
+        return gemv_mul_mat(src0, ne00, ne01, src1, ne11, dst, stream, info, (flags & Q4Q_MUL_MAT_PDL) != 0);
     if (ne11 >= 8 && mma_supported(ne00, ne01, ne11, info) && aligned(src0, 16) && aligned(src1, 16)) {
         if (workspace_bytes < mma_workspace_bytes(ne00, ne11)) return Q4Q_ERR_WORKSPACE;
         if (!workspace) return Q4Q_ERR_NULL;
@@ -94,9 +102,18 @@ extern "C" q4q_status q4q_mul_mat(const void* src0, int64_t ne00, int64_t ne01,
     return generic_mul_mat(src0, ne00, ne01, src1, ne11, dst, workspace, workspace_bytes, stream, info);
 }
 
+extern "C" q4q_status q4q_debug_workspace_size(int64_t ne00, int64_t ne11, int path, size_t* bytes) {
+    if (!bytes) return Q4Q_ERR_NULL;
+    if (ne00 <= 0 || ne00 % QK != 0 || ne00 >= (1 << 20) || ne11 < 0 || ne11 >= (1 << 20)) return Q4Q_ERR_SHAPE;
+    if (path != 0 && path != 1) return Q4Q_ERR_ARG;
+    *bytes = path == 0 ? 0 : mma_workspace_bytes(ne00, ne11);
+    return Q4Q_OK;
+}
+
 extern "C" q4q_status q4q_debug_block_isums(const void* src0, const void* src1_q8_0,
                                             int64_t ne00, int64_t ne01, int64_t ne11, int path,
-                                            int32_t* out, q4q_stream_t stream_) {
+                                            int32_t* out, void* workspace, size_t workspace_bytes,
+                                            q4q_stream_t stream_) {
     q4q_status st = check_mul_mat_shapes(ne00, ne01, ne00, ne11);
     if (st != Q4Q_OK) return st;
     if (path != 0 && path != 1) return Q4Q_ERR_ARG;
@@ -107,7 +124,7 @@ extern "C" q4q_status q4q_debug_block_isums(const void* src0, const void* src1_q
     if ((st = current_device_info(&info)) != Q4Q_OK) return st;
     cudaStream_t stream = (cudaStream_t)stream_;
     if (path == 0) return gemv_debug_isums(src0, src1_q8_0, ne00, ne01, ne11, out, stream, info);
-    return mma_debug_isums(src0, src1_q8_0, ne00, ne01, ne11, out, stream, info);
+    return mma_debug_isums(src0, src1_q8_0, ne00, ne01, ne11, out, workspace, workspace_bytes, stream, info);
 }
 
 extern "C" q4q_status q4q_device_status(q4q_status* status) {

@@ -32,8 +32,10 @@ namespace {
 
 __device__ unsigned int g_gemv_status = 0;
 
-constexpr int THREADS = 256;
+constexpr int THREADS = 288;            // 8 consumer warps + 1 producer warp
+constexpr int CONSUMERS = 256;
 constexpr int MAX_STAGES = 8;
+constexpr int PLAIN_THREADS = 256;      // generic and debug kernels
 
 struct GemvParams {
     int ne00, nb, np, ne01, row_bytes;
@@ -94,46 +96,120 @@ __device__ __forceinline__ int quant_q8_split(const float (&v)[8], float d, uint
     return s;
 }
 
-template <int T, int LPR>
-__global__ void __launch_bounds__(THREADS)
+// Activations of one block pair in the quad layout (+ scales and 8 * sum(q)).
+struct PairActs {
+    uint4 ea, oa, eb, ob;
+    float2 d;
+    int2 s8;
+};
+
+__device__ __forceinline__ PairActs load_pair_acts(const uint4* quads, const float* dy, const int* sy8, int np,
+                                                   int nb, int t, int pr) {
+    PairActs a;
+    const uint4* qp = quads + (t * 4) * np + pr;
+    a.ea = qp[0];
+    a.oa = qp[np];
+    a.eb = qp[2 * np];
+    a.ob = qp[3 * np];
+    a.d = reinterpret_cast<const float2*>(dy + t * nb)[pr];
+    a.s8 = reinterpret_cast<const int2*>(sy8 + t * nb)[pr];
+    return a;
+}
+
+__device__ __forceinline__ float pair_dot(const uint8_t* rowp, int pr, const PairActs& a, float acc) {
+    const uint32_t* wp = reinterpret_cast<const uint32_t*>(rowp + 36 * pr);
+    uint32_t wv[9];
+#pragma unroll
+    for (int i = 0; i < 9; ++i) wv[i] = wp[i];
+    const PairWeights pw = unpack_pair(wv);
+    const int ia = block_dot(pw.qa, a.ea, a.oa) - a.s8.x;
+    const int ib = block_dot(pw.qb, a.eb, a.ob) - a.s8.y;
+    acc = fmaf(pw.da * a.d.x, (float)ia, acc);
+    acc = fmaf(pw.db * a.d.y, (float)ib, acc);
+    return acc;
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+__device__ __forceinline__ void consumer_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(CONSUMERS) : "memory");
+}
+
+// T tokens; LPR lanes per row; PPL > 0: the lane's PPL block pairs of activations
+// are held in registers for the whole kernel (T == 1), PPL == 0: read from shared
+// memory for every row.
+template <int T, int LPR, int PPL>
+__global__ void __launch_bounds__(THREADS, (PPL > 0 && PPL <= 3) ? 2 : 1)
 gemv_q4_0_kernel(const uint8_t* __restrict__ w, const float* __restrict__ x, float* __restrict__ dst,
                  const GemvParams p) {
+    static_assert(PPL == 0 || T == 1, "register-resident activations are for one token");
     extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ int s_ok;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);              // full[0..7], empty[8..15]
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 128);
     uint4* quads = reinterpret_cast<uint4*>(smem + p.act_off);
     float* dy = reinterpret_cast<float*>(smem + p.dy_off);
     int* sy8 = reinterpret_cast<int*>(smem + p.sy_off);
     uint8_t* stages = smem + p.stage_off;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int grid = gridDim.x;
-
-    auto issue = [&](int unit, int s) {
-        const int r0 = unit * p.G;
-        const int nr = min(p.G, p.ne01 - r0);
-        const uint32_t bytes = (uint32_t)nr * (uint32_t)p.row_bytes;
-        const uint32_t bar = smem_u32(&bars[s]);
-        mbar_arrive_expect_tx(bar, bytes);
-        bulk_g2s(smem_u32(stages + (size_t)s * p.stage_bytes), w + (int64_t)r0 * p.row_bytes, bytes, bar);
-    };
+    const uint32_t full0 = smem_u32(&bars[0]), empty0 = smem_u32(&bars[MAX_STAGES]);
 
     if (tid == 0) {
-        for (int s = 0; s < p.S; ++s) mbar_init(smem_u32(&bars[s]), 1);
+        for (int s = 0; s < p.S; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, CONSUMERS / 32);
+        }
+        *abort_flag = 0;
         fence_mbar_init();
     }
     __syncthreads();
-    if (tid == 0) {
-        for (int s = 0; s < p.S; ++s) {
-            const int u = blockIdx.x + s * grid;
-            if (u < p.n_units) issue(u, s);
+    // the next kernel on the stream may start its own set-up now; it still waits
+    // for this grid to finish before it touches memory this grid writes
+    pdl_trigger();
+
+    if (warp == CONSUMERS / 32) {
+        // ---------------- producer: stream weight units through the ring
+        if (lane == 0) {
+            int k = 0;
+            for (int u = blockIdx.x; u < p.n_units; u += grid, ++k) {
+                const int s = k % p.S;
+                if (k >= p.S) {
+                    const uint32_t bar = empty0 + 8 * s, par = ((k / p.S) + 1) & 1;
+                    bool ok = mbar_try_wait(bar, par);
+                    if (!ok) {
+                        const uint64_t t0 = global_timer_ns();
+                        while (!ok && !*abort_flag && global_timer_ns() - t0 < WAIT_LIMIT_NS)
+                            for (int i = 0; i < 32 && !ok; ++i) ok = mbar_try_wait(bar, par);
+                    }
+                    if (!ok) {
+                        if (!*abort_flag) record_error(&g_gemv_status, DEV_TIMEOUT);
+                        *abort_flag = 1;
+                        break;
+                    }
+                }
+                const int r0 = u * p.G;
+                const int nr = min(p.G, p.ne01 - r0);
+                const uint32_t bytes = (uint32_t)nr * (uint32_t)p.row_bytes;
+                mbar_arrive_expect_tx(full0 + 8 * s, bytes);
+                bulk_g2s(smem_u32(stages + (size_t)s * p.stage_bytes), w + (int64_t)r0 * p.row_bytes, bytes,
+                         full0 + 8 * s);
+            }
+            if (*abort_flag) {
+                // let the copies still in flight land before the CTA exits
+                for (int k2 = max(0, k - p.S); k2 < k; ++k2)
+                    mbar_wait_bounded(full0 + 8 * (k2 % p.S), (uint32_t)((k2 / p.S) & 1), WAIT_LIMIT_NS);
+            }
         }
+        return;
     }
 
-    // ---- quantize the T activation rows into shared memory (overlaps the first loads)
+    // ---------------- consumers: activations first (they may come from the previous kernel)
+    pdl_wait();
     {
         const int per_tok = p.nb * 4;
         const int total = T * per_tok;
-        for (int m0 = 0; m0 < total; m0 += THREADS) {
+        for (int m0 = 0; m0 < total; m0 += CONSUMERS) {
             const int m = m0 + tid;
             const bool ok = m < total;
             const int t = ok ? m / per_tok : 0;
@@ -155,39 +231,54 @@ gemv_q4_0_kernel(const uint8_t* __restrict__ w, const float* __restrict__ x, flo
             amax = warp_max4(amax);
             const float d = __fdiv_rn(amax, 127.0f);
             uint32_t ye, yo;
-            int s = quant_q8_split(v, d, ye, yo);
-            s = warp_sum4(s);
+            int sq = quant_q8_split(v, d, ye, yo);
+            sq = warp_sum4(sq);
             if (ok) {
                 const int qi = (t * 4 + (b & 1) * 2) * p.np + (b >> 1);
                 reinterpret_cast<uint32_t*>(&quads[qi])[i] = ye;
                 reinterpret_cast<uint32_t*>(&quads[qi + p.np])[i] = yo;
                 if (i == 0) {
                     dy[t * p.nb + b] = fp16_to_f32(fp16_bits(d));
-                    sy8[t * p.nb + b] = 8 * s;
+                    sy8[t * p.nb + b] = 8 * sq;
                 }
             }
         }
     }
+    consumer_sync();
 
-    const int RP = THREADS / LPR;           // rows processed side by side
+    constexpr int RP = CONSUMERS / LPR;     // rows processed side by side
     const int rr = tid / LPR, sl = tid % LPR;
-    const int ppl = p.np / LPR;             // pairs per lane
     const int passes = (p.G + RP - 1) / RP;
+    PairActs areg[PPL > 0 ? PPL : 1];
+    if (PPL > 0) {
+#pragma unroll
+        for (int kk = 0; kk < (PPL > 0 ? PPL : 1); ++kk)
+            areg[kk] = load_pair_acts(quads, dy, sy8, p.np, p.nb, 0, sl + kk * LPR);
+    }
+    const int ppl = p.np / LPR;
 
     int k = 0;
     for (int u = blockIdx.x; u < p.n_units; u += grid, ++k) {
         const int s = k % p.S;
-        if (tid == 0) s_ok = mbar_wait_bounded(smem_u32(&bars[s]), (uint32_t)((k / p.S) & 1), WAIT_LIMIT_NS) ? 1 : 0;
-        __syncthreads();
-        if (s_ok) mbar_try_wait(smem_u32(&bars[s]), (uint32_t)((k / p.S) & 1));   // per-thread acquire
-        if (!s_ok) {
-            if (tid == 0) {
-                record_error(&g_gemv_status, DEV_TIMEOUT);
-                // let the copies still in flight land before the CTA exits
-                for (int k2 = k + 1, u2 = u + grid; k2 < k + p.S && u2 < p.n_units; ++k2, u2 += grid)
-                    mbar_wait_bounded(smem_u32(&bars[k2 % p.S]), (uint32_t)((k2 / p.S) & 1), WAIT_LIMIT_NS);
+        {
+            const uint32_t bar = full0 + 8 * s, par = (uint32_t)((k / p.S) & 1);
+            int ok = 1;
+            if (lane == 0) {
+                bool got = mbar_try_wait(bar, par);
+                if (!got) {
+                    const uint64_t t0 = global_timer_ns();
+                    while (!got && !*abort_flag && global_timer_ns() - t0 < WAIT_LIMIT_NS)
+                        for (int i = 0; i < 32 && !got; ++i) got = mbar_try_wait(bar, par);
+                }
+                if (!got) {
+                    if (!*abort_flag) record_error(&g_gemv_status, DEV_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                ok = got ? 1 : 0;
             }
-            return;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            mbar_try_wait(bar, par);       // per-lane acquire of the completed phase
         }
         const uint8_t* stage = stages + (size_t)s * p.stage_bytes;
         const int r0 = u * p.G;
@@ -200,22 +291,16 @@ gemv_q4_0_kernel(const uint8_t* __restrict__ w, const float* __restrict__ x, flo
             for (int t = 0; t < T; ++t) acc[t] = 0.0f;
             if (valid) {
                 const uint8_t* rowp = stage + (size_t)j * p.row_bytes;
-                for (int kk = 0; kk < ppl; ++kk) {
-                    const int pr = sl + kk * LPR;
-                    const uint32_t* wp = reinterpret_cast<const uint32_t*>(rowp + 36 * pr);
-                    uint32_t wv[9];
+                if (PPL > 0) {
 #pragma unroll
-                    for (int i = 0; i < 9; ++i) wv[i] = wp[i];
-                    const PairWeights pw = unpack_pair(wv);
+                    for (int kk = 0; kk < (PPL > 0 ? PPL : 1); ++kk)
+                        acc[0] = pair_dot(rowp, sl + kk * LPR, areg[kk], acc[0]);
+                } else {
+                    for (int kk = 0; kk < ppl; ++kk) {
+                        const int pr = sl + kk * LPR;
 #pragma unroll
-                    for (int t = 0; t < T; ++t) {
-                        const uint4* qp = quads + (t * 4) * p.np + pr;
-                        const float2 dd = reinterpret_cast<const float2*>(dy + t * p.nb)[pr];
-                        const int2 ss = reinterpret_cast<const int2*>(sy8 + t * p.nb)[pr];
-                        const int ia = block_dot(pw.qa, qp[0], qp[p.np]) - ss.x;
-                        const int ib = block_dot(pw.qb, qp[2 * p.np], qp[3 * p.np]) - ss.y;
-                        acc[t] = fmaf(pw.da * dd.x, (float)ia, acc[t]);
-                        acc[t] = fmaf(pw.db * dd.y, (float)ib, acc[t]);
+                        for (int t = 0; t < T; ++t)
+                            acc[t] = pair_dot(rowp, pr, load_pair_acts(quads, dy, sy8, p.np, p.nb, t, pr), acc[t]);
                     }
                 }
             }
@@ -230,11 +315,8 @@ gemv_q4_0_kernel(const uint8_t* __restrict__ w, const float* __restrict__ x, flo
                 for (int t = 0; t < T; ++t) dst[(int64_t)t * p.ne01 + r0 + j] = acc[t];
             }
         }
-        __syncthreads();
-        if (tid == 0) {
-            const int nu = u + p.S * grid;
-            if (nu < p.n_units) issue(nu, s);
-        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * s);
     }
 }
 
@@ -242,12 +324,12 @@ gemv_q4_0_kernel(const uint8_t* __restrict__ w, const float* __restrict__ x, flo
 // Any ne00 % 32 == 0, any ne11, src0 2-byte aligned: activations are first
 // quantized to public Q8_0 blocks in the workspace, then one warp per output
 // row reads blocks with 16-bit loads and forms the exact integer block sums.
-__global__ void __launch_bounds__(THREADS)
+__global__ void __launch_bounds__(PLAIN_THREADS)
 generic_q4_0_q8_0_kernel(const uint8_t* __restrict__ w, const uint8_t* __restrict__ yq,
                          float* __restrict__ dst, int nb, int ne01, int ne11) {
     const int lane = threadIdx.x & 31;
-    const int warps = (gridDim.x * THREADS) >> 5;
-    for (int row = (blockIdx.x * THREADS + threadIdx.x) >> 5; row < ne01; row += warps) {
+    const int warps = (gridDim.x * PLAIN_THREADS) >> 5;
+    for (int row = (blockIdx.x * PLAIN_THREADS + threadIdx.x) >> 5; row < ne01; row += warps) {
         const uint8_t* wr = w + (int64_t)row * nb * Q4_0_BYTES;
         for (int t = 0; t < ne11; ++t) {
             const uint8_t* yr = yq + (int64_t)t * nb * Q8_0_BYTES;
@@ -280,12 +362,12 @@ generic_q4_0_q8_0_kernel(const uint8_t* __restrict__ w, const uint8_t* __restric
 // ------------------------------------------------------------- debug path 0 --
 // One thread per (token, row, block pair): the GEMV's unpack_pair / block_dot
 // routines on words assembled with 16-bit loads (any 2-byte-aligned input).
-__global__ void __launch_bounds__(THREADS)
+__global__ void __launch_bounds__(PLAIN_THREADS)
 debug_isums_gemv_kernel(const uint8_t* __restrict__ w, const uint8_t* __restrict__ yq,
                         int32_t* __restrict__ out, int nb, int ne01, int ne11) {
     const int np = nb / 2;
     const int64_t total = (int64_t)ne11 * ne01 * np;
-    for (int64_t g = blockIdx.x * (int64_t)THREADS + threadIdx.x; g < total; g += (int64_t)gridDim.x * THREADS) {
+    for (int64_t g = blockIdx.x * (int64_t)PLAIN_THREADS + threadIdx.x; g < total; g += (int64_t)gridDim.x * PLAIN_THREADS) {
         const int pr = (int)(g % np);
         const int64_t tr = g / np;
         const int row = (int)(tr % ne01);
@@ -325,6 +407,7 @@ debug_isums_gemv_kernel(const uint8_t* __restrict__ w, const uint8_t* __restrict
 struct GemvPlan {
     GemvParams p;
     int lpr;
+    int ppl_reg;       // > 0: activations in registers
     int grid;
     size_t smem;
 };
@@ -340,19 +423,22 @@ bool plan_gemv(int64_t ne00, int64_t ne01, int64_t ne11, const DeviceInfo& info,
     p.row_bytes = p.nb * Q4_0_BYTES;
     int lpr = 4;
     for (int c : {32, 16, 8}) if (p.np % c == 0) { lpr = c; break; }
-    const int RP = THREADS / lpr;
+    const int ppl = p.np / lpr;
+    plan->ppl_reg = (ne11 == 1 && ppl <= 8) ? ppl : 0;
+    const int RP = CONSUMERS / lpr;
     const int64_t act = ne11 * ((int64_t)p.np * 64 + (int64_t)p.nb * 8);
-    // rows per unit: aim at ~24 KB stages, but keep >= 2 units per SM when the matrix allows
-    int64_t G = RP * std::max<int64_t>(1, 24576 / ((int64_t)RP * p.row_bytes));
+    // rows per unit: aim at ~32 KB stages, but keep >= 2 units per SM when the matrix allows
+    const int64_t rp_bytes = (int64_t)RP * p.row_bytes;
+    int64_t G = RP * std::max<int64_t>(1, (32768 + rp_bytes / 2) / rp_bytes);
     while (G > 8 && (ne01 + G - 1) / G < 2 * (int64_t)info.sm_count) G = std::max<int64_t>(8, G / 2);
     G = std::min<int64_t>(G, ne01);
-    int64_t stage = ((G * p.row_bytes) + 127) / 128 * 128;
-    const int64_t head = 128;  // mbarriers
+    const int64_t stage = ((G * p.row_bytes) + 127) / 128 * 128;
+    const int64_t head = 256;  // mbarriers + abort flag
     const int64_t act_bytes = (act + 127) / 128 * 128;
     const int64_t limit = std::min<int64_t>(info.max_smem_optin, 227 * 1024) - 1024;
-    // prefer two CTAs per SM (<= ~110 KB each), else one big CTA
-    int64_t budget2 = std::min<int64_t>(limit, 110 * 1024);
-    int64_t S = (budget2 - head - act_bytes) / stage;
+    const bool two_per_sm = plan->ppl_reg == 0 || plan->ppl_reg <= 3;
+    int64_t S = 0;
+    if (two_per_sm) S = (std::min<int64_t>(limit, 110 * 1024) - head - act_bytes) / stage;
     if (S < 3) S = (limit - head - act_bytes) / stage;
     if (S < 2) return false;
     S = std::min<int64_t>(S, MAX_STAGES);
@@ -366,36 +452,67 @@ bool plan_gemv(int64_t ne00, int64_t ne01, int64_t ne11, const DeviceInfo& info,
     p.stage_off = (int)(head + act_bytes);
     plan->smem = (size_t)(head + act_bytes + S * stage);
     plan->lpr = lpr;
-    const int per_sm = plan->smem <= 113 * 1024 ? 2 : 1;
+    const int per_sm = (plan->smem <= 113 * 1024 && two_per_sm) ? 2 : 1;
     plan->grid = (int)std::min<int64_t>(p.n_units, (int64_t)info.sm_count * per_sm);
     return true;
 }
 
-template <int T, int LPR>
+template <int T, int LPR, int PPL>
 q4q_status launch_gemv_t(const GemvPlan& plan, const uint8_t* w, const float* x, float* dst, cudaStream_t stream,
-                         int device) {
-    // the opt-in shared-memory size is raised once per device (never inside a
-    // stream capture after the first call with the largest size)
+                         int device, bool pdl) {
+    // the opt-in shared-memory size is raised once per device and kernel
     static std::atomic<int> configured[64];
-    auto kern = gemv_q4_0_kernel<T, LPR>;
+    auto kern = gemv_q4_0_kernel<T, LPR, PPL>;
     if (device < 0 || device >= 64) return Q4Q_ERR_CUDA;
     if ((int)plan.smem > configured[device].load()) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem) != cudaSuccess)
             return Q4Q_ERR_CUDA;
         configured[device].store((int)plan.smem);
     }
-    kern<<<plan.grid, THREADS, plan.smem, stream>>>(w, x, dst, plan.p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)plan.grid);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = plan.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    if (cudaLaunchKernelEx(&cfg, kern, w, x, dst, plan.p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return Q4Q_ERR_CUDA;
+    }
     return launch_status();
+}
+
+template <int T, int LPR>
+q4q_status launch_gemv_ppl(const GemvPlan& plan, const uint8_t* w, const float* x, float* dst, cudaStream_t stream,
+                           int device, bool pdl) {
+    if (T == 1) {
+        switch (plan.ppl_reg) {
+            case 1: return launch_gemv_t<T, LPR, (T == 1 ? 1 : 0)>(plan, w, x, dst, stream, device, pdl);
+            case 2: return launch_gemv_t<T, LPR, (T == 1 ? 2 : 0)>(plan, w, x, dst, stream, device, pdl);
+            case 3: return launch_gemv_t<T, LPR, (T == 1 ? 3 : 0)>(plan, w, x, dst, stream, device, pdl);
+            case 4: return launch_gemv_t<T, LPR, (T == 1 ? 4 : 0)>(plan, w, x, dst, stream, device, pdl);
+            case 5: return launch_gemv_t<T, LPR, (T == 1 ? 5 : 0)>(plan, w, x, dst, stream, device, pdl);
+            case 6: return launch_gemv_t<T, LPR, (T == 1 ? 6 : 0)>(plan, w, x, dst, stream, device, pdl);
+            case 7: return launch_gemv_t<T, LPR, (T == 1 ? 7 : 0)>(plan, w, x, dst, stream, device, pdl);
+            case 8: return launch_gemv_t<T, LPR, (T == 1 ? 8 : 0)>(plan, w, x, dst, stream, device, pdl);
+            default: break;
+        }
+    }
+    return launch_gemv_t<T, LPR, 0>(plan, w, x, dst, stream, device, pdl);
 }
 
 template <int T>
 q4q_status launch_gemv_lpr(const GemvPlan& plan, const uint8_t* w, const float* x, float* dst, cudaStream_t stream,
-                           int device) {
+                           int device, bool pdl) {
     switch (plan.lpr) {
-        case 32: return launch_gemv_t<T, 32>(plan, w, x, dst, stream, device);
-        case 16: return launch_gemv_t<T, 16>(plan, w, x, dst, stream, device);
-        case 8:  return launch_gemv_t<T, 8>(plan, w, x, dst, stream, device);
-        default: return launch_gemv_t<T, 4>(plan, w, x, dst, stream, device);
+        case 32: return launch_gemv_ppl<T, 32>(plan, w, x, dst, stream, device, pdl);
+        case 16: return launch_gemv_ppl<T, 16>(plan, w, x, dst, stream, device, pdl);
+        case 8:  return launch_gemv_ppl<T, 8>(plan, w, x, dst, stream, device, pdl);
+        default: return launch_gemv_ppl<T, 4>(plan, w, x, dst, stream, device, pdl);
     }
 }
 
@@ -415,18 +532,18 @@ bool gemv_supported(const void* src0, int64_t ne00, int64_t ne01, const float* s
 }
 
 q4q_status gemv_mul_mat(const void* src0, int64_t ne00, int64_t ne01, const float* src1, int64_t ne11,
-                        float* dst, cudaStream_t stream, const DeviceInfo& info) {
+                        float* dst, cudaStream_t stream, const DeviceInfo& info, bool pdl) {
     GemvPlan plan;
     if (!plan_gemv(ne00, ne01, ne11, info, &plan)) return Q4Q_ERR_SHAPE;
     const uint8_t* w = static_cast<const uint8_t*>(src0);
     switch (ne11) {
-        case 1: return launch_gemv_lpr<1>(plan, w, src1, dst, stream, info.device);
-        case 2: return launch_gemv_lpr<2>(plan, w, src1, dst, stream, info.device);
-        case 3: return launch_gemv_lpr<3>(plan, w, src1, dst, stream, info.device);
-        case 4: return launch_gemv_lpr<4>(plan, w, src1, dst, stream, info.device);
-        case 5: return launch_gemv_lpr<5>(plan, w, src1, dst, stream, info.device);
-        case 6: return launch_gemv_lpr<6>(plan, w, src1, dst, stream, info.device);
-        default: return launch_gemv_lpr<7>(plan, w, src1, dst, stream, info.device);
+        case 1: return launch_gemv_lpr<1>(plan, w, src1, dst, stream, info.device, pdl);
+        case 2: return launch_gemv_lpr<2>(plan, w, src1, dst, stream, info.device, pdl);
+        case 3: return launch_gemv_lpr<3>(plan, w, src1, dst, stream, info.device, pdl);
+        case 4: return launch_gemv_lpr<4>(plan, w, src1, dst, stream, info.device, pdl);
+        case 5: return launch_gemv_lpr<5>(plan, w, src1, dst, stream, info.device, pdl);
+        case 6: return launch_gemv_lpr<6>(plan, w, src1, dst, stream, info.device, pdl);
+        default: return launch_gemv_lpr<7>(plan, w, src1, dst, stream, info.device, pdl);
     }
 }
 
@@ -444,7 +561,7 @@ q4q_status generic_mul_mat(const void* src0, int64_t ne00, int64_t ne01, const f
     if (st != Q4Q_OK) return st;
     const int64_t warps_needed = ne01;
     const int grid = (int)std::min<int64_t>((warps_needed + 7) / 8, (int64_t)info.sm_count * 8);
-    generic_q4_0_q8_0_kernel<<<grid, THREADS, 0, stream>>>(static_cast<const uint8_t*>(src0),
+    generic_q4_0_q8_0_kernel<<<grid, PLAIN_THREADS, 0, stream>>>(static_cast<const uint8_t*>(src0),
                                                            static_cast<const uint8_t*>(workspace), dst,
                                                            (int)(ne00 / QK), (int)ne01, (int)ne11);
     return launch_status();
@@ -456,8 +573,8 @@ q4q_status gemv_debug_isums(const void* src0, const void* src1_q8_0, int64_t ne0
     const int nb = (int)(ne00 / QK);
     const int64_t total = ne11 * ne01 * (nb / 2);
     if (total == 0) return Q4Q_OK;
-    const int grid = (int)std::min<int64_t>((total + THREADS - 1) / THREADS, (int64_t)info.sm_count * 8);
-    debug_isums_gemv_kernel<<<grid, THREADS, 0, stream>>>(static_cast<const uint8_t*>(src0),
+    const int grid = (int)std::min<int64_t>((total + PLAIN_THREADS - 1) / PLAIN_THREADS, (int64_t)info.sm_count * 8);
+    debug_isums_gemv_kernel<<<grid, PLAIN_THREADS, 0, stream>>>(static_cast<const uint8_t*>(src0),
                                                           static_cast<const uint8_t*>(src1_q8_0), out, nb,
                                                           (int)ne01, (int)ne11);
     return launch_status();

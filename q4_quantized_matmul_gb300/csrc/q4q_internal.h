@@ -35,13 +35,14 @@ q4q_status mma_mul_mat(const void* src0, int64_t ne00, int64_t ne01, const float
                        float* dst, void* workspace, size_t workspace_bytes, cudaStream_t stream,
                        const DeviceInfo& info);
 q4q_status mma_debug_isums(const void* src0, const void* src1_q8_0, int64_t ne00, int64_t ne01,
-                           int64_t ne11, int32_t* out, cudaStream_t stream, const DeviceInfo& info);
+                           int64_t ne11, int32_t* out, void* workspace, size_t workspace_bytes,
+                           cudaStream_t stream, const DeviceInfo& info);
 
 // GEMV path (q4q_gemv.cu)
 bool gemv_supported(const void* src0, int64_t ne00, int64_t ne01, const float* src1, int64_t ne11,
                     const DeviceInfo& info);
 q4q_status gemv_mul_mat(const void* src0, int64_t ne00, int64_t ne01, const float* src1, int64_t ne11,
-                        float* dst, cudaStream_t stream, const DeviceInfo& info);
+                        float* dst, cudaStream_t stream, const DeviceInfo& info, bool pdl);
 size_t generic_workspace_bytes(int64_t ne00, int64_t ne11);
 q4q_status generic_mul_mat(const void* src0, int64_t ne00, int64_t ne01, const float* src1, int64_t ne11,
                            float* dst, void* workspace, size_t workspace_bytes, cudaStream_t stream,

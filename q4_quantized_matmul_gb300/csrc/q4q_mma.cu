@@ -1,15 +1,631 @@
-// q4q_mma.cu -- tensor-core path for ne11 >= 8 (placeholder until the tcgen05 kernel lands).
+// q4q_mma.cu -- Q4_0 x Q8_0 mul_mat on the 5th-generation tensor cores (ne11 >= 8).
+//
+// The operation is "llama.cpp 深度解读" §3 "量化矩阵乘法 — 核心算子" as a GEMM:
+//   dst[n][m] = sum_b fp32(d_w[m][b] * d_x[n][b]) * S_b[m][n],
+//   S_b[m][n] = sum_{k in block b} (nibble[m][k] - 8) * q[n][k]     (exact integer).
+// sm_103a has no integer tcgen05 MMA, so both operands are held as fp16 values
+// that are exact small integers (weights in [-8, 7], activations in [-127, 127]).
+// Each 32-wide K block is two K=16 tcgen05.mma (kind::f16) into a FRESH fp32 TMEM
+// accumulator; |S_b| <= 32 * 8 * 127 < 2^24, so the accumulator holds S_b exactly.
+// The per-block scales are then applied by CUDA-core warps reading the slab out of
+// TMEM (tcgen05.ld), while the tensor core fills the other slab buffer.
+//
+// Warp roles (one CTA per 128-row x NT-token output tile, full K loop):
+//   warp 0      : TMA producer of raw Q4_0 bytes (2-D tensor map over the block rows,
+//                 box = 144 bytes (8 blocks, 256 K) x 128 rows) into a 2-deep ring
+//   warp 1      : TMEM allocator and the single MMA-issuing thread
+//   warp 2      : TMA producer of the activation tile (fp16, 128-byte swizzle,
+//                 box = 64 K x NT tokens) into a 4-deep ring
+//   warps 4-7   : dequantizers: raw Q4_0 -> fp16 A tile (128 rows x 64 K) in the
+//                 canonical K-major 128-byte-swizzle layout, plus the fp32 block scales
+//   warps 8..   : epilogue: per 32-K slab, tcgen05.ld the fp32 slab, acc += d_w d_x S
+// K order inside every 8-element group is permuted the same way on both operands
+// ([0,4,1,5,2,6,3,7]) so that a 32-bit word of nibbles turns into fp16 with a
+// handful of bit operations; the dot product does not depend on that order.
+// Every mbarrier wait is bounded; a wait that runs out records Q4Q_ERR_TIMEOUT and
+// the CTA winds down (waits for its own copies, frees its TMEM) and returns.
+#include <algorithm>
+#include <atomic>
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <mutex>
+
 #include "q4q_common.cuh"
 #include "q4q_internal.h"
 
 namespace q4q {
+namespace {
 
-unsigned int mma_take_device_status() { return 0; }
-bool mma_supported(int64_t, int64_t, int64_t, const DeviceInfo&) { return false; }
-size_t mma_workspace_bytes(int64_t, int64_t) { return 0; }
-q4q_status mma_mul_mat(const void*, int64_t, int64_t, const float*, int64_t, float*, void*, size_t,
-                       cudaStream_t, const DeviceInfo&) { return Q4Q_ERR_ARG; }
-q4q_status mma_debug_isums(const void*, const void*, int64_t, int64_t, int64_t, int32_t*, cudaStream_t,
-                           const DeviceInfo&) { return Q4Q_ERR_ARG; }
+__device__ unsigned int g_mma_status = 0;
+
+constexpr int BM = 128;                 // weight rows per CTA tile (MMA M)
+constexpr int KRAW = 256;               // K per raw-weight stage (8 blocks = 144 bytes per row)
+constexpr int KAB = 64;                 // K per A/B stage (2 blocks, one 128-byte swizzle row)
+constexpr int RAW_STAGES = 2;
+constexpr int AB_STAGES = 4;
+constexpr int RAW_BYTES = BM * 144;     // 18432
+constexpr int A_BYTES = BM * KAB * 2;   // 16384
+constexpr int NPAD = 128;               // activation-scale rows are padded to this
+
+// ------------------------------------------------------------------ PTX ----
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row atoms
+// of 1024 bytes (stride-dimension offset 1024), version bits 46..48 = 0b001.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;                 // leading-dimension offset (unused for swizzled K-major)
+    d |= (uint64_t)(1024 >> 4) << 32;       // stride-dimension offset
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;                 // SWIZZLE_128B
+    return d;
+}
+
+// Instruction descriptor, kind::f16: fp16 A and B (both K-major), fp32 D, M x N.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
+    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// bounded wait that also gives up as soon as another role has aborted
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (*reinterpret_cast<volatile unsigned int*>(&g_mma_status) != 0) {   // another CTA gave up
+            *abort_flag = 1;
+            return false;
+        }
+        if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
+            *abort_flag = 1;
+            record_error(&g_mma_status, DEV_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// Lane 0 waits (bounded), the verdict is broadcast, and every lane then takes
+// its own acquire of the completed phase (which cannot advance before this warp
+// arrives on the matching "empty" barrier).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int lane) {
+    int ok = 1;
+    if (lane == 0) ok = wait_or_abort(bar, parity, abort_flag) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) mbar_try_wait(bar, parity);
+    __syncwarp();
+    return ok != 0;
+}
+
+// Q4_0 nibble word (elements e0..e7 at bits 4e) -> 8 fp16 values (e - 8) in the
+// order [e0, e4, e1, e5, e2, e6, e3, e7]: (0x6400 | n) is the fp16 1024 + n, and
+// subtracting 1032 is exact.
+__device__ __forceinline__ uint4 nibbles_to_f16x8(uint32_t q) {
+    const uint32_t MAGIC = 0x64006400u;
+    uint32_t h[4];
+    h[0] = (q & 0x000F000Fu) | MAGIC;
+    h[1] = ((q >> 4) & 0x000F000Fu) | MAGIC;
+    h[2] = ((q >> 8) & 0x000F000Fu) | MAGIC;
+    h[3] = ((q >> 12) & 0x000F000Fu) | MAGIC;
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));   // 1032
+    uint4 out;
+    __half2 r;
+    r = __hsub2(*reinterpret_cast<__half2*>(&h[0]), bias); out.x = *reinterpret_cast<uint32_t*>(&r);
+    r = __hsub2(*reinterpret_cast<__half2*>(&h[1]), bias); out.y = *reinterpret_cast<uint32_t*>(&r);
+    r = __hsub2(*reinterpret_cast<__half2*>(&h[2]), bias); out.z = *reinterpret_cast<uint32_t*>(&r);
+    r = __hsub2(*reinterpret_cast<__half2*>(&h[3]), bias); out.w = *reinterpret_cast<uint32_t*>(&r);
+    return out;
+}
+
+// position p of an 8-element group holds element PERM[p]
+__host__ __device__ constexpr int perm8(int p) { return (p & 1) ? 4 + (p >> 1) : (p >> 1); }
+
+struct MmaParams {
+    int M, N, K, nb, Npad;
+    float* dst;           // [N][M]
+    const float* dx;      // [nb][Npad]
+    int32_t* isums;       // debug: [N][M][nb]
+};
+
+template <int NT>
+struct Cfg {
+    static constexpr int EPI_WARPS = NT >= 128 ? 8 : 4;
+    static constexpr int CPW = NT * 4 / EPI_WARPS;       // columns per epilogue warp
+    static constexpr int THREADS = (8 + EPI_WARPS) * 32;
+    static constexpr int B_BYTES = NT * KAB * 2;
+    static constexpr int TMEM_COLS = NT * 2 < 32 ? 32 : NT * 2;
+    // shared memory map (offsets from a 1024-aligned base)
+    static constexpr int OFF_RAW = 0;
+    static constexpr int OFF_A = OFF_RAW + RAW_STAGES * RAW_BYTES;                  // 36864 (1024-aligned)
+    static constexpr int OFF_B = OFF_A + AB_STAGES * A_BYTES;
+    static constexpr int OFF_DW = OFF_B + AB_STAGES * ((B_BYTES + 1023) / 1024 * 1024);
+    static constexpr int OFF_BAR = OFF_DW + AB_STAGES * 2 * BM * 4;
+    static constexpr int NBARS = 2 * RAW_STAGES + 2 * AB_STAGES + 5;
+    static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
+    static constexpr int SMEM = OFF_MISC + 64 + 1024;                                // + alignment slack
+};
+
+template <int NT, bool DEBUG>
+__global__ void __launch_bounds__(Cfg<NT>::THREADS, 1)
+mma_q4_0_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_b,
+                const MmaParams p) {
+    using C = Cfg<NT>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+    const uint32_t raw_full = smem_u32(&bars[0]);
+    const uint32_t raw_empty = smem_u32(&bars[RAW_STAGES]);
+    const uint32_t ab_full = smem_u32(&bars[2 * RAW_STAGES]);
+    const uint32_t ab_empty = smem_u32(&bars[2 * RAW_STAGES + AB_STAGES]);
+    const uint32_t slab_full = smem_u32(&bars[2 * RAW_STAGES + 2 * AB_STAGES]);
+    const uint32_t slab_empty = slab_full + 16;
+    const uint32_t drain = slab_full + 32;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 16);
+    float* dw_s = reinterpret_cast<float*>(smem + C::OFF_DW);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n0 = blockIdx.x * NT;
+    const int m0 = blockIdx.y * BM;
+    const int n_raw = p.K / KRAW, n_ab = p.K / KAB, n_slab = p.K / 32;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < RAW_STAGES; ++s) {
+            mbar_init(raw_full + 8 * s, 1);
+            mbar_init(raw_empty + 8 * s, 4);
+        }
+        for (int s = 0; s < AB_STAGES; ++s) {
+            mbar_init(ab_full + 8 * s, 4 + 1);
+            mbar_init(ab_empty + 8 * s, 1 + C::EPI_WARPS);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(slab_full + 8 * s, 1);
+            mbar_init(slab_empty + 8 * s, C::EPI_WARPS);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------- raw Q4_0 producer
+        if (lane == 0) {
+            int r = 0;
+            for (; r < n_raw; ++r) {
+                const int st = r % RAW_STAGES;
+                if (r >= RAW_STAGES && !wait_or_abort(raw_empty + 8 * st, ((r / RAW_STAGES) + 1) & 1, abort_flag)) break;
+                mbar_arrive_expect_tx(raw_full + 8 * st, RAW_BYTES);
+                tma_load_2d(sbase + C::OFF_RAW + st * RAW_BYTES, &tmap_w, r * 144, m0, raw_full + 8 * st);
+            }
+            if (*abort_flag)   // let the loads already issued land before the CTA exits
+                for (int r2 = max(0, r - RAW_STAGES); r2 < r; ++r2)
+                    mbar_wait_bounded(raw_full + 8 * (r2 % RAW_STAGES), (r2 / RAW_STAGES) & 1, WAIT_LIMIT_NS);
+        }
+    } else if (warp == 2) {
+        // ---------------- activation tile producer
+        if (lane == 0) {
+            int i = 0;
+            for (; i < n_ab; ++i) {
+                const int s = i % AB_STAGES;
+                if (i >= AB_STAGES && !wait_or_abort(ab_empty + 8 * s, ((i / AB_STAGES) + 1) & 1, abort_flag)) break;
+                mbar_arrive_expect_tx(ab_full + 8 * s, C::B_BYTES);
+                tma_load_2d(sbase + C::OFF_B + s * ((C::B_BYTES + 1023) / 1024 * 1024), &tmap_b, i * KAB, n0,
+                            ab_full + 8 * s);
+            }
+            (void)i;
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t IDESC = idesc_f16(BM, NT);
+            int g = 0;
+            bool ok = true;
+            for (int i = 0; i < n_ab && ok; ++i) {
+                const int s = i % AB_STAGES;
+                if (!wait_or_abort(ab_full + 8 * s, (i / AB_STAGES) & 1, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t a_base = sbase + C::OFF_A + s * A_BYTES;
+                const uint32_t b_base = sbase + C::OFF_B + s * ((C::B_BYTES + 1023) / 1024 * 1024);
+                for (int j = 0; j < 2; ++j, ++g) {
+                    const int buf = g & 1;
+                    if (g >= 2 && !wait_or_abort(slab_empty + 8 * buf, ((g >> 1) + 1) & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < 2; ++kk) {
+                        const uint32_t koff = (uint32_t)(64 * j + 32 * kk);    // bytes along the swizzled row
+                        mma_f16(tmem + (uint32_t)(buf * NT), smem_desc_sw128(a_base + koff),
+                                smem_desc_sw128(b_base + koff), IDESC, (uint32_t)kk);
+                    }
+                    mma_commit(slab_full + 8 * buf);
+                }
+                if (ok) mma_commit(ab_empty + 8 * s);
+            }
+            if (!ok) {
+                // no MMA may still be reading shared memory or writing TMEM at exit
+                mma_commit(drain);
+                mbar_wait_bounded(drain, 0, WAIT_LIMIT_NS);
+            }
+        }
+    } else if (warp >= 4 && warp < 8) {
+        // ---------------- dequantizers: thread t <-> tile row t
+        const int t = threadIdx.x - 128;
+        const int rsw = t & 7;
+        bool ok = true;
+        for (int r = 0; r < n_raw && ok; ++r) {
+            const int st = r % RAW_STAGES;
+            if (!warp_wait(raw_full + 8 * st, (r / RAW_STAGES) & 1, abort_flag, lane)) { ok = false; break; }
+            const uint8_t* rowp = smem + C::OFF_RAW + st * RAW_BYTES + t * 144;
+            for (int a = 0; a < KRAW / KAB; ++a) {
+                const int i = r * (KRAW / KAB) + a;
+                const int s = i % AB_STAGES;
+                if (i >= AB_STAGES && !warp_wait(ab_empty + 8 * s, ((i / AB_STAGES) + 1) & 1, abort_flag, lane)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t* wp = reinterpret_cast<const uint32_t*>(rowp + 36 * a);
+                uint32_t w[9];
+#pragma unroll
+                for (int k = 0; k < 9; ++k) w[k] = wp[k];
+                uint32_t q[8];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) q[k] = __byte_perm(w[k], w[k + 1], 0x5432);   // block 2a
+#pragma unroll
+                for (int k = 0; k < 4; ++k) q[4 + k] = w[5 + k];                          // block 2a+1
+                uint8_t* atile = smem + C::OFF_A + s * A_BYTES + (t >> 3) * 1024 + rsw * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<uint4*>(atile + ((c ^ rsw) << 4)) = nibbles_to_f16x8(q[c]);
+                dw_s[(s * 2 + 0) * BM + t] = fp16_to_f32(w[0]);
+                dw_s[(s * 2 + 1) * BM + t] = fp16_to_f32(w[4] >> 16);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ab_full + 8 * s);
+            }
+            __syncwarp();
+            if (ok && lane == 0) mbar_arrive(raw_empty + 8 * st);
+        }
+    } else if (warp >= 8) {
+        // ---------------- epilogue
+        const int q = warp & 3;                      // TMEM lane quadrant
+        const int h = (warp - 8) >> 2;               // column group
+        const int row = q * 32 + lane;
+        const int m = m0 + row;
+        const int col0 = h * C::CPW;
+        const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
+        float acc[C::CPW];
+#pragma unroll
+        for (int c = 0; c < C::CPW; ++c) acc[c] = 0.0f;
+        for (int g = 0; g < n_slab; ++g) {
+            const int buf = g & 1;
+            const int i = g >> 1, s = i % AB_STAGES, j = g & 1;
+            if (!warp_wait(slab_full + 8 * buf, (g >> 1) & 1, abort_flag, lane)) break;
+            // the stage's scales were written before ab_full completed
+            if (!warp_wait(ab_full + 8 * s, (i / AB_STAGES) & 1, abort_flag, lane)) break;
+            tc_fence_after();
+            const float dwm = dw_s[(s * 2 + j) * BM + row];
+            const float* dxg = p.dx + (size_t)g * p.Npad + n0 + col0;
+#pragma unroll
+            for (int c0 = 0; c0 < C::CPW; c0 += 16) {
+                uint32_t r[16];
+                tmem_ld16(tq + (uint32_t)(buf * NT + col0 + c0), r);
+                tmem_ld_wait();
+                if (DEBUG) {
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        const int n = n0 + col0 + c0 + c;
+                        if (n < p.N && m < p.M)
+                            p.isums[((size_t)n * p.M + m) * p.nb + g] = (int32_t)__uint_as_float(r[c]);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 16; c += 4) {
+                        const float4 d4 = __ldg(reinterpret_cast<const float4*>(dxg + c0 + c));
+                        acc[c0 + c + 0] = fmaf(dwm * d4.x, __uint_as_float(r[c + 0]), acc[c0 + c + 0]);
+                        acc[c0 + c + 1] = fmaf(dwm * d4.y, __uint_as_float(r[c + 1]), acc[c0 + c + 1]);
+                        acc[c0 + c + 2] = fmaf(dwm * d4.z, __uint_as_float(r[c + 2]), acc[c0 + c + 2]);
+                        acc[c0 + c + 3] = fmaf(dwm * d4.w, __uint_as_float(r[c + 3]), acc[c0 + c + 3]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(slab_empty + 8 * buf);
+                if (j == 1) mbar_arrive(ab_empty + 8 * s);
+            }
+        }
+        if (!DEBUG && !*abort_flag && m < p.M) {
+#pragma unroll
+            for (int c = 0; c < C::CPW; ++c) {
+                const int n = n0 + col0 + c;
+                if (n < p.N) p.dst[(size_t)n * p.M + m] = acc[c];
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+// ---------------------------------------------------- activation operands --
+// Q8_0 quantization of each src1 row (same recipe as q4q_quantize_q8_0), written
+// as exact-integer fp16 in the permuted K order, plus the widened block scales
+// d_x[b][n] (zero for the padding rows n >= N).
+__global__ void __launch_bounds__(256)
+act_to_mma_kernel(const float* __restrict__ x, __half* __restrict__ bmat, float* __restrict__ dx, int K, int N,
+                  int Npad) {
+    const int nb = K / QK;
+    const int64_t total = (int64_t)N * nb * 4;
+    for (int64_t m0 = (int64_t)blockIdx.x * 256; m0 < total; m0 += (int64_t)gridDim.x * 256) {
+        const int64_t m = m0 + threadIdx.x;
+        const bool ok = m < total;
+        const int64_t blk = ok ? m >> 2 : 0;
+        const int i = (int)(m & 3);
+        const int n = (int)(blk / nb), b = (int)(blk % nb);
+        float v[8];
+        if (ok) {
+            const float4* src = reinterpret_cast<const float4*>(x + (int64_t)n * K + b * QK + i * 8);
+            const float4 a = __ldg(src), c = __ldg(src + 1);
+            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+            v[4] = c.x; v[5] = c.y; v[6] = c.z; v[7] = c.w;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] = 0.0f;
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(v[e]));
+        amax = warp_max4(amax);
+        const float d = __fdiv_rn(amax, 127.0f);
+        if (ok) {
+            uint32_t hw[4];
+#pragma unroll
+            for (int pp = 0; pp < 4; ++pp) {
+                const int q0 = quant_one(v[perm8(2 * pp)], d, -127.0f, 127.0f);
+                const int q1 = quant_one(v[perm8(2 * pp + 1)], d, -127.0f, 127.0f);
+                const __half2 hv = __halves2half2(__int2half_rn(q0), __int2half_rn(q1));
+                hw[pp] = *reinterpret_cast<const uint32_t*>(&hv);
+            }
+            *reinterpret_cast<uint4*>(bmat + (int64_t)n * K + b * QK + i * 8) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            if (i == 0) dx[(int64_t)b * Npad + n] = fp16_to_f32(fp16_bits(d));
+        }
+    }
+    // padding rows of the scale table
+    const int64_t pad = (int64_t)nb * (Npad - N);
+    for (int64_t e = (int64_t)blockIdx.x * 256 + threadIdx.x; e < pad; e += (int64_t)gridDim.x * 256) {
+        const int64_t b = e / (Npad - N), n = N + e % (Npad - N);
+        dx[b * Npad + n] = 0.0f;
+    }
+}
+
+// Public Q8_0 blocks -> the same operands (debug path).
+__global__ void __launch_bounds__(256)
+q8_to_mma_kernel(const uint8_t* __restrict__ yq, __half* __restrict__ bmat, float* __restrict__ dx, int K, int N,
+                 int Npad) {
+    const int nb = K / QK;
+    const int64_t total = (int64_t)N * nb * 4;
+    for (int64_t m = (int64_t)blockIdx.x * 256 + threadIdx.x; m < total; m += (int64_t)gridDim.x * 256) {
+        const int64_t blk = m >> 2;
+        const int i = (int)(m & 3);
+        const int n = (int)(blk / nb), b = (int)(blk % nb);
+        const uint8_t* y = yq + blk * Q8_0_BYTES;
+        uint32_t hw[4];
+#pragma unroll
+        for (int pp = 0; pp < 4; ++pp) {
+            const int q0 = (int8_t)y[2 + i * 8 + perm8(2 * pp)];
+            const int q1 = (int8_t)y[2 + i * 8 + perm8(2 * pp + 1)];
+            const __half2 hv = __halves2half2(__int2half_rn(q0), __int2half_rn(q1));
+            hw[pp] = *reinterpret_cast<const uint32_t*>(&hv);
+        }
+        *reinterpret_cast<uint4*>(bmat + (int64_t)n * K + b * QK + i * 8) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        if (i == 0) dx[(int64_t)b * Npad + n] = fp16_to_f32((uint32_t)y[0] | ((uint32_t)y[1] << 8));
+    }
+    const int64_t pad = (int64_t)nb * (Npad - N);
+    for (int64_t e = (int64_t)blockIdx.x * 256 + threadIdx.x; e < pad; e += (int64_t)gridDim.x * 256) {
+        const int64_t b = e / (Npad - N), n = N + e % (Npad - N);
+        dx[b * Npad + n] = 0.0f;
+    }
+}
+
+// ------------------------------------------------------------------ host ----
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encode() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode != nullptr;
+}
+
+int pick_nt(int64_t N) {
+    if (N <= 16) return 16;
+    if (N <= 32) return 32;
+    if (N <= 64) return 64;
+    return 128;
+}
+
+int64_t npad_of(int64_t N) { return (N + NPAD - 1) / NPAD * NPAD; }
+
+size_t b_bytes_of(int64_t K, int64_t N) { return ((size_t)N * K * 2 + 255) / 256 * 256; }
+
+template <int NT, bool DEBUG>
+q4q_status launch_mma_t(const CUtensorMap& tw, const CUtensorMap& tb, const MmaParams& p, cudaStream_t stream,
+                        int device) {
+    using C = Cfg<NT>;
+    static std::atomic<int> configured[64];
+    auto kern = mma_q4_0_kernel<NT, DEBUG>;
+    if (device < 0 || device >= 64) return Q4Q_ERR_CUDA;
+    if (!configured[device].load()) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+            return Q4Q_ERR_CUDA;
+        configured[device].store(1);
+    }
+    dim3 grid((unsigned)((p.N + NT - 1) / NT), (unsigned)((p.M + BM - 1) / BM));
+    kern<<<grid, C::THREADS, C::SMEM, stream>>>(tw, tb, p);
+    return launch_status();
+}
+
+template <bool DEBUG>
+q4q_status run_mma(const void* src0, int64_t ne00, int64_t ne01, int64_t ne11, const __half* bmat, const float* dx,
+                   float* dst, int32_t* isums, cudaStream_t stream, const DeviceInfo& info) {
+    if (!get_encode()) return Q4Q_ERR_CUDA;
+    const int NT = pick_nt(ne11);
+    CUtensorMap tw, tb;
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)(ne00 / QK * Q4_0_BYTES), (cuuint64_t)ne01};
+        const cuuint64_t strides[1] = {(cuuint64_t)(ne00 / QK * Q4_0_BYTES)};
+        const cuuint32_t box[2] = {144, BM};
+        const cuuint32_t estr[2] = {1, 1};
+        if (g_encode(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(src0), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return Q4Q_ERR_CUDA;
+    }
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)ne00, (cuuint64_t)ne11};
+        const cuuint64_t strides[1] = {(cuuint64_t)(ne00 * 2)};
+        const cuuint32_t box[2] = {KAB, (cuuint32_t)NT};
+        const cuuint32_t estr[2] = {1, 1};
+        if (g_encode(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(bmat), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return Q4Q_ERR_CUDA;
+    }
+    MmaParams p;
+    p.M = (int)ne01;
+    p.N = (int)ne11;
+    p.K = (int)ne00;
+    p.nb = (int)(ne00 / QK);
+    p.Npad = (int)npad_of(ne11);
+    p.dst = dst;
+    p.dx = dx;
+    p.isums = isums;
+    switch (NT) {
+        case 16: return launch_mma_t<16, DEBUG>(tw, tb, p, stream, info.device);
+        case 32: return launch_mma_t<32, DEBUG>(tw, tb, p, stream, info.device);
+        case 64: return launch_mma_t<64, DEBUG>(tw, tb, p, stream, info.device);
+        default: return launch_mma_t<128, DEBUG>(tw, tb, p, stream, info.device);
+    }
+}
+
+}  // namespace
+
+unsigned int mma_take_device_status() {
+    unsigned int v = 0, z = 0;
+    if (cudaMemcpyFromSymbol(&v, g_mma_status, sizeof(v)) != cudaSuccess) return Q4Q_ERR_CUDA;
+    if (v) cudaMemcpyToSymbol(g_mma_status, &z, sizeof(z));
+    return v;
+}
+
+bool mma_supported(int64_t ne00, int64_t ne01, int64_t ne11, const DeviceInfo& info) {
+    if (info.cc_major != 10) return false;
+    if (ne00 < KRAW || ne00 % KRAW != 0 || ne01 <= 0 || ne11 <= 0 || ne11 >= (1 << 20)) return false;
+    if (ne01 >= (1ll << 31) || ne00 >= (1 << 20)) return false;
+    return Cfg<128>::SMEM <= info.max_smem_optin && get_encode();
+}
+
+size_t mma_workspace_bytes(int64_t ne00, int64_t ne11) {
+    return b_bytes_of(ne00, ne11) + (size_t)(ne00 / QK) * (size_t)npad_of(ne11) * 4;
+}
+
+q4q_status mma_mul_mat(const void* src0, int64_t ne00, int64_t ne01, const float* src1, int64_t ne11, float* dst,
+                       void* workspace, size_t workspace_bytes, cudaStream_t stream, const DeviceInfo& info) {
+    if (workspace_bytes < mma_workspace_bytes(ne00, ne11)) return Q4Q_ERR_WORKSPACE;
+    __half* bmat = static_cast<__half*>(workspace);
+    float* dx = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + b_bytes_of(ne00, ne11));
+    const int64_t items = ne11 * (ne00 / QK) * 4;
+    const int grid = (int)std::min<int64_t>((items + 255) / 256, (int64_t)info.sm_count * 8);
+    act_to_mma_kernel<<<grid, 256, 0, stream>>>(src1, bmat, dx, (int)ne00, (int)ne11, (int)npad_of(ne11));
+    q4q_status st = launch_status();
+    if (st != Q4Q_OK) return st;
+    return run_mma<false>(src0, ne00, ne01, ne11, bmat, dx, dst, nullptr, stream, info);
+}
+
+size_t mma_debug_workspace_bytes(int64_t ne00, int64_t ne11) { return mma_workspace_bytes(ne00, ne11); }
+
+q4q_status mma_debug_isums(const void* src0, const void* src1_q8_0, int64_t ne00, int64_t ne01, int64_t ne11,
+                           int32_t* out, void* workspace, size_t workspace_bytes, cudaStream_t stream,
+                           const DeviceInfo& info) {
+    if (!mma_supported(ne00, ne01, std::max<int64_t>(ne11, 8), info)) return Q4Q_ERR_SHAPE;
+    if (!aligned(src0, 16)) return Q4Q_ERR_ALIGN;
+    if (workspace_bytes < mma_workspace_bytes(ne00, ne11)) return Q4Q_ERR_WORKSPACE;
+    if (!workspace) return Q4Q_ERR_NULL;
+    if (!aligned(workspace, 256)) return Q4Q_ERR_ALIGN;
+    __half* bmat = static_cast<__half*>(workspace);
+    float* dx = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + b_bytes_of(ne00, ne11));
+    const int64_t items = ne11 * (ne00 / QK) * 4;
+    const int grid = (int)std::min<int64_t>((items + 255) / 256, (int64_t)info.sm_count * 8);
+    q8_to_mma_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint8_t*>(src1_q8_0), bmat, dx, (int)ne00,
+                                               (int)ne11, (int)npad_of(ne11));
+    q4q_status st = launch_status();
+    if (st != Q4Q_OK) return st;
+    return run_mma<true>(src0, ne00, ne01, ne11, bmat, dx, nullptr, out, stream, info);
+}
 
 }  // namespace q4q

@@ -77,34 +77,38 @@ quantize_fast_kernel(const float* __restrict__ src, uint8_t* __restrict__ dst, i
     }
 }
 
-// Any alignment (src 4-byte aligned): one thread per block, scalar traffic.
+// Any alignment (src 4-byte aligned): one thread per block; the blocks of a
+// CTA are assembled in shared memory and leave as consecutive byte stores.
 template <bool IS_Q4>
 __global__ void __launch_bounds__(THREADS)
 quantize_generic_kernel(const float* __restrict__ src, uint8_t* __restrict__ dst, int64_t nblocks) {
     constexpr int BB = IS_Q4 ? Q4_0_BYTES : Q8_0_BYTES;
-    for (int64_t gb = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; gb < nblocks;
-         gb += (int64_t)gridDim.x * blockDim.x) {
-        const float* x = src + gb * QK;
-        float amax = 0.0f;
-        for (int k = 0; k < QK; ++k) amax = fmaxf(amax, fabsf(x[k]));
-        uint8_t* o = dst + gb * BB;
-        if (IS_Q4) {
-            const float d = __fdiv_rn(amax, 8.0f);
-            const uint16_t h = fp16_bits(d);
-            o[0] = (uint8_t)(h & 0xff);
-            o[1] = (uint8_t)(h >> 8);
-            for (int j = 0; j < QK / 2; ++j) {
-                const int lo = quant_one(x[2 * j], d, -8.0f, 7.0f) + 8;
-                const int hi = quant_one(x[2 * j + 1], d, -8.0f, 7.0f) + 8;
-                o[2 + j] = (uint8_t)(lo | (hi << 4));
+    __shared__ __align__(16) uint8_t stage[THREADS * BB];
+    for (int64_t g0 = (int64_t)blockIdx.x * THREADS; g0 < nblocks; g0 += (int64_t)gridDim.x * THREADS) {
+        const int64_t gb = g0 + threadIdx.x;
+        uint8_t* o = stage + threadIdx.x * BB;
+        if (gb < nblocks) {
+            const float* x = src + gb * QK;
+            float amax = 0.0f;
+            for (int k = 0; k < QK; ++k) amax = fmaxf(amax, fabsf(x[k]));
+            const float d = __fdiv_rn(amax, IS_Q4 ? 8.0f : 127.0f);
+            *reinterpret_cast<uint16_t*>(o) = fp16_bits(d);     // o is 2-byte aligned (BB is even)
+            if (IS_Q4) {
+                for (int j = 0; j < QK / 2; ++j) {
+                    const int lo = quant_one(x[2 * j], d, -8.0f, 7.0f) + 8;
+                    const int hi = quant_one(x[2 * j + 1], d, -8.0f, 7.0f) + 8;
+                    o[2 + j] = (uint8_t)(lo | (hi << 4));
+                }
+            } else {
+                for (int k = 0; k < QK; ++k) o[2 + k] = (uint8_t)(quant_one(x[k], d, -127.0f, 127.0f) & 0xff);
             }
-        } else {
-            const float d = __fdiv_rn(amax, 127.0f);
-            const uint16_t h = fp16_bits(d);
-            o[0] = (uint8_t)(h & 0xff);
-            o[1] = (uint8_t)(h >> 8);
-            for (int k = 0; k < QK; ++k) o[2 + k] = (uint8_t)(quant_one(x[k], d, -127.0f, 127.0f) & 0xff);
         }
+        __syncthreads();
+        const int64_t left = nblocks - g0;
+        const int bytes = (int)((left < THREADS ? left : THREADS) * BB);
+        uint8_t* out = dst + g0 * BB;
+        for (int i = threadIdx.x; i < bytes; i += THREADS) out[i] = stage[i];
+        __syncthreads();
     }
 }
 
@@ -130,7 +134,7 @@ q4q_status launch_quantize(bool q4, const float* src, void* dst, int64_t ncols, 
         if (q4) quantize_fast_kernel<true><<<grid, THREADS, 0, stream>>>(src, out, nblocks);
         else    quantize_fast_kernel<false><<<grid, THREADS, 0, stream>>>(src, out, nblocks);
     } else {
-        const int grid = (int)std::min<int64_t>((nblocks + THREADS - 1) / THREADS, (int64_t)info.sm_count * 8);
+        const int grid = (int)std::min<int64_t>((nblocks + THREADS - 1) / THREADS, (int64_t)info.sm_count * 4);
         if (q4) quantize_generic_kernel<true><<<grid, THREADS, 0, stream>>>(src, out, nblocks);
         else    quantize_generic_kernel<false><<<grid, THREADS, 0, stream>>>(src, out, nblocks);
     }

@@ -23,8 +23,9 @@ def lib():
 def test_header_declares_the_boundary():
     from q4_quantized_matmul_gb300 import _lib
     names = set(_lib.declared_entry_points())
-    assert {"q4q_quantize_q4_0", "q4q_quantize_q8_0", "q4q_mul_mat", "q4q_mul_mat_workspace_size",
-            "q4q_debug_block_isums", "q4q_device_status", "q4q_status_string", "q4q_version"} <= names
+    assert {"q4q_quantize_q4_0", "q4q_quantize_q8_0", "q4q_mul_mat", "q4q_mul_mat_ex", "q4q_mul_mat_workspace_size",
+            "q4q_debug_block_isums", "q4q_debug_workspace_size", "q4q_device_status", "q4q_status_string",
+            "q4q_version"} <= names
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -92,8 +93,12 @@ def test_argument_errors_need_no_gpu(lib):
     assert lib.q4q_quantize_q4_0(None, fake, 32, 1, None) == 1
     assert lib.q4q_quantize_q8_0(P(0x1002), fake, 32, 1, None) == 3
     # debug entry
-    assert lib.q4q_debug_block_isums(fake, fake, 64, 2, 1, 5, fake, None) == 7
-    assert lib.q4q_debug_block_isums(fake, fake, 64, 0, 1, 0, fake, None) == 0
+    assert lib.q4q_debug_block_isums(fake, fake, 64, 2, 1, 5, fake, None, 0, None) == 7
+    assert lib.q4q_debug_block_isums(fake, fake, 64, 0, 1, 0, fake, None, 0, None) == 0
+    assert lib.q4q_debug_workspace_size(64, 1, 0, ctypes.byref(ctypes.c_size_t())) == 0
+    assert lib.q4q_debug_workspace_size(64, 1, 2, ctypes.byref(ctypes.c_size_t())) == 7
+    # unknown launch flags
+    assert lib.q4q_mul_mat_ex(fake, 64, 4, fake, 64, 1, fake, None, 0, 2, None) == 7
     # workspace query
     n = ctypes.c_size_t(123)
     assert lib.q4q_mul_mat_workspace_size(64, 4, 1, None) == 1

@@ -131,6 +131,36 @@ def test_block_isums_extremes(q4q):
     np.testing.assert_array_equal(got, ref)
 
 
+@pytest.mark.parametrize("ne00,ne01,ne11", [(256, 1, 1), (256, 5, 3), (512, 130, 9), (1024, 200, 17),
+                                            (4096, 64, 40), (768, 37, 130)])
+def test_block_isums_mma_routine(q4q, ne00, ne01, ne11):
+    # one 32-wide K block per fresh TMEM accumulator, read back as exact integers
+    rng = np.random.default_rng([ne00, ne01, ne11, 4])
+    w = _special_weights(rng, ne01, ne00)
+    x = rng.standard_normal((ne11, ne00)).astype(np.float32)
+    x[:, ::5] *= 40
+    wq = oracle.quantize_q4_0(w)
+    xq = oracle.quantize_q8_0(x)
+    ref = oracle.block_isums(wq, xq, ne00, ne01, ne11)
+    got = q4q.q4q_debug_block_isums(dev(wq), dev(xq), ne00, ne01, ne11, path=1).cpu().numpy()
+    np.testing.assert_array_equal(got, ref)
+    assert q4q.q4q_device_status() == 0
+
+
+def test_block_isums_mma_extremes(q4q):
+    ne00, ne01, ne11 = 256, 3, 2
+    wq = np.zeros((ne01, 8 * 18), np.uint8)
+    wq[0, :] = 0x00
+    wq[1, :] = 0xFF
+    wq[2, :] = 0x0F
+    xq = np.zeros((ne11, 8 * 34), np.uint8)
+    xq[0, :] = np.int8(-127).view(np.uint8)
+    xq[1, :] = np.int8(127).view(np.uint8)
+    ref = oracle.block_isums(wq, xq, ne00, ne01, ne11)
+    got = q4q.q4q_debug_block_isums(dev(wq), dev(xq), ne00, ne01, ne11, path=1).cpu().numpy()
+    np.testing.assert_array_equal(got, ref)
+
+
 # ------------------------------------------------------------------- mul_mat --
 
 GEMV_SHAPES = [(256, 1), (256, 3), (768, 2304), (768, 1000), (3072, 768), (4096, 1024), (14336, 64),
@@ -159,6 +189,44 @@ def test_mul_mat_other_paths(q4q, ne00, ne01, ne11):
     got = q4q.q4q_mul_mat(q4q.q4q_quantize_q4_0(dev(w)), ne00, ne01, dev(x)).cpu().numpy()
     ref, scale = oracle.mul_mat(oracle.quantize_q4_0(w), ne00, ne01, x, nthreads=8)
     assert_close(got, ref, scale)
+
+
+MMA_SHAPES = [(256, 128, 8), (512, 300, 16), (768, 130, 17), (4096, 1024, 64), (4096, 257, 129), (1024, 64, 200),
+              (14336, 256, 512)]
+
+
+@pytest.mark.parametrize("ne00,ne01,ne11", MMA_SHAPES)
+def test_mul_mat_tensor_core(q4q, ne00, ne01, ne11):
+    rng = np.random.default_rng([ne00, ne01, ne11, 5])
+    w = _special_weights(rng, ne01, ne00)
+    x = rng.standard_normal((ne11, ne00)).astype(np.float32)
+    x[ne11 // 2] = 0.0
+    got = q4q.q4q_mul_mat(q4q.q4q_quantize_q4_0(dev(w)), ne00, ne01, dev(x)).cpu().numpy()
+    ref, scale = oracle.mul_mat(oracle.quantize_q4_0(w), ne00, ne01, x, nthreads=8)
+    assert_close(got, ref, scale)
+    assert q4q.q4q_device_status() == 0
+
+
+def test_mul_mat_pdl_chain(q4q):
+    # y1 = W1 x, y2 = W2 y1, y3 = W3 y2 with programmatic dependent launch: every
+    # call must see its predecessor's output (same kernels, so results are identical)
+    rng = np.random.default_rng(9)
+    dims = [1024, 2048, 768, 1536]
+    ws = [q4q.q4q_quantize_q4_0(dev((rng.standard_normal((dims[i + 1], dims[i])) * 0.02).astype(np.float32)))
+          for i in range(3)]
+    x = dev(rng.standard_normal((1, dims[0])).astype(np.float32))
+    outs = {}
+    for flags in (0, q4q.Q4Q_MUL_MAT_PDL):
+        y = x
+        for i in range(3):
+            y = q4q.q4q_mul_mat(ws[i], dims[i], dims[i + 1], y, flags=flags)
+        outs[flags] = y.cpu().numpy()
+    np.testing.assert_array_equal(outs[0], outs[q4q.Q4Q_MUL_MAT_PDL])
+    # and against the oracle, step by step
+    y = x.cpu().numpy()
+    for i in range(3):
+        y, _ = oracle.mul_mat(ws[i].cpu().numpy(), dims[i], dims[i + 1], y)
+    np.testing.assert_allclose(outs[0], y, rtol=1e-4, atol=1e-6)
 
 
 def test_mul_mat_misaligned_weights_take_generic_path(q4q):
@@ -236,4 +304,25 @@ def test_full_size_decode_workloads(q4q, name):
         np.testing.assert_array_equal(wq_d.view(ne01, -1)[torch.from_numpy(rows).cuda()].cpu().numpy(), wq_rows)
         ref, scale = oracle.mul_mat(wq_rows, ne00, rows.size, x, nthreads=8)
         assert_close(got[:, rows], ref, scale)
+    assert q4q.q4q_device_status() == 0
+
+
+@pytest.mark.parametrize("name,ne11", [("llama3_8b_batched", 8), ("llama3_8b_batched", 64),
+                                       ("llama3_8b_batched", 512), ("stress_prefill", 2048)])
+def test_full_size_batched_workloads(q4q, name, ne11):
+    """The tensor-core path at full size: every matrix of the workload, outputs on
+    up to 1024 sampled rows (plus first and last) for every token."""
+    wl = workloads.WORKLOADS[name]
+    for i, (ne00, ne01) in enumerate(wl.shapes):
+        if name == "llama3_8b_batched" and i in (2, 3, 5):
+            continue           # v = k, o = q, up = gate in shape
+        w, x = workloads.problem(name, i, ne11)
+        wq_d = q4q.q4q_quantize_q4_0(dev(w))
+        got = q4q.q4q_mul_mat(wq_d, ne00, ne01, dev(x)).cpu().numpy()
+        rows = _sample_rows(ne01, 1024, 100 + i)
+        wq_rows = wq_d.view(ne01, -1)[torch.from_numpy(rows).cuda()].cpu().numpy()
+        np.testing.assert_array_equal(wq_rows, oracle.quantize_q4_0(w[rows]))
+        ref, scale = oracle.mul_mat(wq_rows, ne00, rows.size, x, nthreads=16)
+        assert_close(got[:, rows], ref, scale)
+        del wq_d
     assert q4q.q4q_device_status() == 0
