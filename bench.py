@@ -175,10 +175,13 @@ def run_ours(args, rank, world, local_rank):
     workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
 
     stream = torch.cuda.Stream(device=dev)
+    # decode chains launch with programmatic dependent launch: each call may start
+    # streaming its (resident, read-only) weights while the previous call finishes
+    flags = q4q.Q4Q_MUL_MAT_PDL if ne11 < 8 else 0
 
     def step(c):
         for i, (ne00, ne01) in enumerate(shapes):
-            q4q.q4q_mul_mat(wsets[c][i], ne00, ne01, xs[i], dst=dsts[i], workspace=workspace)
+            q4q.q4q_mul_mat(wsets[c][i], ne00, ne01, xs[i], dst=dsts[i], workspace=workspace, flags=flags)
 
     with torch.cuda.stream(stream):
         for c in range(copies):         # first calls outside capture (one-time set-up per kernel)
@@ -280,7 +283,7 @@ def run_ours(args, rank, world, local_rank):
     def e2e_step(c):
         xd.copy_(xh, non_blocking=True)
         for i, (ne00, ne01) in enumerate(shapes):
-            q4q.q4q_mul_mat(wsets[c][i], ne00, ne01, xviews[i], dst=oviews[i], workspace=workspace)
+            q4q.q4q_mul_mat(wsets[c][i], ne00, ne01, xviews[i], dst=oviews[i], workspace=workspace, flags=flags)
         oh.copy_(od, non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -310,6 +313,8 @@ def run_ours(args, rank, world, local_rank):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ems = float(t.item())
     e2e_value = world * wbytes * args.steps / (ems * 1e-3) / 1e9
+
+    batched = measure_batched(dev, stream, args) if (rank == 0 and args.batched_tokens > 0) else None
 
     # ---- CPU baseline: the oracle on this host's cores, bounded sample
     cpu = cpu_baseline(args.workload, ne11, budget_s=args.cpu_seconds) if (rank == 0 and args.cpu_seconds > 0) else None
@@ -341,7 +346,7 @@ def run_ours(args, rank, world, local_rank):
             "launch": "one CUDA graph per weight copy, %d q4q_mul_mat calls per step" % nmat,
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
-        "gpu_launches": nmat * args.steps,
+        "gpu_launches": nmat * args.steps * (1 if ne11 < 8 else 2),
         "roofline": {
             "bound": "hbm",
             "kernel": "gemv_q4_0_kernel (fused Q8_0 activation quantize + Q4_0 GEMV)" if ne11 < 8 else "mul_mat",
@@ -365,8 +370,90 @@ def run_ours(args, rank, world, local_rank):
                             "ms": round(quant_ms, 3), "note": "q4q_quantize_q4_0 over the set, once, per matrix"},
         "cpu_baseline": cpu,
         "clocks": clocks,
+        "batched": batched,
     }
     return line
+
+
+def measure_batched(dev, stream, args):
+    """The other half of the metric: int8-equivalent TOPS (2*M*N*K per second) of
+    the tensor-core path on the Llama-3-8B-shaped projection set at args.batched_tokens
+    tokens (seed 3 workload), weights resident, activations quantized inside each call."""
+    import torch
+
+    import q4_quantized_matmul_gb300 as q4q
+    from q4_quantized_matmul_gb300 import workloads
+    name, ne11 = "llama3_8b_batched", args.batched_tokens
+    shapes = list(workloads.WORKLOADS[name].shapes)
+    wq, xs, ds = [], [], []
+    for i, (ne00, ne01) in enumerate(shapes):
+        w, x = workloads.problem(name, i, ne11)
+        wd = torch.from_numpy(w).to(dev)
+        wq.append(q4q.q4q_quantize_q4_0(wd))
+        del wd
+        xs.append(torch.from_numpy(x).to(dev))
+        ds.append(torch.empty((ne11, ne01), dtype=torch.float32, device=dev))
+    ws = torch.empty(max(q4q.q4q_mul_mat_workspace_size(k, n, ne11) for k, n in shapes), dtype=torch.uint8,
+                     device=dev)
+
+    def step():
+        for i, (ne00, ne01) in enumerate(shapes):
+            q4q.q4q_mul_mat(wq[i], ne00, ne01, xs[i], dst=ds[i], workspace=ws)
+
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        step()
+    steps = 10
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g.replay()
+        e0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    ops = sum(2.0 * k * n * ne11 for k, n in shapes)
+    # per-launch durations of each call (activation quantize + tensor-core GEMM)
+    per = []
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(2e8))
+        evs = []
+        for i, (ne00, ne01) in enumerate(shapes):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            q4q.q4q_mul_mat(wq[i], ne00, ne01, xs[i], dst=ds[i], workspace=ws)
+            b.record(stream)
+            evs.append((i, a, b))
+    torch.cuda.synchronize()
+    for i, a, b in evs:
+        k, n = shapes[i]
+        per.append({"shape": "%d->%d" % (k, n), "us": round(a.elapsed_time(b) * 1e3, 1),
+                    "tops": round(2.0 * k * n * ne11 / (a.elapsed_time(b) * 1e-3) / 1e12, 1)})
+    peak = _measured_bf16()
+    tops = ops / (ms * 1e-3) / 1e12
+    out = {"workload": name, "ne11": ne11, "ms_per_step": round(ms, 4), "int8_equiv_tops": round(tops, 1),
+           "unit": "TOPS (2*M*N*K/s)", "roofline": {"bound": "tensor", "achieved": round(tops, 1),
+                                                      "peak": peak[0], "peak_kind": peak[1], "unit": "TFLOP/s",
+                                                      "frac": round(tops / peak[0], 4),
+                                                      "note": "fp16 exact-integer operands on tcgen05 kind::f16; "
+                                                              "peak = dense f16/bf16"},
+           "per_launch": per}
+    del wq, xs, ds, ws
+    torch.cuda.empty_cache()
+    return out
+
+
+def _measured_bf16():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured burst"
+    except Exception:
+        return 1900.0, "fallback"
 
 
 def cpu_baseline(workload, ne11, budget_s=10.0, reps_min=1):
@@ -486,6 +573,8 @@ def main():
     ap.add_argument("--ne11", type=int, default=0, help="override the workload's token count")
     ap.add_argument("--soak", type=float, default=1.5, help="seconds of untimed load before warm-up")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline budget (0 = skip)")
+    ap.add_argument("--batched-tokens", type=int, default=512,
+                    help="also measure the tensor-core path on the Llama-3-8B set at this many tokens (0 = skip)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
