@@ -132,6 +132,33 @@ Q4Q_API q4q_status q4q_mul_mat_ex(const void* src0, int64_t ne00, int64_t ne01,
                           float* dst, void* workspace, size_t workspace_bytes,
                           unsigned int flags, q4q_stream_t stream);
 
+/* Size of the library-owned scratch array used by q4q_mul_mat_noalloc (per GPU). */
+#define Q4Q_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* q4q_mul_mat for callers that cannot allocate device memory.  The pages have no
+ * counterpart to this call; it exists for callers such as a plugin inside a host
+ * application that owns every device allocation (an inference server with its
+ * own memory pool, a runtime that forbids allocation after start-up) and so has
+ * no workspace to pass.  It computes exactly what q4q_mul_mat computes, with the
+ * same arguments minus the workspace, and allocates nothing: the scratch space
+ * that the tensor-core and generic paths need comes from one static device array
+ * of Q4Q_NOALLOC_SCRATCH_BYTES that the library owns on every GPU that loads it,
+ * until the process exits.
+ *  - Limit: problems whose q4q_mul_mat_workspace_size exceeds
+ *    Q4Q_NOALLOC_SCRATCH_BYTES are rejected with Q4Q_ERR_WORKSPACE before any
+ *    launch (e.g. ne11 = 512 tokens fits up to ne00 = 7680; ne11 = 2048 does not
+ *    fit at ne00 = 4096).
+ *  - Set-up: the first call on a device, made while that device is current,
+ *    looks up the array's device address (cudaGetSymbolAddress) and caches it;
+ *    make that first call before any stream capture.
+ *  - Sharing: every call on a device uses the same array, which keeps whatever
+ *    the last call left in it (no call needs it to start at zero: each call
+ *    rewrites every scratch byte it reads).  Calls that overlap on the GPU (on
+ *    different streams, or from several host threads) race on it; serialize them. */
+Q4Q_API q4q_status q4q_mul_mat_noalloc(const void* src0, int64_t ne00, int64_t ne01,
+                               const float* src1, int64_t ne10, int64_t ne11,
+                               float* dst, q4q_stream_t stream);
+
 /* Debug: per-block integer sums isum(i01, i11, b) (§3's `sumi`) of Q4_0 weights
  * and already-quantized Q8_0 activations, computed by the device routine of the
  * chosen path: path 0 = the GEMV block-dot routine (dp4a on nibble words),

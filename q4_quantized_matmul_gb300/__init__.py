@@ -19,7 +19,8 @@ from . import _lib
 
 __all__ = [
     "Q4QError", "q4q_quantize_q4_0", "q4q_quantize_q8_0", "q4q_mul_mat_workspace_size",
-    "q4q_mul_mat", "q4q_debug_block_isums", "q4q_debug_workspace_size", "Q4Q_MUL_MAT_PDL", "q4q_device_status", "q4q_status_string",
+    "q4q_mul_mat", "q4q_debug_block_isums", "q4q_debug_workspace_size", "Q4Q_MUL_MAT_PDL",
+    "q4q_mul_mat_noalloc", "Q4Q_NOALLOC_SCRATCH_BYTES", "q4q_device_status", "q4q_status_string",
     "q4q_version", "q4_0_row_bytes", "q8_0_row_bytes", "mul_mat_host",
 ]
 
@@ -136,6 +137,26 @@ def q4q_mul_mat(src0: torch.Tensor, ne00: int, ne01: int, src1: torch.Tensor,
 
 
 Q4Q_MUL_MAT_PDL = 1
+Q4Q_NOALLOC_SCRATCH_BYTES = 8 << 20
+
+
+def q4q_mul_mat_noalloc(src0: torch.Tensor, ne00: int, ne01: int, src1: torch.Tensor,
+                        dst: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """q4q_mul_mat without a workspace, for callers that cannot allocate device
+    memory: the library's own static scratch array (Q4Q_NOALLOC_SCRATCH_BYTES per
+    GPU) stands in for it.  Calls that overlap on the GPU share that array and
+    race; larger problems raise Q4QError (Q4Q_ERR_WORKSPACE)."""
+    if src1.dtype != torch.float32:
+        raise TypeError("src1 must be float32")
+    x = src1.reshape(-1, src1.shape[-1]) if src1.dim() != 2 else src1
+    ne11, ne10 = x.shape
+    if dst is None:
+        dst = torch.empty((ne11, ne01), dtype=torch.float32, device=x.device)
+    if ne01 * ne11 == 0:
+        return dst
+    _check("q4q_mul_mat_noalloc", _lib.load().q4q_mul_mat_noalloc(_dev(src0, "src0"), ne00, ne01, _dev(x, "src1"),
+                                                                 ne10, ne11, _dev(dst, "dst"), _stream(stream)))
+    return dst
 
 
 def q4q_debug_workspace_size(ne00: int, ne11: int, path: int) -> int:
