@@ -180,7 +180,7 @@ gemv_q4_0_kernel(const uint8_t* __restrict__ w, const float* __restrict__ x, flo
                     if (!ok) {
                         const uint64_t t0 = global_timer_ns();
                         while (!ok && !*abort_flag && global_timer_ns() - t0 < WAIT_LIMIT_NS)
-                            for (int i = 0; i < 32 && !ok; ++i) ok = mbar_try_wait(bar, par);
+                            ok = mbar_try_wait_sleep(bar, par, SLEEP_HINT_NS);
                     }
                     if (!ok) {
                         if (!*abort_flag) record_error(&g_gemv_status, DEV_TIMEOUT);
@@ -268,7 +268,7 @@ gemv_q4_0_kernel(const uint8_t* __restrict__ w, const float* __restrict__ x, flo
                 if (!got) {
                     const uint64_t t0 = global_timer_ns();
                     while (!got && !*abort_flag && global_timer_ns() - t0 < WAIT_LIMIT_NS)
-                        for (int i = 0; i < 32 && !got; ++i) got = mbar_try_wait(bar, par);
+                        got = mbar_try_wait_sleep(bar, par, SLEEP_HINT_NS);
                 }
                 if (!got) {
                     if (!*abort_flag) record_error(&g_gemv_status, DEV_TIMEOUT);
@@ -427,21 +427,37 @@ bool plan_gemv(int64_t ne00, int64_t ne01, int64_t ne11, const DeviceInfo& info,
     plan->ppl_reg = (ne11 == 1 && ppl <= 8) ? ppl : 0;
     const int RP = CONSUMERS / lpr;
     const int64_t act = ne11 * ((int64_t)p.np * 64 + (int64_t)p.nb * 8);
-    // rows per unit: aim at ~32 KB stages, but keep >= 2 units per SM when the matrix allows
-    const int64_t rp_bytes = (int64_t)RP * p.row_bytes;
-    int64_t G = RP * std::max<int64_t>(1, (32768 + rp_bytes / 2) / rp_bytes);
-    while (G > 8 && (ne01 + G - 1) / G < 2 * (int64_t)info.sm_count) G = std::max<int64_t>(8, G / 2);
-    G = std::min<int64_t>(G, ne01);
-    const int64_t stage = ((G * p.row_bytes) + 127) / 128 * 128;
     const int64_t head = 256;  // mbarriers + abort flag
     const int64_t act_bytes = (act + 127) / 128 * 128;
     const int64_t limit = std::min<int64_t>(info.max_smem_optin, 227 * 1024) - 1024;
+    const int64_t sms = info.sm_count;
+    const int64_t wbytes = ne01 * (int64_t)p.row_bytes;
     const bool two_per_sm = plan->ppl_reg == 0 || plan->ppl_reg <= 3;
-    int64_t S = 0;
-    if (two_per_sm) S = (std::min<int64_t>(limit, 110 * 1024) - head - act_bytes) / stage;
-    if (S < 3) S = (limit - head - act_bytes) / stage;
-    if (S < 2) return false;
-    S = std::min<int64_t>(S, MAX_STAGES);
+    int64_t G, S, stage;
+    bool small = false;
+    if (two_per_sm && wbytes <= 96 * 1024 * sms) {
+        // Small matrix: one CTA per SM holds every unit it owns in flight from the
+        // start (about two units each), and leaves room on the SM for the next
+        // kernel's CTA, which can then prefetch its own weights under PDL.
+        G = std::max<int64_t>(1, (ne01 + 2 * sms - 1) / (2 * sms));
+        const int64_t units = (ne01 + G - 1) / G;
+        S = std::min<int64_t>(MAX_STAGES, (units + sms - 1) / sms);
+        stage = ((G * p.row_bytes) + 127) / 128 * 128;
+        small = head + act_bytes + S * stage <= std::min<int64_t>(limit, 110 * 1024);
+    }
+    if (!small) {
+        // rows per unit: aim at ~32 KB stages, but keep >= 2 units per SM when the matrix allows
+        const int64_t rp_bytes = (int64_t)RP * p.row_bytes;
+        G = RP * std::max<int64_t>(1, (32768 + rp_bytes / 2) / rp_bytes);
+        while (G > 8 && (ne01 + G - 1) / G < 2 * sms) G = std::max<int64_t>(8, G / 2);
+        G = std::min<int64_t>(G, ne01);
+        stage = ((G * p.row_bytes) + 127) / 128 * 128;
+        S = 0;
+        if (two_per_sm) S = (std::min<int64_t>(limit, 110 * 1024) - head - act_bytes) / stage;
+        if (S < 3) S = (limit - head - act_bytes) / stage;
+        if (S < 2) return false;
+        S = std::min<int64_t>(S, MAX_STAGES);
+    }
     p.G = (int)G;
     p.n_units = (int)((ne01 + G - 1) / G);
     p.S = (int)S;
@@ -452,8 +468,8 @@ bool plan_gemv(int64_t ne00, int64_t ne01, int64_t ne11, const DeviceInfo& info,
     p.stage_off = (int)(head + act_bytes);
     plan->smem = (size_t)(head + act_bytes + S * stage);
     plan->lpr = lpr;
-    const int per_sm = (plan->smem <= 113 * 1024 && two_per_sm) ? 2 : 1;
-    plan->grid = (int)std::min<int64_t>(p.n_units, (int64_t)info.sm_count * per_sm);
+    const int per_sm = (!small && plan->smem <= 113 * 1024 && two_per_sm) ? 2 : 1;
+    plan->grid = (int)std::min<int64_t>(p.n_units, sms * per_sm);
     return true;
 }
 

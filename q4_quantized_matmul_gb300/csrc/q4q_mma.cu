@@ -12,7 +12,7 @@
 //
 // Warp roles (one CTA per 128-row x NT-token output tile, full K loop):
 //   warp 0      : TMA producer of raw Q4_0 bytes (2-D tensor map over the block rows,
-//                 box = 144 bytes (8 blocks, 256 K) x 128 rows) into a 2-deep ring
+//                 box = 144 bytes (8 blocks, 256 K) x 128 rows) into a 3-deep ring
 //   warp 1      : TMEM allocator and the single MMA-issuing thread
 //   warp 2      : TMA producer of the activation tile (fp16, 128-byte swizzle,
 //                 box = 64 K x NT tokens) into a 4-deep ring
@@ -41,7 +41,7 @@ __device__ unsigned int g_mma_status = 0;
 constexpr int BM = 128;                 // weight rows per CTA tile (MMA M)
 constexpr int KRAW = 256;               // K per raw-weight stage (8 blocks = 144 bytes per row)
 constexpr int KAB = 64;                 // K per A/B stage (2 blocks, one 128-byte swizzle row)
-constexpr int RAW_STAGES = 2;
+constexpr int RAW_STAGES = 3;
 constexpr int AB_STAGES = 4;
 constexpr int RAW_BYTES = BM * 144;     // 18432
 constexpr int A_BYTES = BM * KAB * 2;   // 16384
@@ -95,6 +95,17 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         : "r"(taddr));
 }
 
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row atoms
@@ -119,8 +130,7 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, SLEEP_HINT_NS)) return true;
         if (*abort_flag) return false;
         if (*reinterpret_cast<volatile unsigned int*>(&g_mma_status) != 0) {   // another CTA gave up
             *abort_flag = 1;
@@ -176,20 +186,47 @@ struct MmaParams {
     int32_t* isums;       // debug: [N][M][nb]
 };
 
+__device__ __forceinline__ uint64_t pack2(float x, float y) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+    return r;
+}
+
+__device__ __forceinline__ void unpack2(uint64_t r, float& x, float& y) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(r));
+}
+
+// two fp32 lanes at once: d = a * b, d = a * b + c (each lane rounded as fmul / fmaf)
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
 template <int NT>
 struct Cfg {
     static constexpr int EPI_WARPS = NT >= 128 ? 8 : 4;
     static constexpr int CPW = NT * 4 / EPI_WARPS;       // columns per epilogue warp
     static constexpr int THREADS = (8 + EPI_WARPS) * 32;
     static constexpr int B_BYTES = NT * KAB * 2;
-    static constexpr int TMEM_COLS = NT * 2 < 32 ? 32 : NT * 2;
+    static constexpr int B_STRIDE = (B_BYTES + 1023) / 1024 * 1024;
+    static constexpr int NBUF = NT * 4 <= 512 ? 4 : 2;   // TMEM slab buffers
+    static constexpr int TMEM_COLS = NT * NBUF < 32 ? 32 : NT * NBUF;
+    static constexpr int DX_BYTES = 2 * NT * 4;           // activation scales of one A/B stage
     // shared memory map (offsets from a 1024-aligned base)
     static constexpr int OFF_RAW = 0;
-    static constexpr int OFF_A = OFF_RAW + RAW_STAGES * RAW_BYTES;                  // 36864 (1024-aligned)
+    static constexpr int OFF_A = OFF_RAW + RAW_STAGES * RAW_BYTES;                  // 55296 (1024-aligned)
     static constexpr int OFF_B = OFF_A + AB_STAGES * A_BYTES;
-    static constexpr int OFF_DW = OFF_B + AB_STAGES * ((B_BYTES + 1023) / 1024 * 1024);
-    static constexpr int OFF_BAR = OFF_DW + AB_STAGES * 2 * BM * 4;
-    static constexpr int NBARS = 2 * RAW_STAGES + 2 * AB_STAGES + 5;
+    static constexpr int OFF_DW = OFF_B + AB_STAGES * B_STRIDE;
+    static constexpr int OFF_DX = OFF_DW + AB_STAGES * 2 * BM * 4;
+    static constexpr int OFF_BAR = OFF_DX + AB_STAGES * DX_BYTES;
+    static constexpr int NBARS = 2 * RAW_STAGES + 2 * AB_STAGES + 2 * NBUF + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
     static constexpr int SMEM = OFF_MISC + 64 + 1024;                                // + alignment slack
 };
@@ -199,6 +236,7 @@ __global__ void __launch_bounds__(Cfg<NT>::THREADS, 1)
 mma_q4_0_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_b,
                 const MmaParams p) {
     using C = Cfg<NT>;
+    constexpr int NBUF = C::NBUF;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -208,11 +246,12 @@ mma_q4_0_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
     const uint32_t ab_full = smem_u32(&bars[2 * RAW_STAGES]);
     const uint32_t ab_empty = smem_u32(&bars[2 * RAW_STAGES + AB_STAGES]);
     const uint32_t slab_full = smem_u32(&bars[2 * RAW_STAGES + 2 * AB_STAGES]);
-    const uint32_t slab_empty = slab_full + 16;
-    const uint32_t drain = slab_full + 32;
+    const uint32_t slab_empty = slab_full + 8 * NBUF;
+    const uint32_t drain = slab_full + 16 * NBUF;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 16);
     float* dw_s = reinterpret_cast<float*>(smem + C::OFF_DW);
+    const float* dx_s = reinterpret_cast<const float*>(smem + C::OFF_DX);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * NT;
@@ -228,7 +267,7 @@ mma_q4_0_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
             mbar_init(ab_full + 8 * s, 4 + 1);
             mbar_init(ab_empty + 8 * s, 1 + C::EPI_WARPS);
         }
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < NBUF; ++s) {
             mbar_init(slab_full + 8 * s, 1);
             mbar_init(slab_empty + 8 * s, C::EPI_WARPS);
         }
@@ -257,17 +296,22 @@ mma_q4_0_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                     mbar_wait_bounded(raw_full + 8 * (r2 % RAW_STAGES), (r2 / RAW_STAGES) & 1, WAIT_LIMIT_NS);
         }
     } else if (warp == 2) {
-        // ---------------- activation tile producer
+        // ---------------- activation tile + activation scale producer
         if (lane == 0) {
             int i = 0;
             for (; i < n_ab; ++i) {
                 const int s = i % AB_STAGES;
                 if (i >= AB_STAGES && !wait_or_abort(ab_empty + 8 * s, ((i / AB_STAGES) + 1) & 1, abort_flag)) break;
-                mbar_arrive_expect_tx(ab_full + 8 * s, C::B_BYTES);
-                tma_load_2d(sbase + C::OFF_B + s * ((C::B_BYTES + 1023) / 1024 * 1024), &tmap_b, i * KAB, n0,
-                            ab_full + 8 * s);
+                const uint32_t bar = ab_full + 8 * s;
+                mbar_arrive_expect_tx(bar, C::B_BYTES + C::DX_BYTES);
+                tma_load_2d(sbase + C::OFF_B + s * C::B_STRIDE, &tmap_b, i * KAB, n0, bar);
+                const uint32_t dxd = sbase + C::OFF_DX + s * C::DX_BYTES;
+                bulk_g2s(dxd, p.dx + (size_t)(2 * i) * p.Npad + n0, NT * 4, bar);
+                bulk_g2s(dxd + NT * 4, p.dx + (size_t)(2 * i + 1) * p.Npad + n0, NT * 4, bar);
             }
-            (void)i;
+            if (*abort_flag)
+                for (int i2 = max(0, i - AB_STAGES); i2 < i; ++i2)
+                    mbar_wait_bounded(ab_full + 8 * (i2 % AB_STAGES), (i2 / AB_STAGES) & 1, WAIT_LIMIT_NS);
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer
@@ -280,10 +324,10 @@ mma_q4_0_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                 if (!wait_or_abort(ab_full + 8 * s, (i / AB_STAGES) & 1, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t a_base = sbase + C::OFF_A + s * A_BYTES;
-                const uint32_t b_base = sbase + C::OFF_B + s * ((C::B_BYTES + 1023) / 1024 * 1024);
+                const uint32_t b_base = sbase + C::OFF_B + s * C::B_STRIDE;
                 for (int j = 0; j < 2; ++j, ++g) {
-                    const int buf = g & 1;
-                    if (g >= 2 && !wait_or_abort(slab_empty + 8 * buf, ((g >> 1) + 1) & 1, abort_flag)) {
+                    const int buf = g % NBUF;
+                    if (g >= NBUF && !wait_or_abort(slab_empty + 8 * buf, ((g / NBUF) + 1) & 1, abort_flag)) {
                         ok = false;
                         break;
                     }
@@ -305,14 +349,23 @@ mma_q4_0_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
             }
         }
     } else if (warp >= 4 && warp < 8) {
-        // ---------------- dequantizers: thread t <-> tile row t
+        // ---------------- dequantizers: thread t <-> tile row t; a row's 8 raw blocks
+        // (144 bytes) are read with nine 16-byte loads (row pitch 144 bytes keeps the
+        // eight lanes of each load phase on distinct banks)
         const int t = threadIdx.x - 128;
         const int rsw = t & 7;
         bool ok = true;
         for (int r = 0; r < n_raw && ok; ++r) {
             const int st = r % RAW_STAGES;
             if (!warp_wait(raw_full + 8 * st, (r / RAW_STAGES) & 1, abort_flag, lane)) { ok = false; break; }
-            const uint8_t* rowp = smem + C::OFF_RAW + st * RAW_BYTES + t * 144;
+            const uint4* rowp = reinterpret_cast<const uint4*>(smem + C::OFF_RAW + st * RAW_BYTES + t * 144);
+            uint32_t wv[36];
+#pragma unroll
+            for (int k = 0; k < 9; ++k) {
+                const uint4 v = rowp[k];
+                wv[4 * k + 0] = v.x; wv[4 * k + 1] = v.y; wv[4 * k + 2] = v.z; wv[4 * k + 3] = v.w;
+            }
+#pragma unroll
             for (int a = 0; a < KRAW / KAB; ++a) {
                 const int i = r * (KRAW / KAB) + a;
                 const int s = i % AB_STAGES;
@@ -320,25 +373,25 @@ mma_q4_0_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                     ok = false;
                     break;
                 }
-                const uint32_t* wp = reinterpret_cast<const uint32_t*>(rowp + 36 * a);
-                uint32_t w[9];
-#pragma unroll
-                for (int k = 0; k < 9; ++k) w[k] = wp[k];
+                // pair a = blocks 2a, 2a+1 = words 9a .. 9a+8 of the row
                 uint32_t q[8];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) q[k] = __byte_perm(w[k], w[k + 1], 0x5432);   // block 2a
+                for (int k = 0; k < 4; ++k) q[k] = __byte_perm(wv[9 * a + k], wv[9 * a + k + 1], 0x5432);
 #pragma unroll
-                for (int k = 0; k < 4; ++k) q[4 + k] = w[5 + k];                          // block 2a+1
+                for (int k = 0; k < 4; ++k) q[4 + k] = wv[9 * a + 5 + k];
                 uint8_t* atile = smem + C::OFF_A + s * A_BYTES + (t >> 3) * 1024 + rsw * 128;
 #pragma unroll
                 for (int c = 0; c < 8; ++c)
                     *reinterpret_cast<uint4*>(atile + ((c ^ rsw) << 4)) = nibbles_to_f16x8(q[c]);
-                dw_s[(s * 2 + 0) * BM + t] = fp16_to_f32(w[0]);
-                dw_s[(s * 2 + 1) * BM + t] = fp16_to_f32(w[4] >> 16);
+                dw_s[(s * 2 + 0) * BM + t] = fp16_to_f32(wv[9 * a]);
+                dw_s[(s * 2 + 1) * BM + t] = fp16_to_f32(wv[9 * a + 4] >> 16);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(ab_full + 8 * s);
             }
+            // Release the raw stage only now: every word loaded from it has been
+            // consumed by the conversions above, so no load of this stage can still
+            // be in flight when the producer's TMA starts overwriting it.
             __syncwarp();
             if (ok && lane == 0) mbar_arrive(raw_empty + 8 * st);
         }
@@ -350,38 +403,41 @@ mma_q4_0_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
         const int m = m0 + row;
         const int col0 = h * C::CPW;
         const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
-        float acc[C::CPW];
+        uint64_t acc[C::CPW / 2];
 #pragma unroll
-        for (int c = 0; c < C::CPW; ++c) acc[c] = 0.0f;
+        for (int c = 0; c < C::CPW / 2; ++c) acc[c] = 0;
         for (int g = 0; g < n_slab; ++g) {
-            const int buf = g & 1;
+            const int buf = g % NBUF;
             const int i = g >> 1, s = i % AB_STAGES, j = g & 1;
-            if (!warp_wait(slab_full + 8 * buf, (g >> 1) & 1, abort_flag, lane)) break;
-            // the stage's scales were written before ab_full completed
-            if (!warp_wait(ab_full + 8 * s, (i / AB_STAGES) & 1, abort_flag, lane)) break;
+            if (!warp_wait(slab_full + 8 * buf, (g / NBUF) & 1, abort_flag, lane)) break;
+            // the stage's weight scales were written before ab_full completed
+            if (j == 0 && !warp_wait(ab_full + 8 * s, (i / AB_STAGES) & 1, abort_flag, lane)) break;
             tc_fence_after();
             const float dwm = dw_s[(s * 2 + j) * BM + row];
-            const float* dxg = p.dx + (size_t)g * p.Npad + n0 + col0;
+            const uint64_t dw2 = pack2(dwm, dwm);
+            const float4* dxs = reinterpret_cast<const float4*>(dx_s + (s * 2 + j) * NT + col0);
+            constexpr int CH = C::CPW >= 32 ? 32 : 16;     // columns per TMEM load round trip
 #pragma unroll
-            for (int c0 = 0; c0 < C::CPW; c0 += 16) {
-                uint32_t r[16];
-                tmem_ld16(tq + (uint32_t)(buf * NT + col0 + c0), r);
+            for (int c0 = 0; c0 < C::CPW; c0 += CH) {
+                uint32_t r[CH];
+                if constexpr (CH == 32) tmem_ld32(tq + (uint32_t)(buf * NT + col0 + c0), r);
+                else tmem_ld16(tq + (uint32_t)(buf * NT + col0 + c0), r);
                 tmem_ld_wait();
                 if (DEBUG) {
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) {
+                    for (int c = 0; c < CH; ++c) {
                         const int n = n0 + col0 + c0 + c;
                         if (n < p.N && m < p.M)
                             p.isums[((size_t)n * p.M + m) * p.nb + g] = (int32_t)__uint_as_float(r[c]);
                     }
                 } else {
 #pragma unroll
-                    for (int c = 0; c < 16; c += 4) {
-                        const float4 d4 = __ldg(reinterpret_cast<const float4*>(dxg + c0 + c));
-                        acc[c0 + c + 0] = fmaf(dwm * d4.x, __uint_as_float(r[c + 0]), acc[c0 + c + 0]);
-                        acc[c0 + c + 1] = fmaf(dwm * d4.y, __uint_as_float(r[c + 1]), acc[c0 + c + 1]);
-                        acc[c0 + c + 2] = fmaf(dwm * d4.z, __uint_as_float(r[c + 2]), acc[c0 + c + 2]);
-                        acc[c0 + c + 3] = fmaf(dwm * d4.w, __uint_as_float(r[c + 3]), acc[c0 + c + 3]);
+                    for (int c = 0; c < CH; c += 4) {
+                        const float4 d4 = dxs[(c0 + c) >> 2];
+                        const uint64_t s01 = pack2(__uint_as_float(r[c]), __uint_as_float(r[c + 1]));
+                        const uint64_t s23 = pack2(__uint_as_float(r[c + 2]), __uint_as_float(r[c + 3]));
+                        acc[(c0 + c) >> 1] = ffma2(fmul2(dw2, pack2(d4.x, d4.y)), s01, acc[(c0 + c) >> 1]);
+                        acc[((c0 + c) >> 1) + 1] = ffma2(fmul2(dw2, pack2(d4.z, d4.w)), s23, acc[((c0 + c) >> 1) + 1]);
                     }
                 }
             }
@@ -394,9 +450,12 @@ mma_q4_0_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
         }
         if (!DEBUG && !*abort_flag && m < p.M) {
 #pragma unroll
-            for (int c = 0; c < C::CPW; ++c) {
-                const int n = n0 + col0 + c;
-                if (n < p.N) p.dst[(size_t)n * p.M + m] = acc[c];
+            for (int c = 0; c < C::CPW / 2; ++c) {
+                float x0, x1;
+                unpack2(acc[c], x0, x1);
+                const int n = n0 + col0 + 2 * c;
+                if (n < p.N) p.dst[(size_t)n * p.M + m] = x0;
+                if (n + 1 < p.N) p.dst[(size_t)(n + 1) * p.M + m] = x1;
             }
         }
     }
