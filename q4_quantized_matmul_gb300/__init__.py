@@ -51,11 +51,14 @@ def _stream(stream) -> Optional[int]:
     return stream
 
 
-def _dev(t: torch.Tensor, name: str):
+def _dev(t: torch.Tensor, name: str, min_bytes: int = 0):
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError("%s must be a CUDA tensor" % name)
     if not t.is_contiguous():
         raise ValueError("%s must be contiguous" % name)
+    if t.numel() * t.element_size() < min_bytes:
+        raise ValueError("%s holds %d bytes, the call reads or writes %d" % (
+            name, t.numel() * t.element_size(), min_bytes))
     return ctypes.c_void_p(t.data_ptr())
 
 
@@ -81,7 +84,8 @@ def _quantize(fn: str, src: torch.Tensor, dst: Optional[torch.Tensor], row_bytes
     nrows, ncols = src.shape
     if dst is None:
         dst = torch.empty((nrows, row_bytes(ncols)), dtype=torch.uint8, device=src.device)
-    _check(fn, getattr(_lib.load(), fn)(_dev(src, "src"), _dev(dst, "dst"), ncols, nrows, _stream(stream)))
+    _check(fn, getattr(_lib.load(), fn)(_dev(src, "src"), _dev(dst, "dst", nrows * row_bytes(ncols)), ncols, nrows,
+                                         _stream(stream)))
     return dst
 
 
@@ -127,12 +131,14 @@ def q4q_mul_mat(src0: torch.Tensor, ne00: int, ne01: int, src1: torch.Tensor,
     if ne01 * ne11 == 0:
         return dst
     lib = _lib.load()
+    w_ptr = _dev(src0, "src0", ne01 * q4_0_row_bytes(ne00))
+    d_ptr = _dev(dst, "dst", 4 * ne01 * ne11)
     if flags:
-        _check("q4q_mul_mat_ex", lib.q4q_mul_mat_ex(_dev(src0, "src0"), ne00, ne01, _dev(x, "src1"), ne10, ne11,
-                                                   _dev(dst, "dst"), ws_ptr, ws_bytes, int(flags), _stream(stream)))
+        _check("q4q_mul_mat_ex", lib.q4q_mul_mat_ex(w_ptr, ne00, ne01, _dev(x, "src1"), ne10, ne11,
+                                                   d_ptr, ws_ptr, ws_bytes, int(flags), _stream(stream)))
     else:
-        _check("q4q_mul_mat", lib.q4q_mul_mat(_dev(src0, "src0"), ne00, ne01, _dev(x, "src1"), ne10, ne11,
-                                             _dev(dst, "dst"), ws_ptr, ws_bytes, _stream(stream)))
+        _check("q4q_mul_mat", lib.q4q_mul_mat(w_ptr, ne00, ne01, _dev(x, "src1"), ne10, ne11,
+                                             d_ptr, ws_ptr, ws_bytes, _stream(stream)))
     return dst
 
 
@@ -154,8 +160,9 @@ def q4q_mul_mat_noalloc(src0: torch.Tensor, ne00: int, ne01: int, src1: torch.Te
         dst = torch.empty((ne11, ne01), dtype=torch.float32, device=x.device)
     if ne01 * ne11 == 0:
         return dst
-    _check("q4q_mul_mat_noalloc", _lib.load().q4q_mul_mat_noalloc(_dev(src0, "src0"), ne00, ne01, _dev(x, "src1"),
-                                                                 ne10, ne11, _dev(dst, "dst"), _stream(stream)))
+    _check("q4q_mul_mat_noalloc", _lib.load().q4q_mul_mat_noalloc(_dev(src0, "src0", ne01 * q4_0_row_bytes(ne00)),
+                                                                 ne00, ne01, _dev(x, "src1"), ne10, ne11,
+                                                                 _dev(dst, "dst", 4 * ne01 * ne11), _stream(stream)))
     return dst
 
 
@@ -177,8 +184,10 @@ def q4q_debug_block_isums(src0: torch.Tensor, src1_q8_0: torch.Tensor, ne00: int
     ws_ptr = _dev(workspace, "workspace") if workspace is not None else None
     ws_bytes = workspace.numel() if workspace is not None else 0
     _check("q4q_debug_block_isums",
-           _lib.load().q4q_debug_block_isums(_dev(src0, "src0"), _dev(src1_q8_0, "src1_q8_0"), ne00, ne01, ne11,
-                                             int(path), _dev(out, "out"), ws_ptr, ws_bytes, _stream(stream)))
+           _lib.load().q4q_debug_block_isums(_dev(src0, "src0", ne01 * q4_0_row_bytes(ne00)),
+                                             _dev(src1_q8_0, "src1_q8_0", ne11 * q8_0_row_bytes(ne00)), ne00, ne01,
+                                             ne11, int(path), _dev(out, "out", 4 * ne11 * ne01 * (ne00 // QK)),
+                                             ws_ptr, ws_bytes, _stream(stream)))
     return out
 
 

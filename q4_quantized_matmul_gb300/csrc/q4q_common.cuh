@@ -38,12 +38,51 @@ __device__ __forceinline__ int warp_sum4(int v) {
     return v;
 }
 
-// q = clamp(round_half_away(x / d), lo, hi); 0 when d == 0
+// q = clamp(round_half_away(x / d), lo, hi); 0 when d == 0.  The quotient is
+// the IEEE one (fl(x / d)), exactly as the encoder defines it.
 __device__ __forceinline__ int quant_one(float x, float d, float lo, float hi) {
     if (d == 0.0f) return 0;
     float r = roundf(__fdiv_rn(x, d));
     r = fminf(fmaxf(r, lo), hi);
     return (int)r;
+}
+
+// Hardware reciprocal (about 1 ulp); only ever used inside quant8's error
+// budget, never as a stored value.
+__device__ __forceinline__ float recip_approx(float d) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(d));
+    return r;
+}
+
+// quant_one for 8 values of one block, without a division on the common path.
+// inv = 1/d to within 2^-22 relative, so t = fl(x * inv) is within 6e-5 of
+// fl(x / d) (|x / d| <= 128 since |x| <= amax and d = amax / 8 or amax / 127).
+// Round-half-away and round-to-nearest-even differ only at half-integers, and
+// both are constant between them, so where t is more than 1e-3 away from a
+// half-integer rintf(t) == roundf(fl(x / d)).  Elements inside that band (or
+// with a non-finite t, e.g. a reciprocal flushed to infinity) take the exact
+// quotient; the warp vote keeps those divisions off the common path.
+// Must be called by all 32 lanes of the warp.
+__device__ __forceinline__ void quant8(const float (&v)[8], float d, float lo, float hi, int (&q)[8]) {
+    const float inv = recip_approx(d);
+    float r[8];
+    bool near = false;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const float t = v[e] * inv;
+        r[e] = rintf(t);
+        near |= !(fabsf(t - r[e]) <= 0.499f);
+    }
+    if (__any_sync(0xffffffffu, near && d != 0.0f)) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float t = v[e] * inv;
+            if (d != 0.0f && !(fabsf(t - rintf(t)) <= 0.499f)) r[e] = roundf(__fdiv_rn(v[e], d));
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) q[e] = (d == 0.0f) ? 0 : (int)fminf(fmaxf(r[e], lo), hi);
 }
 
 __device__ __forceinline__ uint16_t fp16_bits(float d) {
@@ -56,14 +95,14 @@ __device__ __forceinline__ float fp16_to_f32(uint32_t bits16) {
 
 // Eight consecutive elements of one block -> one 32-bit word of Q4_0 nibbles.
 // Byte j of the block's qs holds element 2j (low) and 2j+1 (high), so the 8
-// elements e = 0..7 of this word land at bit 4e.
+// elements e = 0..7 of this word land at bit 4e.  All 32 lanes of the warp must
+// call it (see quant8).
 __device__ __forceinline__ uint32_t pack_q4_word(const float (&v)[8], float d) {
+    int q[8];
+    quant8(v, d, -8.0f, 7.0f, q);
     uint32_t w = 0;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        int q = quant_one(v[e], d, -8.0f, 7.0f) + 8;
-        w |= (uint32_t)q << (4 * e);
-    }
+    for (int e = 0; e < 8; ++e) w |= (uint32_t)(q[e] + 8) << (4 * e);
     return w;
 }
 

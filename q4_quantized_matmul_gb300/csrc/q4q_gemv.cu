@@ -81,13 +81,15 @@ __device__ __forceinline__ int block_dot(const uint32_t (&q)[4], const uint4& ye
 
 // Quantize 8 consecutive activations (elements 8i..8i+7 of one block) to Q8_0
 // and split them into the even word (elements 8i, 8i+2, 8i+4, 8i+6) and the odd
-// word (8i+1, ...).  Returns sum of the 8 codes.
+// word (8i+1, ...).  Returns sum of the 8 codes.  All 32 lanes must call it.
 __device__ __forceinline__ int quant_q8_split(const float (&v)[8], float d, uint32_t& ye, uint32_t& yo) {
     int s = 0;
     ye = 0; yo = 0;
+    int qv[8];
+    quant8(v, d, -127.0f, 127.0f, qv);
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-        const int q = quant_one(v[e], d, -127.0f, 127.0f);
+        const int q = qv[e];
         s += q;
         const uint32_t b = (uint32_t)(q & 0xff);
         if (e & 1) yo |= b << (8 * (e >> 1));
@@ -207,39 +209,52 @@ gemv_q4_0_kernel(const uint8_t* __restrict__ w, const float* __restrict__ x, flo
     // ---------------- consumers: activations first (they may come from the previous kernel)
     pdl_wait();
     {
+        // Each thread owns 8 consecutive activations of one block per item; the
+        // loads of U items are issued together so that their L2 latencies overlap.
+        constexpr int U = 4;
         const int per_tok = p.nb * 4;
-        const int total = T * per_tok;
-        for (int m0 = 0; m0 < total; m0 += CONSUMERS) {
-            const int m = m0 + tid;
-            const bool ok = m < total;
-            const int t = ok ? m / per_tok : 0;
-            const int rem = m - t * per_tok;
-            const int b = rem >> 2, i = rem & 3;
-            float v[8];
-            if (ok) {
-                const float4* src = reinterpret_cast<const float4*>(x + (int64_t)t * p.ne00 + b * QK + i * 8);
-                const float4 a = __ldg(src), c = __ldg(src + 1);
-                v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-                v[4] = c.x; v[5] = c.y; v[6] = c.z; v[7] = c.w;
-            } else {
+        const int total = T * per_tok;               // a multiple of 32: warps stay uniform
+        for (int m0 = 0; m0 < total; m0 += CONSUMERS * U) {
+            float4 va[U], vb[U];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] = 0.0f;
+            for (int u = 0; u < U; ++u) {
+                const int m = m0 + u * CONSUMERS + tid;
+                if (m < total) {
+                    const int t = m / per_tok, rem = m - t * per_tok;
+                    const float4* src =
+                        reinterpret_cast<const float4*>(x + (int64_t)t * p.ne00 + (rem >> 2) * QK + (rem & 3) * 8);
+                    va[u] = __ldg(src);
+                    vb[u] = __ldg(src + 1);
+                } else {
+                    va[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    vb[u] = va[u];
+                }
             }
-            float amax = 0.0f;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(v[e]));
-            amax = warp_max4(amax);
-            const float d = __fdiv_rn(amax, 127.0f);
-            uint32_t ye, yo;
-            int sq = quant_q8_split(v, d, ye, yo);
-            sq = warp_sum4(sq);
-            if (ok) {
-                const int qi = (t * 4 + (b & 1) * 2) * p.np + (b >> 1);
-                reinterpret_cast<uint32_t*>(&quads[qi])[i] = ye;
-                reinterpret_cast<uint32_t*>(&quads[qi + p.np])[i] = yo;
-                if (i == 0) {
-                    dy[t * p.nb + b] = fp16_to_f32(fp16_bits(d));
-                    sy8[t * p.nb + b] = 8 * sq;
+            for (int u = 0; u < U; ++u) {
+                const int m = m0 + u * CONSUMERS + tid;
+                if (m0 + u * CONSUMERS >= total) break;    // uniform across the CTA
+                const bool ok = m < total;
+                const int t = ok ? m / per_tok : 0;
+                const int rem = m - t * per_tok;
+                const int b = rem >> 2, i = rem & 3;
+                const float v[8] = {va[u].x, va[u].y, va[u].z, va[u].w, vb[u].x, vb[u].y, vb[u].z, vb[u].w};
+                float amax = 0.0f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(v[e]));
+                amax = warp_max4(amax);
+                const float d = __fdiv_rn(amax, 127.0f);
+                uint32_t ye, yo;
+                int sq = quant_q8_split(v, d, ye, yo);
+                sq = warp_sum4(sq);
+                if (ok) {
+                    const int qi = (t * 4 + (b & 1) * 2) * p.np + (b >> 1);
+                    reinterpret_cast<uint32_t*>(&quads[qi])[i] = ye;
+                    reinterpret_cast<uint32_t*>(&quads[qi + p.np])[i] = yo;
+                    if (i == 0) {
+                        dy[t * p.nb + b] = fp16_to_f32(fp16_bits(d));
+                        sy8[t * p.nb + b] = 8 * sq;
+                    }
                 }
             }
         }

@@ -95,15 +95,16 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         : "r"(taddr));
 }
 
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+}
+
+template <int CK>
+__device__ __forceinline__ void tmem_ld_chunk(uint32_t taddr, uint32_t (&r)[CK]) {
+    if constexpr (CK == 8) tmem_ld8(taddr, r);
+    else tmem_ld16(taddr, r);
 }
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
@@ -403,59 +404,105 @@ mma_q4_0_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
         const int m = m0 + row;
         const int col0 = h * C::CPW;
         const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
-        uint64_t acc[C::CPW / 2];
+        if constexpr (DEBUG) {
+            for (int g = 0; g < n_slab; ++g) {
+                const int buf = g % NBUF;
+                const int i = g >> 1, s = i % AB_STAGES, j = g & 1;
+                if (!warp_wait(slab_full + 8 * buf, (g / NBUF) & 1, abort_flag, lane)) break;
+                tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < C::CPW / 2; ++c) acc[c] = 0;
-        for (int g = 0; g < n_slab; ++g) {
-            const int buf = g % NBUF;
-            const int i = g >> 1, s = i % AB_STAGES, j = g & 1;
-            if (!warp_wait(slab_full + 8 * buf, (g / NBUF) & 1, abort_flag, lane)) break;
-            // the stage's weight scales were written before ab_full completed
-            if (j == 0 && !warp_wait(ab_full + 8 * s, (i / AB_STAGES) & 1, abort_flag, lane)) break;
-            tc_fence_after();
-            const float dwm = dw_s[(s * 2 + j) * BM + row];
-            const uint64_t dw2 = pack2(dwm, dwm);
-            const float4* dxs = reinterpret_cast<const float4*>(dx_s + (s * 2 + j) * NT + col0);
-            constexpr int CH = C::CPW >= 32 ? 32 : 16;     // columns per TMEM load round trip
+                for (int c0 = 0; c0 < C::CPW; c0 += 8) {
+                    uint32_t r[8];
+                    tmem_ld8(tq + (uint32_t)(buf * NT + col0 + c0), r);
+                    tmem_ld_wait();
 #pragma unroll
-            for (int c0 = 0; c0 < C::CPW; c0 += CH) {
-                uint32_t r[CH];
-                if constexpr (CH == 32) tmem_ld32(tq + (uint32_t)(buf * NT + col0 + c0), r);
-                else tmem_ld16(tq + (uint32_t)(buf * NT + col0 + c0), r);
-                tmem_ld_wait();
-                if (DEBUG) {
-#pragma unroll
-                    for (int c = 0; c < CH; ++c) {
+                    for (int c = 0; c < 8; ++c) {
                         const int n = n0 + col0 + c0 + c;
                         if (n < p.N && m < p.M)
                             p.isums[((size_t)n * p.M + m) * p.nb + g] = (int32_t)__uint_as_float(r[c]);
                     }
-                } else {
-#pragma unroll
-                    for (int c = 0; c < CH; c += 4) {
-                        const float4 d4 = dxs[(c0 + c) >> 2];
-                        const uint64_t s01 = pack2(__uint_as_float(r[c]), __uint_as_float(r[c + 1]));
-                        const uint64_t s23 = pack2(__uint_as_float(r[c + 2]), __uint_as_float(r[c + 3]));
-                        acc[(c0 + c) >> 1] = ffma2(fmul2(dw2, pack2(d4.x, d4.y)), s01, acc[(c0 + c) >> 1]);
-                        acc[((c0 + c) >> 1) + 1] = ffma2(fmul2(dw2, pack2(d4.z, d4.w)), s23, acc[((c0 + c) >> 1) + 1]);
-                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(slab_empty + 8 * buf);
+                    if (j == 1) mbar_arrive(ab_empty + 8 * s);
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(slab_empty + 8 * buf);
-                if (j == 1) mbar_arrive(ab_empty + 8 * s);
-            }
-        }
-        if (!DEBUG && !*abort_flag && m < p.M) {
+        } else {
+            // Software pipeline over 16-column chunks (8 for the narrowest tile): the
+            // TMEM load of the next chunk -- crossing into the next slab when needed --
+            // is in flight while the current chunk is scaled and accumulated.
+            constexpr int CK = C::CPW >= 32 ? 16 : 8;
+            constexpr int NC = C::CPW / CK;          // chunks per slab, even
+            static_assert(NC % 2 == 0, "chunk double-buffering needs an even count");
+            uint64_t acc[C::CPW / 2];
 #pragma unroll
-            for (int c = 0; c < C::CPW / 2; ++c) {
-                float x0, x1;
-                unpack2(acc[c], x0, x1);
-                const int n = n0 + col0 + 2 * c;
-                if (n < p.N) p.dst[(size_t)n * p.M + m] = x0;
-                if (n + 1 < p.N) p.dst[(size_t)(n + 1) * p.M + m] = x1;
+            for (int c = 0; c < C::CPW / 2; ++c) acc[c] = 0;
+            uint32_t ra[CK], rb[CK];
+            bool aborted = !warp_wait(slab_full, 0, abort_flag, lane) ||
+                           !warp_wait(ab_full, 0, abort_flag, lane);
+            if (!aborted) {
+                tc_fence_after();
+                tmem_ld_chunk<CK>(tq + (uint32_t)col0, ra);
+                tmem_ld_wait();
+            }
+            for (int g = 0; g < n_slab && !aborted; ++g) {
+                const int buf = g % NBUF;
+                const int i = g >> 1, s = i % AB_STAGES, j = g & 1;
+                const float dwm = dw_s[(s * 2 + j) * BM + row];
+                const uint64_t dw2 = pack2(dwm, dwm);
+                const float4* dxs = reinterpret_cast<const float4*>(dx_s + (s * 2 + j) * NT + col0);
+#pragma unroll
+                for (int c = 0; c < NC; ++c) {
+                    uint32_t (&cur)[CK] = (c & 1) ? rb : ra;
+                    uint32_t (&nxt)[CK] = (c & 1) ? ra : rb;
+                    if (c + 1 < NC) {
+                        tmem_ld_chunk<CK>(tq + (uint32_t)(buf * NT + col0 + (c + 1) * CK), nxt);
+                    } else {
+                        // every load of slab g has completed: hand its TMEM buffer back
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(slab_empty + 8 * buf);
+                        const int g1 = g + 1;
+                        if (g1 < n_slab) {
+                            const int i1 = g1 >> 1;
+                            if (!warp_wait(slab_full + 8 * (g1 % NBUF), (g1 / NBUF) & 1, abort_flag, lane) ||
+                                ((g1 & 1) == 0 &&
+                                 !warp_wait(ab_full + 8 * (i1 % AB_STAGES), (i1 / AB_STAGES) & 1, abort_flag, lane))) {
+                                aborted = true;
+                            } else {
+                                tc_fence_after();
+                                tmem_ld_chunk<CK>(tq + (uint32_t)((g1 % NBUF) * NT + col0), nxt);
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int cc = 0; cc < CK; cc += 4) {
+                        const float4 d4 = dxs[(c * CK + cc) >> 2];
+                        const int a0 = (c * CK + cc) >> 1;
+                        acc[a0] = ffma2(fmul2(dw2, pack2(d4.x, d4.y)),
+                                        pack2(__uint_as_float(cur[cc]), __uint_as_float(cur[cc + 1])), acc[a0]);
+                        acc[a0 + 1] = ffma2(fmul2(dw2, pack2(d4.z, d4.w)),
+                                            pack2(__uint_as_float(cur[cc + 2]), __uint_as_float(cur[cc + 3])), acc[a0 + 1]);
+                    }
+                    tmem_ld_wait();
+                }
+                // the stage's scales have been read for both of its slabs
+                if (j == 1) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(ab_empty + 8 * s);
+                }
+            }
+            if (!aborted && !*abort_flag && m < p.M) {
+#pragma unroll
+                for (int c = 0; c < C::CPW / 2; ++c) {
+                    float x0, x1;
+                    unpack2(acc[c], x0, x1);
+                    const int n = n0 + col0 + 2 * c;
+                    if (n < p.N) p.dst[(size_t)n * p.M + m] = x0;
+                    if (n + 1 < p.N) p.dst[(size_t)(n + 1) * p.M + m] = x1;
+                }
             }
         }
     }
@@ -496,12 +543,14 @@ act_to_mma_kernel(const float* __restrict__ x, __half* __restrict__ bmat, float*
         for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(v[e]));
         amax = warp_max4(amax);
         const float d = __fdiv_rn(amax, 127.0f);
+        int qv[8];
+        quant8(v, d, -127.0f, 127.0f, qv);          // every lane takes part (warp vote inside)
         if (ok) {
             uint32_t hw[4];
 #pragma unroll
             for (int pp = 0; pp < 4; ++pp) {
-                const int q0 = quant_one(v[perm8(2 * pp)], d, -127.0f, 127.0f);
-                const int q1 = quant_one(v[perm8(2 * pp + 1)], d, -127.0f, 127.0f);
+                const int q0 = qv[perm8(2 * pp)];
+                const int q1 = qv[perm8(2 * pp + 1)];
                 const __half2 hv = __halves2half2(__int2half_rn(q0), __int2half_rn(q1));
                 hw[pp] = *reinterpret_cast<const uint32_t*>(&hv);
             }

@@ -56,13 +56,12 @@ quantize_fast_kernel(const float* __restrict__ src, uint8_t* __restrict__ dst, i
             if (part == 0) *reinterpret_cast<uint16_t*>(sb) = fp16_bits(d);
         } else {
             const float d = __fdiv_rn(amax, 127.0f);
+            int qv[8];
+            quant8(v, d, -127.0f, 127.0f, qv);
             uint16_t* q = reinterpret_cast<uint16_t*>(sb + 2 + 8 * part);
 #pragma unroll
-            for (int e = 0; e < 8; e += 2) {
-                const uint32_t q0 = (uint32_t)(quant_one(v[e], d, -127.0f, 127.0f) & 0xff);
-                const uint32_t q1 = (uint32_t)(quant_one(v[e + 1], d, -127.0f, 127.0f) & 0xff);
-                q[e >> 1] = (uint16_t)(q0 | (q1 << 8));
-            }
+            for (int e = 0; e < 8; e += 2)
+                q[e >> 1] = (uint16_t)((uint32_t)(qv[e] & 0xff) | ((uint32_t)(qv[e + 1] & 0xff) << 8));
             if (part == 0) *reinterpret_cast<uint16_t*>(sb) = fp16_bits(d);
         }
         __syncthreads();

@@ -91,6 +91,53 @@ def test_quantize_misaligned_buffers(q4q, kind):
     assert dst[0].item() == 0
 
 
+def _near_tie_rows(rng, levels, nrows):
+    """Blocks whose quotients x/d sit within a few ulps of half-integers (the
+    places where round-half-away-from-zero is decided), for random scales."""
+    rows = []
+    for _ in range(nrows):
+        amax = np.float32(rng.uniform(0.01, 100.0))
+        d = np.float32(amax / np.float32(levels))
+        blk = np.empty(32, np.float32)
+        blk[0] = -amax if levels == 8 else amax
+        for j in range(1, 32):
+            k = rng.integers(-levels, levels) + 0.5
+            x = np.float32(k * np.float64(d))
+            for _ in range(int(rng.integers(-3, 4))):
+                x = np.nextafter(x, np.float32(np.inf) if rng.random() < 0.5 else np.float32(-np.inf))
+            blk[j] = x if abs(x) <= amax else np.float32(np.sign(x) * amax)
+        rows.append(blk)
+    return np.stack(rows).reshape(nrows // 8, 256)
+
+
+@pytest.mark.parametrize("kind", ["q4_0", "q8_0"])
+def test_quantize_near_ties_bit_exact(q4q, kind):
+    rng = np.random.default_rng(31)
+    levels = 8 if kind == "q4_0" else 127
+    w = _near_tie_rows(rng, levels, 4096)
+    fn = q4q.q4q_quantize_q4_0 if kind == "q4_0" else q4q.q4q_quantize_q8_0
+    ref = oracle.quantize_q4_0(w) if kind == "q4_0" else oracle.quantize_q8_0(w)
+    np.testing.assert_array_equal(fn(dev(w)).cpu().numpy(), ref)
+
+
+def test_mul_mat_near_tie_activations(q4q):
+    # the activation quantization inside both mul_mat paths meets the same ties
+    rng = np.random.default_rng(32)
+    x = _near_tie_rows(rng, 127, 512).reshape(-1, 1024)
+    assert x.shape == (16, 1024)
+    ne00 = 1024
+    w = (rng.standard_normal((300, ne00)) * 0.02).astype(np.float32)
+    wq = oracle.quantize_q4_0(w)
+    for ne11 in (1, 3, 16):
+        got = q4q.q4q_mul_mat(dev(wq), ne00, 300, dev(x[:ne11])).cpu().numpy()
+        ref, scale = oracle.mul_mat(wq, ne00, 300, x[:ne11])
+        assert_close(got, ref, scale)
+    xq = oracle.quantize_q8_0(x[:16])
+    for path in (0, 1):
+        got = q4q.q4q_debug_block_isums(dev(wq), dev(xq), ne00, 300, 16, path=path).cpu().numpy()
+        np.testing.assert_array_equal(got, oracle.block_isums(wq, xq, ne00, 300, 16))
+
+
 def test_quantize_hand_block(q4q):
     w = ((np.arange(32) - 16) * 0.25).astype(np.float32).reshape(1, 32)
     got = q4q.q4q_quantize_q4_0(dev(w)).cpu().numpy()
