@@ -7,8 +7,11 @@ by the resident Q4_0 weights (one q4q_mul_mat call per matrix, captured once in
 a CUDA graph and replayed).  Weight quantization (Q4_0 encode) happens once
 before timing, as a model load would do it, and is timed separately.
 
-Default workload: GPT-2 117M decode-step weight set at 1 token (12 layers x
-{768->2304, 768->768, 768->3072, 3072->768} + lm_head 768->50257), seed 1.
+Default workload: the Llama-3-8B-shaped decode projections at 1 token (q, k, v,
+o, gate, up, down, lm_head; 418 MB of Q4_0 weights), seed 2 -- the set the 1-token
+GEMV target is judged on.  The same JSON line also carries the GPT-2 117M
+decode-step weight set (49 small matrices, launch-latency bound) and the
+tensor-core path at 512 tokens.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
 
@@ -252,8 +255,10 @@ def run_ours(args, rank, world, local_rank):
                 b.record(stream)
                 evs.append((i, a, b))
     torch.cuda.synchronize()
+    per_shape = {}
     for i, a, b in evs:
         per_ms.append(a.elapsed_time(b))
+        per_shape.setdefault(i, []).append(a.elapsed_time(b))
     reps = len(per_ms) // nmat
     kern_ms_per_step = sum(per_ms) / reps
     act_bytes = sum(4 * k * ne11 for k, n in shapes)
@@ -315,6 +320,8 @@ def run_ours(args, rank, world, local_rank):
     e2e_value = world * wbytes * args.steps / (ems * 1e-3) / 1e9
 
     batched = measure_batched(dev, stream, args) if (rank == 0 and args.batched_tokens > 0) else None
+    second = (measure_decode(dev, stream, args.secondary_decode)
+              if (rank == 0 and args.secondary_decode and args.secondary_decode != args.workload) else None)
 
     # ---- CPU baseline: the oracle on this host's cores, bounded sample
     cpu = cpu_baseline(args.workload, ne11, budget_s=args.cpu_seconds) if (rank == 0 and args.cpu_seconds > 0) else None
@@ -358,6 +365,9 @@ def run_ours(args, rank, world, local_rank):
             "traffic": (traffic_step / nmat) if traffic_step else None,
             "algorithmic_bytes_per_launch": alg_bytes_step / nmat,
             "avg_launch_us": round(kern_ms_per_step * 1e3 / nmat, 3),
+            "per_launch": [{"shape": "%d->%d" % shapes[i], "us": round(1e3 * statistics.median(v), 2),
+                            "gb_s": round(_weights_bytes([shapes[i]]) / (1e-3 * statistics.median(v)) / 1e9, 1)}
+                           for i, v in sorted(per_shape.items())],
             "note": "achieved = algorithmic bytes (Q4_0 weights + fp32 activations + fp32 outputs) of the "
                     "step's launches / their summed CUDA-event durations (each launch bracketed by events, "
                     "L2-cold weight copies)",
@@ -371,8 +381,66 @@ def run_ours(args, rank, world, local_rank):
         "cpu_baseline": cpu,
         "clocks": clocks,
         "batched": batched,
+        "secondary_decode": second,
     }
     return line
+
+
+def measure_decode(dev, stream, name, steps=300):
+    """A second 1-token workload, timed like the main one: weight copies > 3 x L2,
+    one CUDA graph per copy of PDL-chained q4q_mul_mat calls."""
+    import torch
+
+    import q4_quantized_matmul_gb300 as q4q
+    from q4_quantized_matmul_gb300 import workloads
+    wl = workloads.WORKLOADS[name]
+    shapes = list(wl.shapes)
+    wq, xs, ds = [], [], []
+    for i, (ne00, ne01) in enumerate(shapes):
+        w, x = workloads.problem(name, i, 1)
+        wd = torch.from_numpy(w).to(dev)
+        wq.append(q4q.q4q_quantize_q4_0(wd))
+        del wd
+        xs.append(torch.from_numpy(x).to(dev))
+        ds.append(torch.empty((1, ne01), dtype=torch.float32, device=dev))
+    wbytes = _weights_bytes(shapes)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    copies = max(2, -(-3 * l2 // wbytes))
+    wsets = [wq] + [[t.clone() for t in wq] for _ in range(copies - 1)]
+
+    def step(c):
+        for i, (ne00, ne01) in enumerate(shapes):
+            q4q.q4q_mul_mat(wsets[c][i], ne00, ne01, xs[i], dst=ds[i], flags=q4q.Q4Q_MUL_MAT_PDL)
+
+    with torch.cuda.stream(stream):
+        for c in range(copies):
+            step(c)
+    torch.cuda.synchronize()
+    graphs = []
+    for c in range(copies):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step(c)
+        graphs.append(g)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for k in range(10):
+            graphs[k % copies].replay()
+        e0.record(stream)
+        for k in range(steps):
+            graphs[k % copies].replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    peak, kind = _measured_peaks()
+    gbs = wbytes / (ms * 1e-3) / 1e9
+    out = {"workload": name, "description": wl.description, "value": round(gbs, 1), "unit": "GB/s",
+           "ms_per_step": round(ms, 5), "frac_of_hbm": round(gbs / peak, 4), "matrices": len(shapes),
+           "us_per_matrix": round(ms * 1e3 / len(shapes), 3),
+           "note": "dependent-chain launch (PDL), one kernel per matrix; small matrices are launch-latency bound"}
+    del wsets, wq, xs, ds
+    torch.cuda.empty_cache()
+    return out
 
 
 def measure_batched(dev, stream, args):
@@ -569,7 +637,9 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="gpt2_decode_step")
+    ap.add_argument("--workload", default="llama3_8b_decode")
+    ap.add_argument("--secondary-decode", default="gpt2_decode_step",
+                    help="also time this 1-token workload (empty = skip)")
     ap.add_argument("--ne11", type=int, default=0, help="override the workload's token count")
     ap.add_argument("--soak", type=float, default=1.5, help="seconds of untimed load before warm-up")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline budget (0 = skip)")

@@ -47,6 +47,20 @@ __device__ __forceinline__ int quant_one(float x, float d, float lo, float hi) {
     return (int)r;
 }
 
+// Block scales without a division.  amax / 8 is exactly amax * 0.125 (a power of
+// two).  For amax / 127: with C = fl(1/127), q = fl(amax * C) and the exact
+// remainder r = fma(-q, 127, amax), fma(r, C, q) is the correctly rounded
+// quotient; this was checked against IEEE division for every positive finite
+// binary32 amax (the CPU test suite re-checks a strided sample of them).
+__device__ __forceinline__ float scale_q4(float amax) { return __fmul_rn(amax, 0.125f); }
+
+__device__ __forceinline__ float scale_q8(float amax) {
+    const float C = 0x1.020408p-7f;                  // fl(1/127)
+    const float q = __fmul_rn(amax, C);
+    const float r = __fmaf_rn(-q, 127.0f, amax);
+    return __fmaf_rn(r, C, q);
+}
+
 // Hardware reciprocal (about 1 ulp); only ever used inside quant8's error
 // budget, never as a stored value.
 __device__ __forceinline__ float recip_approx(float d) {

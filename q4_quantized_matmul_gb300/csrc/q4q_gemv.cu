@@ -243,7 +243,7 @@ gemv_q4_0_kernel(const uint8_t* __restrict__ w, const float* __restrict__ x, flo
 #pragma unroll
                 for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(v[e]));
                 amax = warp_max4(amax);
-                const float d = __fdiv_rn(amax, 127.0f);
+                const float d = scale_q8(amax);
                 uint32_t ye, yo;
                 int sq = quant_q8_split(v, d, ye, yo);
                 sq = warp_sum4(sq);

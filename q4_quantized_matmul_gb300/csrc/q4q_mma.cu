@@ -18,7 +18,8 @@
 //                 box = 64 K x NT tokens) into a 4-deep ring
 //   warps 4-7   : dequantizers: raw Q4_0 -> fp16 A tile (128 rows x 64 K) in the
 //                 canonical K-major 128-byte-swizzle layout, plus the fp32 block scales
-//   warps 8..   : epilogue: per 32-K slab, tcgen05.ld the fp32 slab, acc += d_w d_x S
+//   warps 8..   : epilogue, NT/32 warps per TMEM lane quadrant: per 32-K slab each warp
+//                 loads its 32 columns with one tcgen05.ld and applies acc += d_w d_x S
 // K order inside every 8-element group is permuted the same way on both operands
 // ([0,4,1,5,2,6,3,7]) so that a 32-bit word of nibbles turns into fp16 with a
 // handful of bit operations; the dot product does not depend on that order.
@@ -101,10 +102,22 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
                  : "r"(taddr));
 }
 
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
 template <int CK>
 __device__ __forceinline__ void tmem_ld_chunk(uint32_t taddr, uint32_t (&r)[CK]) {
     if constexpr (CK == 8) tmem_ld8(taddr, r);
-    else tmem_ld16(taddr, r);
+    else if constexpr (CK == 16) tmem_ld16(taddr, r);
+    else tmem_ld32(taddr, r);
 }
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
@@ -145,16 +158,13 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
     }
 }
 
-// Lane 0 waits (bounded), the verdict is broadcast, and every lane then takes
-// its own acquire of the completed phase (which cannot advance before this warp
-// arrives on the matching "empty" barrier).
+// Every lane polls the barrier itself (each gets its own acquire of the completed
+// phase, which cannot advance before this warp arrives on the matching "empty"
+// barrier); a single vote makes the verdict warp-uniform.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int lane) {
-    int ok = 1;
-    if (lane == 0) ok = wait_or_abort(bar, parity, abort_flag) ? 1 : 0;
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (ok) mbar_try_wait(bar, parity);
-    __syncwarp();
-    return ok != 0;
+    (void)lane;
+    const bool ok = mbar_try_wait(bar, parity) || wait_or_abort(bar, parity, abort_flag);
+    return __all_sync(0xffffffffu, ok);
 }
 
 // Q4_0 nibble word (elements e0..e7 at bits 4e) -> 8 fp16 values (e - 8) in the
@@ -212,7 +222,8 @@ __device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
 
 template <int NT>
 struct Cfg {
-    static constexpr int EPI_WARPS = NT >= 128 ? 8 : 4;
+    // epilogue warps: NT/32 per TMEM lane quadrant (each owns 32 columns), at least one
+    static constexpr int EPI_WARPS = NT >= 128 ? 16 : (NT >= 64 ? 8 : 4);
     static constexpr int CPW = NT * 4 / EPI_WARPS;       // columns per epilogue warp
     static constexpr int THREADS = (8 + EPI_WARPS) * 32;
     static constexpr int B_BYTES = NT * KAB * 2;
@@ -239,7 +250,9 @@ mma_q4_0_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
     using C = Cfg<NT>;
     constexpr int NBUF = C::NBUF;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // align to 1024 bytes by pointer arithmetic on the shared array itself, so the
+    // compiler keeps every derived pointer in the shared address space
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(smem);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     const uint32_t raw_full = smem_u32(&bars[0]);
@@ -350,9 +363,8 @@ mma_q4_0_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
             }
         }
     } else if (warp >= 4 && warp < 8) {
-        // ---------------- dequantizers: thread t <-> tile row t; a row's 8 raw blocks
-        // (144 bytes) are read with nine 16-byte loads (row pitch 144 bytes keeps the
-        // eight lanes of each load phase on distinct banks)
+        // ---------------- dequantizers: thread t <-> tile row t; each A/B stage needs
+        // one pair of the row's 8 raw blocks, read as three 16-byte loads
         const int t = threadIdx.x - 128;
         const int rsw = t & 7;
         bool ok = true;
@@ -360,12 +372,6 @@ mma_q4_0_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
             const int st = r % RAW_STAGES;
             if (!warp_wait(raw_full + 8 * st, (r / RAW_STAGES) & 1, abort_flag, lane)) { ok = false; break; }
             const uint4* rowp = reinterpret_cast<const uint4*>(smem + C::OFF_RAW + st * RAW_BYTES + t * 144);
-            uint32_t wv[36];
-#pragma unroll
-            for (int k = 0; k < 9; ++k) {
-                const uint4 v = rowp[k];
-                wv[4 * k + 0] = v.x; wv[4 * k + 1] = v.y; wv[4 * k + 2] = v.z; wv[4 * k + 3] = v.w;
-            }
 #pragma unroll
             for (int a = 0; a < KRAW / KAB; ++a) {
                 const int i = r * (KRAW / KAB) + a;
@@ -374,18 +380,27 @@ mma_q4_0_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                     ok = false;
                     break;
                 }
-                // pair a = blocks 2a, 2a+1 = words 9a .. 9a+8 of the row
+                // pair a = blocks 2a, 2a+1 = words 9a .. 9a+8 of the row, inside the three
+                // 16-byte chunks (9a)/4 .. (9a)/4 + 2 (16-byte loads keep the eight lanes
+                // of each load phase on distinct banks: the row pitch is 144 bytes)
+                uint32_t wv[12];
+#pragma unroll
+                for (int k = 0; k < 3; ++k) {
+                    const uint4 v4 = rowp[(9 * a) / 4 + k];
+                    wv[4 * k + 0] = v4.x; wv[4 * k + 1] = v4.y; wv[4 * k + 2] = v4.z; wv[4 * k + 3] = v4.w;
+                }
+                const int w0 = (9 * a) % 4;                  // first word of the pair (compile time)
                 uint32_t q[8];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) q[k] = __byte_perm(wv[9 * a + k], wv[9 * a + k + 1], 0x5432);
+                for (int k = 0; k < 4; ++k) q[k] = __byte_perm(wv[w0 + k], wv[w0 + k + 1], 0x5432);   // block 2a
 #pragma unroll
-                for (int k = 0; k < 4; ++k) q[4 + k] = wv[9 * a + 5 + k];
+                for (int k = 0; k < 4; ++k) q[4 + k] = wv[w0 + 5 + k];                              // block 2a+1
                 uint8_t* atile = smem + C::OFF_A + s * A_BYTES + (t >> 3) * 1024 + rsw * 128;
 #pragma unroll
                 for (int c = 0; c < 8; ++c)
                     *reinterpret_cast<uint4*>(atile + ((c ^ rsw) << 4)) = nibbles_to_f16x8(q[c]);
-                dw_s[(s * 2 + 0) * BM + t] = fp16_to_f32(wv[9 * a]);
-                dw_s[(s * 2 + 1) * BM + t] = fp16_to_f32(wv[9 * a + 4] >> 16);
+                dw_s[(s * 2 + 0) * BM + t] = fp16_to_f32(wv[w0]);
+                dw_s[(s * 2 + 1) * BM + t] = fp16_to_f32(wv[w0 + 4] >> 16);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(ab_full + 8 * s);
@@ -430,63 +445,41 @@ mma_q4_0_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                 }
             }
         } else {
-            // Software pipeline over 16-column chunks (8 for the narrowest tile): the
-            // TMEM load of the next chunk -- crossing into the next slab when needed --
-            // is in flight while the current chunk is scaled and accumulated.
-            constexpr int CK = C::CPW >= 32 ? 16 : 8;
-            constexpr int NC = C::CPW / CK;          // chunks per slab, even
-            static_assert(NC % 2 == 0, "chunk double-buffering needs an even count");
+            // One TMEM round trip per slab per warp (its CPW <= 32 columns); the
+            // NT/32 warps that share a lane quadrant overlap their load latencies.
+            constexpr int CK = C::CPW;
+            static_assert(CK == 16 || CK == 32, "one load per slab");
             uint64_t acc[C::CPW / 2];
 #pragma unroll
             for (int c = 0; c < C::CPW / 2; ++c) acc[c] = 0;
-            uint32_t ra[CK], rb[CK];
-            bool aborted = !warp_wait(slab_full, 0, abort_flag, lane) ||
-                           !warp_wait(ab_full, 0, abort_flag, lane);
-            if (!aborted) {
-                tc_fence_after();
-                tmem_ld_chunk<CK>(tq + (uint32_t)col0, ra);
-                tmem_ld_wait();
-            }
-            for (int g = 0; g < n_slab && !aborted; ++g) {
+            bool aborted = false;
+            for (int g = 0; g < n_slab; ++g) {
                 const int buf = g % NBUF;
                 const int i = g >> 1, s = i % AB_STAGES, j = g & 1;
+                if (!warp_wait(slab_full + 8 * buf, (g / NBUF) & 1, abort_flag, lane) ||
+                    (j == 0 && !warp_wait(ab_full + 8 * s, (i / AB_STAGES) & 1, abort_flag, lane))) {
+                    aborted = true;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t r[CK];
+                tmem_ld_chunk<CK>(tq + (uint32_t)(buf * NT + col0), r);
                 const float dwm = dw_s[(s * 2 + j) * BM + row];
                 const uint64_t dw2 = pack2(dwm, dwm);
                 const float4* dxs = reinterpret_cast<const float4*>(dx_s + (s * 2 + j) * NT + col0);
+                tmem_ld_wait();
+                // the slab is in registers: hand its TMEM buffer back to the MMA issuer
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(slab_empty + 8 * buf);
 #pragma unroll
-                for (int c = 0; c < NC; ++c) {
-                    uint32_t (&cur)[CK] = (c & 1) ? rb : ra;
-                    uint32_t (&nxt)[CK] = (c & 1) ? ra : rb;
-                    if (c + 1 < NC) {
-                        tmem_ld_chunk<CK>(tq + (uint32_t)(buf * NT + col0 + (c + 1) * CK), nxt);
-                    } else {
-                        // every load of slab g has completed: hand its TMEM buffer back
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(slab_empty + 8 * buf);
-                        const int g1 = g + 1;
-                        if (g1 < n_slab) {
-                            const int i1 = g1 >> 1;
-                            if (!warp_wait(slab_full + 8 * (g1 % NBUF), (g1 / NBUF) & 1, abort_flag, lane) ||
-                                ((g1 & 1) == 0 &&
-                                 !warp_wait(ab_full + 8 * (i1 % AB_STAGES), (i1 / AB_STAGES) & 1, abort_flag, lane))) {
-                                aborted = true;
-                            } else {
-                                tc_fence_after();
-                                tmem_ld_chunk<CK>(tq + (uint32_t)((g1 % NBUF) * NT + col0), nxt);
-                            }
-                        }
-                    }
-#pragma unroll
-                    for (int cc = 0; cc < CK; cc += 4) {
-                        const float4 d4 = dxs[(c * CK + cc) >> 2];
-                        const int a0 = (c * CK + cc) >> 1;
-                        acc[a0] = ffma2(fmul2(dw2, pack2(d4.x, d4.y)),
-                                        pack2(__uint_as_float(cur[cc]), __uint_as_float(cur[cc + 1])), acc[a0]);
-                        acc[a0 + 1] = ffma2(fmul2(dw2, pack2(d4.z, d4.w)),
-                                            pack2(__uint_as_float(cur[cc + 2]), __uint_as_float(cur[cc + 3])), acc[a0 + 1]);
-                    }
-                    tmem_ld_wait();
+                for (int c = 0; c < CK / 4; ++c) {
+                    const float4 d4 = dxs[c];
+                    acc[2 * c] = ffma2(fmul2(dw2, pack2(d4.x, d4.y)),
+                                       pack2(__uint_as_float(r[4 * c]), __uint_as_float(r[4 * c + 1])), acc[2 * c]);
+                    acc[2 * c + 1] = ffma2(fmul2(dw2, pack2(d4.z, d4.w)),
+                                           pack2(__uint_as_float(r[4 * c + 2]), __uint_as_float(r[4 * c + 3])),
+                                           acc[2 * c + 1]);
                 }
                 // the stage's scales have been read for both of its slabs
                 if (j == 1) {
@@ -542,7 +535,7 @@ act_to_mma_kernel(const float* __restrict__ x, __half* __restrict__ bmat, float*
 #pragma unroll
         for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(v[e]));
         amax = warp_max4(amax);
-        const float d = __fdiv_rn(amax, 127.0f);
+        const float d = scale_q8(amax);
         int qv[8];
         quant8(v, d, -127.0f, 127.0f, qv);          // every lane takes part (warp vote inside)
         if (ok) {

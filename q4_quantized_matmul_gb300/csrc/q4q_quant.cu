@@ -48,14 +48,14 @@ quantize_fast_kernel(const float* __restrict__ src, uint8_t* __restrict__ dst, i
         amax = warp_max4(amax);
         uint8_t* sb = stage + bl * BB;
         if (IS_Q4) {
-            const float d = __fdiv_rn(amax, 8.0f);
+            const float d = scale_q4(amax);
             const uint32_t w = pack_q4_word(v, d);
             uint16_t* q = reinterpret_cast<uint16_t*>(sb + 2 + 4 * part);
             q[0] = (uint16_t)(w & 0xffffu);
             q[1] = (uint16_t)(w >> 16);
             if (part == 0) *reinterpret_cast<uint16_t*>(sb) = fp16_bits(d);
         } else {
-            const float d = __fdiv_rn(amax, 127.0f);
+            const float d = scale_q8(amax);
             int qv[8];
             quant8(v, d, -127.0f, 127.0f, qv);
             uint16_t* q = reinterpret_cast<uint16_t*>(sb + 2 + 8 * part);
