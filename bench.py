@@ -127,6 +127,24 @@ class ClockSampler:
                 "power_w_max": max(r["power"] for r in rows)}
 
 
+# ------------------------------------------------------- cross-rank logic ---
+
+def max_over_ranks(ms: float, world: int, device=None) -> float:
+    """Slowest rank's time (the job finishes when every replica has)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(bytes_per_rank_step: float, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job GB/s: every rank streams its own replica of the weights (weak scaling)."""
+    return world * bytes_per_rank_step * steps / (max_ms * 1e-3) / 1e9
+
+
 # --------------------------------------------------------------- the arms ---
 
 def _weights_bytes(shapes):
@@ -229,15 +247,11 @@ def run_ours(args, rank, world, local_rank):
         e1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     clocks = sampler.stop() if sampler else None
 
     ms_per_step = ms / args.steps
-    value = world * wbytes * args.steps / (ms * 1e-3) / 1e9
+    value = job_throughput(wbytes, args.steps, world, ms)
 
     # ---- per-launch durations of the mul_mat kernel (same calls, event-bracketed, L2-cold copies)
     per_ms = []
@@ -312,12 +326,8 @@ def run_ours(args, rank, world, local_rank):
         e1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    ems = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ems], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ems = float(t.item())
-    e2e_value = world * wbytes * args.steps / (ems * 1e-3) / 1e9
+    ems = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    e2e_value = job_throughput(wbytes, args.steps, world, ems)
 
     batched = measure_batched(dev, stream, args) if (rank == 0 and args.batched_tokens > 0) else None
     second = (measure_decode(dev, stream, args.secondary_decode)
