@@ -69,34 +69,76 @@ __device__ __forceinline__ float recip_approx(float d) {
     return r;
 }
 
-// quant_one for 8 values of one block, without a division on the common path.
-// inv = 1/d to within 2^-22 relative, so t = fl(x * inv) is within 6e-5 of
-// fl(x / d) (|x / d| <= 128 since |x| <= amax and d = amax / 8 or amax / 127).
-// Round-half-away and round-to-nearest-even differ only at half-integers, and
-// both are constant between them, so where t is more than 1e-3 away from a
-// half-integer rintf(t) == roundf(fl(x / d)).  Elements inside that band (or
-// with a non-finite t, e.g. a reciprocal flushed to infinity) take the exact
-// quotient; the warp vote keeps those divisions off the common path.
-// Must be called by all 32 lanes of the warp.
-__device__ __forceinline__ void quant8(const float (&v)[8], float d, float lo, float hi, int (&q)[8]) {
-    const float inv = recip_approx(d);
-    float r[8];
+// quant_one for N groups of 8 values (group n belongs to a block with scale
+// d[n]), without a division on the common path.  inv = rcp.approx(d) is within
+// 1 ulp (2^-23 relative) of 1/d, so t = fl(x * inv) is within 1.8e-7 |x / d| of
+// x / d, and fl(x / d) within half an ulp (<= 3.9e-6 for |x / d| <= 128) of
+// x / d: |t - fl(x / d)| <= 2.7e-5, since |x| <= amax and d = amax / 8 or amax /
+// 127 give |x / d| <= 127.0001.  Round-half-away and round-to-nearest-even differ
+// only at half-integers, and both are constant between them, so where t is more
+// than NEAR_BAND = 5e-5 away from every half-integer, round-to-nearest-even(t)
+// == roundf(fl(x / d)).  Elements inside that band (or with a non-finite t, e.g.
+// a reciprocal flushed to infinity) take the exact quotient; one warp vote over
+// all N groups keeps those divisions off the common path.  Must be called by all
+// 32 lanes of the warp.
+constexpr float NEAR_LIMIT = 0.49995f;            // 0.5 - NEAR_BAND
+//
+// RAW: the codes are only right in their low byte (the caller packs bytes and
+// handles d == 0 itself); for Q8_0, where no clamp is needed.
+template <int N, bool RAW = false>
+__device__ __forceinline__ void quant8n(const float (&v)[N][8], const float (&d)[N], float lo, float hi,
+                                        int (&q)[N][8]) {
+    // Round to nearest even by adding 1.5 * 2^23 (|t| <= 2^22 here): the integer
+    // lands in the low mantissa bits, so the code is the float's bit pattern minus
+    // that of the constant -- full-rate adds instead of rint/convert instructions.
+    constexpr float MAGIC = 12582912.0f;
+    constexpr int MAGIC_BITS = 0x4B400000;
+    float inv[N];
+#pragma unroll
+    for (int n = 0; n < N; ++n) inv[n] = recip_approx(d[n]);
     bool near = false;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        const float t = v[e] * inv;
-        r[e] = rintf(t);
-        near |= !(fabsf(t - r[e]) <= 0.499f);
-    }
-    if (__any_sync(0xffffffffu, near && d != 0.0f)) {
+    for (int n = 0; n < N; ++n) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            const float t = v[e] * inv;
-            if (d != 0.0f && !(fabsf(t - rintf(t)) <= 0.499f)) r[e] = roundf(__fdiv_rn(v[e], d));
+            const float t = v[n][e] * inv[n];
+            const float rm = __fadd_rn(t, MAGIC);
+            // MAGIC_BITS has zero low bytes: the raw bits already hold the code's low byte
+            q[n][e] = RAW ? __float_as_int(rm) : __float_as_int(rm) - MAGIC_BITS;
+            near |= !(fabsf(__fsub_rn(t, __fsub_rn(rm, MAGIC))) <= NEAR_LIMIT) && d[n] != 0.0f;
         }
     }
+    if (__any_sync(0xffffffffu, near)) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) q[e] = (d == 0.0f) ? 0 : (int)fminf(fmaxf(r[e], lo), hi);
+        for (int n = 0; n < N; ++n) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float t = v[n][e] * inv[n];
+                const float r = __fsub_rn(__fadd_rn(t, MAGIC), MAGIC);
+                if (d[n] != 0.0f && !(fabsf(__fsub_rn(t, r)) <= NEAR_LIMIT)) q[n][e] = (int)roundf(__fdiv_rn(v[n][e], d[n]));
+            }
+        }
+    }
+    // Codes stay inside [lo, hi] by construction except one: |x / d| <= 127.0001
+    // never rounds past 127 (Q8_0), and x / d >= -8 never below -8 (Q4_0), but
+    // x = +amax gives +8 in Q4_0, which the format stops at 7.
+    (void)lo;
+    if constexpr (RAW) return;
+    const int ihi = (int)hi;
+#pragma unroll
+    for (int n = 0; n < N; ++n) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            int c = q[n][e];
+            if (hi < 127.0f) c = min(c, ihi);
+            q[n][e] = (d[n] == 0.0f) ? 0 : c;
+        }
+    }
+}
+
+__device__ __forceinline__ void quant8(const float (&v)[8], float d, float lo, float hi, int (&q)[8]) {
+    quant8n<1>(reinterpret_cast<const float (&)[1][8]>(v), reinterpret_cast<const float (&)[1]>(d), lo, hi,
+               reinterpret_cast<int (&)[1][8]>(q));
 }
 
 __device__ __forceinline__ uint16_t fp16_bits(float d) {
@@ -190,6 +232,38 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
         ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
 }
+
+// ------------------------------------------------------ thread-block clusters --
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Address, in the shared::cluster window, of shared-memory address `addr` of this
+// CTA mapped into the CTA of rank `rank` of the cluster (same offset there).
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t d;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(addr), "r"(rank));
+    return d;
+}
+
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Cluster barrier (not .aligned: threads of one warp may take it separately).
+// arrive has release semantics, wait acquire: shared-memory stores a thread made
+// into any CTA of the cluster before its arrive are visible to every thread of
+// the cluster after its wait.  wait returns once every non-exited thread of the
+// cluster has arrived.
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait;" ::: "memory"); }
 
 __device__ __forceinline__ void record_error(unsigned int* word, unsigned int code) {
     atomicCAS(word, 0u, code);

@@ -23,6 +23,9 @@
 //    with the odd ones: isum = dp4a(lo, even) + dp4a(hi, odd) - 8 * sum(q).
 #include <algorithm>
 #include <atomic>
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include "q4q_common.cuh"
 #include "q4q_internal.h"
@@ -36,6 +39,7 @@ constexpr int THREADS = 288;            // 8 consumer warps + 1 producer warp
 constexpr int CONSUMERS = 256;
 constexpr int MAX_STAGES = 8;
 constexpr int PLAIN_THREADS = 256;      // generic and debug kernels
+constexpr int64_t CLUSTER_MIN_X = 8192;  // activations (elements) from which CTA pairs share the quantization
 
 struct GemvParams {
     int ne00, nb, np, ne01, row_bytes;
@@ -79,23 +83,129 @@ __device__ __forceinline__ int block_dot(const uint32_t (&q)[4], const uint4& ye
     return s;
 }
 
-// Quantize 8 consecutive activations (elements 8i..8i+7 of one block) to Q8_0
-// and split them into the even word (elements 8i, 8i+2, 8i+4, 8i+6) and the odd
-// word (8i+1, ...).  Returns sum of the 8 codes.  All 32 lanes must call it.
-__device__ __forceinline__ int quant_q8_split(const float (&v)[8], float d, uint32_t& ye, uint32_t& yo) {
-    int s = 0;
-    ye = 0; yo = 0;
-    int qv[8];
-    quant8(v, d, -127.0f, 127.0f, qv);
+// Item m of the activations (token t, m = t * 4 nb + 4 b + i) covers elements
+// 8i..8i+7 of block b; thread tid owns items m0 + u * CONSUMERS + tid.
+template <int T>
+__device__ __forceinline__ int act_item(int m, int per_tok, int& rem) {
+    int t = 0;
+    rem = m;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        const int q = qv[e];
-        s += q;
-        const uint32_t b = (uint32_t)(q & 0xff);
-        if (e & 1) yo |= b << (8 * (e >> 1));
-        else       ye |= b << (8 * (e >> 1));
+    for (int tt = 1; tt < T; ++tt)
+        if (rem >= per_tok) { rem -= per_tok; ++t; }
+    return t;
+}
+
+// Where the quantized activations go: the shared-memory base address of each of
+// the CL CTAs of the cluster (CL == 1: this CTA only) and the offsets of the
+// quad, scale and 8 * sum(q) arrays, which are the same in every CTA.
+template <int CL>
+struct ActDst {
+    uint32_t base[CL];
+    uint32_t q, d, s;
+};
+
+template <int CL>
+__device__ __forceinline__ void act_put(const uint32_t (&base)[CL], uint32_t off, uint32_t v) {
+    if constexpr (CL == 1) {
+        st_shared_u32(base[0] + off, v);
+    } else {
+#pragma unroll
+        for (int r = 0; r < CL; ++r) st_cluster_u32(base[r] + off, v);
     }
-    return s;
+}
+
+// Quantize items C0 .. C0 + C - 1 (C <= 4) of the NI loaded ones to Q8_0 and
+// store them in the quad layout; each step runs across the C items so that the
+// latencies of the shuffles, reciprocals and the warp vote overlap.  The codes
+// of an item are split into the even word (elements 8i, 8i+2, 8i+4, 8i+6) and
+// the odd word (8i+1, ...).  Chunks of at most 4 keep the codes of only 4 items
+// live next to the loaded values.  Item u of this thread is m0 + u * CONSUMERS +
+// tid; items at or past `end` are not stored.
+template <int T, int NI, int C0, int CL>
+__device__ __forceinline__ void quantize_chunk(const float (&v)[NI][8], int nb, int np, int m0, int end,
+                                               const ActDst<CL>& dst, int tid) {
+    constexpr int C = (NI - C0) < 4 ? (NI - C0) : 4;
+    const int per_tok = nb * 4;
+    float w[C][8], d[C];
+#pragma unroll
+    for (int u = 0; u < C; ++u) {
+        float amax = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            w[u][e] = v[C0 + u][e];
+            amax = fmaxf(amax, fabsf(w[u][e]));
+        }
+        d[u] = amax;
+    }
+#pragma unroll
+    for (int u = 0; u < C; ++u) d[u] = fmaxf(d[u], __shfl_xor_sync(0xffffffffu, d[u], 1));
+#pragma unroll
+    for (int u = 0; u < C; ++u) d[u] = scale_q8(fmaxf(d[u], __shfl_xor_sync(0xffffffffu, d[u], 2)));
+    int q[C][8];
+    quant8n<C, true>(w, d, -127.0f, 127.0f, q);
+    uint32_t ye[C], yo[C];
+    int sq[C];
+#pragma unroll
+    for (int u = 0; u < C; ++u) {
+        // low bytes of the codes: even elements into ye, odd into yo
+        const uint32_t e01 = __byte_perm((uint32_t)q[u][0], (uint32_t)q[u][2], 0x0040);
+        const uint32_t e23 = __byte_perm((uint32_t)q[u][4], (uint32_t)q[u][6], 0x0040);
+        const uint32_t o01 = __byte_perm((uint32_t)q[u][1], (uint32_t)q[u][3], 0x0040);
+        const uint32_t o23 = __byte_perm((uint32_t)q[u][5], (uint32_t)q[u][7], 0x0040);
+        ye[u] = d[u] == 0.0f ? 0u : __byte_perm(e01, e23, 0x5410);
+        yo[u] = d[u] == 0.0f ? 0u : __byte_perm(o01, o23, 0x5410);
+        sq[u] = __dp4a((int)ye[u], 0x01010101, __dp4a((int)yo[u], 0x01010101, 0));
+    }
+#pragma unroll
+    for (int u = 0; u < C; ++u) sq[u] += __shfl_xor_sync(0xffffffffu, sq[u], 1);
+#pragma unroll
+    for (int u = 0; u < C; ++u) sq[u] += __shfl_xor_sync(0xffffffffu, sq[u], 2);
+#pragma unroll
+    for (int u = 0; u < C; ++u) {
+        const int m = m0 + (C0 + u) * CONSUMERS + tid;
+        if (m < end) {
+            int rem;
+            const int t = act_item<T>(m, per_tok, rem);
+            const int b = rem >> 2, i = rem & 3;
+            const uint32_t qoff = (uint32_t)(((t * 4 + (b & 1) * 2) * np + (b >> 1)) * 16 + i * 4);
+            act_put<CL>(dst.base, dst.q + qoff, ye[u]);
+            act_put<CL>(dst.base, dst.q + qoff + (uint32_t)np * 16u, yo[u]);
+            if (i == 0) {
+                const uint32_t soff = (uint32_t)(t * nb + b) * 4u;
+                act_put<CL>(dst.base, dst.d + soff, __float_as_uint(fp16_to_f32(fp16_bits(d[u]))));
+                act_put<CL>(dst.base, dst.s + soff, (uint32_t)(8 * sq[u]));
+            }
+        }
+    }
+    if constexpr (C0 + C < NI) quantize_chunk<T, NI, C0 + C, CL>(v, nb, np, m0, end, dst, tid);
+}
+
+// Quantize NI items per thread of the activations (items m0 + u * CONSUMERS +
+// tid below `end`) to Q8_0 into shared memory.  Every load is issued before any
+// arithmetic, so their latencies overlap.  m0 is a multiple of 4, so the four
+// lanes of a block stay in one aligned group; all 32 lanes of every consumer
+// warp must call it.
+template <int T, int NI, int CL>
+__device__ __forceinline__ void quantize_acts(const float* __restrict__ x, int ne00, int nb, int np, int m0,
+                                              int end, const ActDst<CL>& dst, int tid) {
+    const int per_tok = nb * 4;
+    float v[NI][8];
+#pragma unroll
+    for (int u = 0; u < NI; ++u) {
+        const int m = m0 + u * CONSUMERS + tid;
+        if (m < end) {
+            int rem;
+            const int t = act_item<T>(m, per_tok, rem);
+            const float4* src = reinterpret_cast<const float4*>(x + (int64_t)t * ne00 + (rem >> 2) * QK + (rem & 3) * 8);
+            const float4 lo = __ldg(src), hi = __ldg(src + 1);
+            v[u][0] = lo.x; v[u][1] = lo.y; v[u][2] = lo.z; v[u][3] = lo.w;
+            v[u][4] = hi.x; v[u][5] = hi.y; v[u][6] = hi.z; v[u][7] = hi.w;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[u][e] = 0.0f;
+        }
+    }
+    quantize_chunk<T, NI, 0, CL>(v, nb, np, m0, end, dst, tid);
 }
 
 // Activations of one block pair in the quad layout (+ scales and 8 * sum(q)).
@@ -140,9 +250,12 @@ __device__ __forceinline__ void consumer_sync() {
 
 // T tokens; LPR lanes per row; PPL > 0: the lane's PPL block pairs of activations
 // are held in registers for the whole kernel (T == 1), PPL == 0: read from shared
-// memory for every row.
-template <int T, int LPR, int PPL>
-__global__ void __launch_bounds__(THREADS, (PPL > 0 && PPL <= 3) ? 2 : 1)
+// memory for every row.  CL > 1: the grid is made of clusters of CL CTAs that
+// split the activation quantization: each quantizes 1/CL of the blocks and
+// writes the result into the shared memory of every CTA of its cluster, so each
+// SM loads only 1/CL of the fp32 activations from L2.
+template <int T, int LPR, int PPL, int CL>
+__global__ void __launch_bounds__(THREADS, PPL <= 3 ? 2 : 1)
 gemv_q4_0_kernel(const uint8_t* __restrict__ w, const float* __restrict__ x, float* __restrict__ dst,
                  const GemvParams p) {
     static_assert(PPL == 0 || T == 1, "register-resident activations are for one token");
@@ -166,6 +279,12 @@ gemv_q4_0_kernel(const uint8_t* __restrict__ w, const float* __restrict__ x, flo
         fence_mbar_init();
     }
     __syncthreads();
+    if constexpr (CL > 1) {
+        // first cluster barrier phase: every CTA of the cluster has started, so
+        // its shared memory may be written by its peers from here on
+        cluster_arrive();
+        cluster_wait();
+    }
     // the next kernel on the stream may start its own set-up now; it still waits
     // for this grid to finish before it touches memory this grid writes
     pdl_trigger();
@@ -173,6 +292,9 @@ gemv_q4_0_kernel(const uint8_t* __restrict__ w, const float* __restrict__ x, flo
     if (warp == CONSUMERS / 32) {
         // ---------------- producer: stream weight units through the ring
         if (lane == 0) {
+            // second phase: the producer publishes nothing, it arrives at once (the
+            // other lanes of this warp have exited and are not waited for)
+            if constexpr (CL > 1) cluster_arrive();
             int k = 0;
             for (int u = blockIdx.x; u < p.n_units; u += grid, ++k) {
                 const int s = k % p.S;
@@ -209,57 +331,36 @@ gemv_q4_0_kernel(const uint8_t* __restrict__ w, const float* __restrict__ x, flo
     // ---------------- consumers: activations first (they may come from the previous kernel)
     pdl_wait();
     {
-        // Each thread owns 8 consecutive activations of one block per item; the
-        // loads of U items are issued together so that their L2 latencies overlap.
-        constexpr int U = 4;
-        const int per_tok = p.nb * 4;
-        const int total = T * per_tok;               // a multiple of 32: warps stay uniform
-        for (int m0 = 0; m0 < total; m0 += CONSUMERS * U) {
-            float4 va[U], vb[U];
+        // this CTA's share: blocks [f0, f1) of the T * nb blocks (token-major)
+        const int nbt = T * p.nb;
+        const int rank = CL > 1 ? (int)cluster_ctarank() : 0;
+        const int f0 = (int)(((int64_t)rank * nbt) / CL), f1 = (int)(((int64_t)(rank + 1) * nbt) / CL);
+        ActDst<CL> ad;
+        const uint32_t sbase = smem_u32(smem);
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int m = m0 + u * CONSUMERS + tid;
-                if (m < total) {
-                    const int t = m / per_tok, rem = m - t * per_tok;
-                    const float4* src =
-                        reinterpret_cast<const float4*>(x + (int64_t)t * p.ne00 + (rem >> 2) * QK + (rem & 3) * 8);
-                    va[u] = __ldg(src);
-                    vb[u] = __ldg(src + 1);
-                } else {
-                    va[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    vb[u] = va[u];
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int m = m0 + u * CONSUMERS + tid;
-                if (m0 + u * CONSUMERS >= total) break;    // uniform across the CTA
-                const bool ok = m < total;
-                const int t = ok ? m / per_tok : 0;
-                const int rem = m - t * per_tok;
-                const int b = rem >> 2, i = rem & 3;
-                const float v[8] = {va[u].x, va[u].y, va[u].z, va[u].w, vb[u].x, vb[u].y, vb[u].z, vb[u].w};
-                float amax = 0.0f;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(v[e]));
-                amax = warp_max4(amax);
-                const float d = scale_q8(amax);
-                uint32_t ye, yo;
-                int sq = quant_q8_split(v, d, ye, yo);
-                sq = warp_sum4(sq);
-                if (ok) {
-                    const int qi = (t * 4 + (b & 1) * 2) * p.np + (b >> 1);
-                    reinterpret_cast<uint32_t*>(&quads[qi])[i] = ye;
-                    reinterpret_cast<uint32_t*>(&quads[qi + p.np])[i] = yo;
-                    if (i == 0) {
-                        dy[t * p.nb + b] = fp16_to_f32(fp16_bits(d));
-                        sy8[t * p.nb + b] = 8 * sq;
-                    }
-                }
-            }
+        for (int r = 0; r < CL; ++r) ad.base[r] = CL > 1 ? mapa_shared(sbase, (uint32_t)r) : sbase;
+        ad.q = (uint32_t)p.act_off;
+        ad.d = (uint32_t)p.dy_off;
+        ad.s = (uint32_t)p.sy_off;
+        if (PPL > 0) {
+            // one token, nb = 2 * PPL * LPR blocks, at most ceil(nb / CL) of them
+            // here (4 items each): all in one batch
+            constexpr int NBMAX = (2 * (PPL > 0 ? PPL : 1) * LPR + CL - 1) / CL;
+            constexpr int NI = (4 * NBMAX + CONSUMERS - 1) / CONSUMERS;
+            quantize_acts<T, NI, CL>(x, p.ne00, p.nb, p.np, 4 * f0, 4 * f1, ad, tid);
+        } else {
+            constexpr int U = 3;
+            for (int m0 = 4 * f0; m0 < 4 * f1; m0 += CONSUMERS * U)
+                quantize_acts<T, U, CL>(x, p.ne00, p.nb, p.np, m0, 4 * f1, ad, tid);
         }
     }
-    consumer_sync();
+    if constexpr (CL > 1) {
+        // second phase: every CTA's share is in every CTA's shared memory
+        cluster_arrive();
+        cluster_wait();
+    } else {
+        consumer_sync();
+    }
 
     constexpr int RP = CONSUMERS / LPR;     // rows processed side by side
     const int rr = tid / LPR, sl = tid % LPR;
@@ -423,7 +524,9 @@ struct GemvPlan {
     GemvParams p;
     int lpr;
     int ppl_reg;       // > 0: activations in registers
-    int grid;
+    int grid;          // CTAs without clusters
+    int cl;            // cluster size to try (1 or 2)
+    int sms;
     size_t smem;
 };
 
@@ -485,36 +588,107 @@ bool plan_gemv(int64_t ne00, int64_t ne01, int64_t ne11, const DeviceInfo& info,
     plan->lpr = lpr;
     const int per_sm = (!small && plan->smem <= 113 * 1024 && two_per_sm) ? 2 : 1;
     plan->grid = (int)std::min<int64_t>(p.n_units, sms * per_sm);
+    plan->sms = (int)sms;
+    // Splitting the activation quantization over a pair of CTAs pays only where
+    // each SM would otherwise load tens of KB of fp32 activations: below that the
+    // pair's barrier (each CTA waits for the slower one) costs more than it saves.
+    plan->cl = ne11 * ne00 >= CLUSTER_MIN_X ? 2 : 1;
     return true;
+}
+
+template <int T, int LPR, int PPL, int CL>
+cudaLaunchConfig_t gemv_config(const GemvPlan& plan, int grid, cudaStream_t stream, bool pdl,
+                               cudaLaunchAttribute (&attr)[2]) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = plan.smem;
+    cfg.stream = stream;
+    int n = 0;
+    if (pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (CL > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = CL;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cfg;
+}
+
+// Raise the kernel's opt-in shared-memory size (once per device and size), and
+// return how many of its CTAs fit on the device at once in clusters of CL
+// (cached per device and shared-memory size; 0 if the query fails).
+template <int T, int LPR, int PPL, int CL>
+int gemv_prepare(const GemvPlan& plan, int device) {
+    static std::mutex mu;
+    static std::map<std::pair<int, size_t>, int> resident;
+    static int configured[64] = {};
+    auto kern = gemv_q4_0_kernel<T, LPR, PPL, CL>;
+    std::lock_guard<std::mutex> lock(mu);
+    if ((int)plan.smem > configured[device]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return 0;
+        }
+        configured[device] = (int)plan.smem;
+    }
+    const auto key = std::make_pair(device, plan.smem);
+    auto it = resident.find(key);
+    if (it != resident.end()) return it->second;
+    int n = 0;
+    if (CL == 1) {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, THREADS, plan.smem) == cudaSuccess)
+            n = per_sm * plan.sms;
+    } else {
+        cudaLaunchAttribute attr[2];
+        const cudaLaunchConfig_t cfg = gemv_config<T, LPR, PPL, CL>(plan, CL, nullptr, false, attr);
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) == cudaSuccess) n = clusters * CL;
+    }
+    (void)cudaGetLastError();
+    resident[key] = n;
+    return n;
+}
+
+template <int T, int LPR, int PPL, int CL>
+q4q_status gemv_launch_cl(const GemvPlan& plan, int grid, const uint8_t* w, const float* x, float* dst,
+                          cudaStream_t stream, bool pdl) {
+    cudaLaunchAttribute attr[2];
+    const cudaLaunchConfig_t cfg = gemv_config<T, LPR, PPL, CL>(plan, grid, stream, pdl, attr);
+    if (cudaLaunchKernelEx(&cfg, gemv_q4_0_kernel<T, LPR, PPL, CL>, w, x, dst, plan.p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return Q4Q_ERR_CUDA;
+    }
+    return launch_status();
+}
+
+// CTAs of a launch in clusters of cl: every unit gets a CTA where the device
+// holds that many at once, rounded to whole clusters.
+inline int cluster_grid(int n_units, int resident, int cl) {
+    const int want = (n_units + cl - 1) / cl * cl;
+    return std::min(want, resident / cl * cl);
 }
 
 template <int T, int LPR, int PPL>
 q4q_status launch_gemv_t(const GemvPlan& plan, const uint8_t* w, const float* x, float* dst, cudaStream_t stream,
                          int device, bool pdl) {
-    // the opt-in shared-memory size is raised once per device and kernel
-    static std::atomic<int> configured[64];
-    auto kern = gemv_q4_0_kernel<T, LPR, PPL>;
     if (device < 0 || device >= 64) return Q4Q_ERR_CUDA;
-    if ((int)plan.smem > configured[device].load()) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem) != cudaSuccess)
-            return Q4Q_ERR_CUDA;
-        configured[device].store((int)plan.smem);
+    // Clusters only where they keep (nearly) every planned CTA resident.
+    const int need = plan.grid - plan.grid / 16;
+    if (plan.cl >= 2) {
+        const int g = cluster_grid(plan.p.n_units, gemv_prepare<T, LPR, PPL, 2>(plan, device), 2);
+        if (g >= 2 && g >= need) return gemv_launch_cl<T, LPR, PPL, 2>(plan, g, w, x, dst, stream, pdl);
     }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)plan.grid);
-    cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = plan.smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
-    if (cudaLaunchKernelEx(&cfg, kern, w, x, dst, plan.p) != cudaSuccess) {
-        (void)cudaGetLastError();
-        return Q4Q_ERR_CUDA;
-    }
-    return launch_status();
+    if (gemv_prepare<T, LPR, PPL, 1>(plan, device) <= 0) return Q4Q_ERR_CUDA;
+    return gemv_launch_cl<T, LPR, PPL, 1>(plan, plan.grid, w, x, dst, stream, pdl);
 }
 
 template <int T, int LPR>
