@@ -59,14 +59,23 @@ def _measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def kernel_source_hash(kernel_file: str) -> str:
+    """First 16 hex digits of the sha256 of a kernel's source file followed by the
+    shared device header it includes (either change invalidates a profile)."""
+    h = hashlib.sha256()
+    for f in (kernel_file, "q4q_common.cuh"):
+        with open(os.path.join(ROOT, "q4_quantized_matmul_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def _profile_traffic(kernel_file: str, summary: str):
     """DRAM bytes per launch from a committed ncu summary, if the kernel source is
-    unchanged since it was taken (the summary records the source's sha256)."""
+    unchanged since it was taken (the summary records kernel_source_hash)."""
     try:
         with open(os.path.join(ROOT, "profiles", summary), encoding="utf-8") as f:
             text = f.read()
-        src = open(os.path.join(ROOT, "q4_quantized_matmul_gb300", "csrc", kernel_file), "rb").read()
-        sha = hashlib.sha256(src).hexdigest()[:16]
+        sha = kernel_source_hash(kernel_file)
         m_sha = re.search(r"source_sha256_16:\s*([0-9a-f]+)", text)
         m_tr = re.search(r"dram_bytes_per_step:\s*([0-9.eE+]+)", text)
         if m_sha and m_tr and m_sha.group(1) == sha:
@@ -331,7 +340,8 @@ def run_ours(args, rank, world, local_rank):
 
     batched = measure_batched(dev, stream, args) if (rank == 0 and args.batched_tokens > 0) else None
     second = (measure_decode(dev, stream, args.secondary_decode)
-              if (rank == 0 and args.secondary_decode and args.secondary_decode != args.workload) else None)
+              if (rank == 0 and args.secondary_decode not in ("", "none") and args.secondary_decode != args.workload)
+              else None)
 
     # ---- CPU baseline: the oracle on this host's cores, bounded sample
     cpu = cpu_baseline(args.workload, ne11, budget_s=args.cpu_seconds) if (rank == 0 and args.cpu_seconds > 0) else None

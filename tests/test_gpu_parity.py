@@ -110,6 +110,58 @@ def _near_tie_rows(rng, levels, nrows):
     return np.stack(rows).reshape(nrows // 8, 256)
 
 
+def _band_edge_rows(rng, levels, nrows):
+    """Blocks whose quotients x/d lie at distances 1e-6 .. 2e-3 (log-uniform, either
+    side) from half-integers: across the band the kernels treat as a possible tie,
+    so that a quotient approximation worse than its stated bound would round some
+    of them to the wrong side."""
+    rows = []
+    for _ in range(nrows):
+        amax = np.float32(rng.uniform(0.01, 100.0))
+        d = np.float32(amax / np.float32(levels))
+        blk = np.empty(32, np.float32)
+        blk[0] = -amax if levels == 8 else amax
+        k = rng.integers(-levels, levels, size=31) + 0.5
+        delta = np.exp(rng.uniform(np.log(1e-6), np.log(2e-3), size=31)) * rng.choice([-1.0, 1.0], size=31)
+        x = ((k + delta) * np.float64(d)).astype(np.float32)
+        blk[1:] = np.clip(x, -amax, amax)
+        rows.append(blk)
+    return np.stack(rows).reshape(nrows // 8, 256)
+
+
+@pytest.mark.parametrize("kind", ["q4_0", "q8_0"])
+def test_quantize_band_edges_bit_exact(q4q, kind):
+    rng = np.random.default_rng(33)
+    levels = 8 if kind == "q4_0" else 127
+    w = _band_edge_rows(rng, levels, 8192)
+    fn = q4q.q4q_quantize_q4_0 if kind == "q4_0" else q4q.q4q_quantize_q8_0
+    ref = oracle.quantize_q4_0(w) if kind == "q4_0" else oracle.quantize_q8_0(w)
+    np.testing.assert_array_equal(fn(dev(w)).cpu().numpy(), ref)
+
+
+def test_mul_mat_band_edge_activations(q4q):
+    # Q4_0 weights with a single nonzero code per block (+1 at one element), so that
+    # every output isolates activation codes: a code off by one changes the output
+    # by d_w * d_x, far above the tolerance
+    rng = np.random.default_rng(34)
+    ne00, ne01 = 4096, 64
+    x = _band_edge_rows(rng, 127, 16 * ne00 // 32).reshape(16, ne00)
+    wq_rows = np.zeros((ne01, ne00 // 32, 18), np.uint8)
+    wq_rows[:, :, 0:2] = np.frombuffer(np.float16(0.5).tobytes(), np.uint8)
+    wq_rows[:, :, 2:] = 0x88                                      # every nibble 8: value 0
+    sel = rng.integers(0, 32, size=(ne01, ne00 // 32))
+    for r in range(ne01):
+        for b in range(ne00 // 32):
+            j = sel[r, b]
+            byte = 2 + j // 2
+            wq_rows[r, b, byte] = (0x89 if j % 2 == 0 else 0x98)    # nibble 9: value +1 * d
+    wq = wq_rows.reshape(-1)
+    for ne11 in (1, 3, 7, 16):
+        got = q4q.q4q_mul_mat(dev(wq), ne00, ne01, dev(x[:ne11])).cpu().numpy()
+        ref, scale = oracle.mul_mat(wq, ne00, ne01, x[:ne11])
+        assert_close(got, ref, scale)
+
+
 @pytest.mark.parametrize("kind", ["q4_0", "q8_0"])
 def test_quantize_near_ties_bit_exact(q4q, kind):
     rng = np.random.default_rng(31)
