@@ -288,7 +288,11 @@ def run_ours(args, rank, world, local_rank):
     out_bytes = sum(4 * n * ne11 for k, n in shapes)
     alg_bytes_step = wbytes + act_bytes + out_bytes
     peak, peak_kind = _measured_peaks()
-    achieved = alg_bytes_step / (kern_ms_per_step * 1e-3) / 1e9
+    # The timed region runs nothing but this kernel (nmat launches per step), so its
+    # average launch duration there is ms_per_step / nmat (PDL lets consecutive
+    # launches overlap their set-up, as they do in the timed step).
+    achieved = alg_bytes_step / (ms_per_step * 1e-3) / 1e9
+    isolated = alg_bytes_step / (kern_ms_per_step * 1e-3) / 1e9
     traffic_step = _profile_traffic("q4q_gemv.cu", "gemv_q4_0_%s.md" % args.workload) if ne11 < 8 else None
 
     # ---- end to end through the public API with host buffers (pinned), graph-captured
@@ -384,13 +388,20 @@ def run_ours(args, rank, world, local_rank):
             "frac": round(achieved / peak, 4),
             "traffic": (traffic_step / nmat) if traffic_step else None,
             "algorithmic_bytes_per_launch": alg_bytes_step / nmat,
-            "avg_launch_us": round(kern_ms_per_step * 1e3 / nmat, 3),
-            "per_launch": [{"shape": "%d->%d" % shapes[i], "us": round(1e3 * statistics.median(v), 2),
-                            "gb_s": round(_weights_bytes([shapes[i]]) / (1e-3 * statistics.median(v)) / 1e9, 1)}
-                           for i, v in sorted(per_shape.items())],
-            "note": "achieved = algorithmic bytes (Q4_0 weights + fp32 activations + fp32 outputs) of the "
-                    "step's launches / their summed CUDA-event durations (each launch bracketed by events, "
-                    "L2-cold weight copies)",
+            "avg_launch_us": round(ms_per_step * 1e3 / nmat, 3),
+            "note": "achieved = algorithmic bytes (Q4_0 weights + fp32 activations + fp32 outputs) per "
+                    "launch / average launch duration in the timed region (CUDA events on the launching "
+                    "stream; the region runs only this kernel, %d launches per step)" % nmat,
+            "isolated": {
+                "achieved": round(isolated, 1),
+                "frac": round(isolated / peak, 4),
+                "avg_launch_us": round(kern_ms_per_step * 1e3 / nmat, 3),
+                "per_launch": [{"shape": "%d->%d" % shapes[i], "us": round(1e3 * statistics.median(v), 2),
+                                "gb_s": round(_weights_bytes([shapes[i]]) / (1e-3 * statistics.median(v)) / 1e9, 1)}
+                               for i, v in sorted(per_shape.items())],
+                "note": "each launch alone between its own CUDA events (stream held by a spin kernel while "
+                        "they are queued), no PDL overlap, L2-cold weight copies",
+            },
         },
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": act_bytes,
                 "d2h_bytes_per_step": out_bytes,
