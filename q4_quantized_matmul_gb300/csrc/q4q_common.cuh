@@ -195,8 +195,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Same test, but the thread may be suspended in hardware for up to `hint_ns`
-// while the phase is incomplete (it resumes as soon as the phase completes), so
-// waiting warps do not spin on the issue slots and the shared-memory pipe.
+// while the phase is incomplete (it resumes as soon as the phase completes).
 __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
     uint32_t ok;
     asm volatile(
@@ -215,14 +214,27 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
-// Wait for phase `parity` of an mbarrier, for at most `limit_ns` nanoseconds.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
-    uint64_t t0 = global_timer_ns();
-    while (true) {
-        if (mbar_try_wait_sleep(bar, parity, SLEEP_HINT_NS)) return true;
-        if (global_timer_ns() - t0 > limit_ns) return false;
+// Wait for phase `parity` of an mbarrier, for at most about `limit_ns`
+// nanoseconds, or until *stop becomes non-zero (stop may be null).  Polls with the
+// plain try_wait, which suspends the thread in hardware while the phase is
+// incomplete, so a waiting warp takes almost no issue slots from working ones; the
+// stop flag and the clock are looked at every 64 polls.
+__device__ __forceinline__ bool mbar_wait_until(uint32_t bar, uint32_t parity, volatile int* stop,
+                                                uint64_t limit_ns) {
+    uint64_t t0 = 0;
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((n & 63u) == 0u) {
+            if (stop && *stop) return false;
+            const uint64_t t = global_timer_ns();
+            if (t0 == 0) t0 = t;
+            else if (t - t0 > limit_ns) return false;
+        }
     }
+}
+
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    return mbar_wait_until(bar, parity, nullptr, limit_ns);
 }
 
 // 1-D bulk copy global -> shared (TMA engine), completion counted on `bar`.

@@ -300,12 +300,7 @@ gemv_q4_0_kernel(const uint8_t* __restrict__ w, const float* __restrict__ x, flo
                 const int s = k % p.S;
                 if (k >= p.S) {
                     const uint32_t bar = empty0 + 8 * s, par = ((k / p.S) + 1) & 1;
-                    bool ok = mbar_try_wait(bar, par);
-                    if (!ok) {
-                        const uint64_t t0 = global_timer_ns();
-                        while (!ok && !*abort_flag && global_timer_ns() - t0 < WAIT_LIMIT_NS)
-                            ok = mbar_try_wait_sleep(bar, par, SLEEP_HINT_NS);
-                    }
+                    const bool ok = mbar_wait_until(bar, par, abort_flag, WAIT_LIMIT_NS);
                     if (!ok) {
                         if (!*abort_flag) record_error(&g_gemv_status, DEV_TIMEOUT);
                         *abort_flag = 1;
@@ -380,12 +375,7 @@ gemv_q4_0_kernel(const uint8_t* __restrict__ w, const float* __restrict__ x, flo
             const uint32_t bar = full0 + 8 * s, par = (uint32_t)((k / p.S) & 1);
             int ok = 1;
             if (lane == 0) {
-                bool got = mbar_try_wait(bar, par);
-                if (!got) {
-                    const uint64_t t0 = global_timer_ns();
-                    while (!got && !*abort_flag && global_timer_ns() - t0 < WAIT_LIMIT_NS)
-                        got = mbar_try_wait_sleep(bar, par, SLEEP_HINT_NS);
-                }
+                const bool got = mbar_wait_until(bar, par, abort_flag, WAIT_LIMIT_NS);
                 if (!got) {
                     if (!*abort_flag) record_error(&g_gemv_status, DEV_TIMEOUT);
                     *abort_flag = 1;

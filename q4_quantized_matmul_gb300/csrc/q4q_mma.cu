@@ -453,39 +453,51 @@ mma_q4_0_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
 #pragma unroll
             for (int c = 0; c < C::CPW / 2; ++c) acc[c] = 0;
             bool aborted = false;
-            for (int g = 0; g < n_slab; ++g) {
-                const int buf = g % NBUF;
-                const int i = g >> 1, s = i % AB_STAGES, j = g & 1;
-                if (!warp_wait(slab_full + 8 * buf, (g / NBUF) & 1, abort_flag, lane) ||
-                    (j == 0 && !warp_wait(ab_full + 8 * s, (i / AB_STAGES) & 1, abort_flag, lane))) {
-                    aborted = true;
-                    break;
+            for (int i = 0; i < n_ab && !aborted; ++i) {
+                const int s = i % AB_STAGES;
+                // One check per stage with both polls in flight together: the stage's
+                // activation scales, and its second slab.  The MMA issuer commits the
+                // second slab after the first, and a commit completes only once every
+                // earlier MMA of that thread has, so the second slab implies the first.
+                {
+                    const int g1 = 2 * i + 1;
+                    const uint32_t bar_a = ab_full + 8 * s, par_a = (uint32_t)((i / AB_STAGES) & 1);
+                    const uint32_t bar_b = slab_full + 8 * (g1 % NBUF), par_b = (uint32_t)((g1 / NBUF) & 1);
+                    const bool ra = mbar_try_wait(bar_a, par_a);
+                    const bool rb = mbar_try_wait(bar_b, par_b);
+                    if (!__all_sync(0xffffffffu, ra && rb) &&
+                        !(warp_wait(bar_a, par_a, abort_flag, lane) && warp_wait(bar_b, par_b, abort_flag, lane))) {
+                        aborted = true;
+                        break;
+                    }
                 }
                 tc_fence_after();
-                uint32_t r[CK];
-                tmem_ld_chunk<CK>(tq + (uint32_t)(buf * NT + col0), r);
-                const float dwm = dw_s[(s * 2 + j) * BM + row];
-                const uint64_t dw2 = pack2(dwm, dwm);
-                const float4* dxs = reinterpret_cast<const float4*>(dx_s + (s * 2 + j) * NT + col0);
-                tmem_ld_wait();
-                // the slab is in registers: hand its TMEM buffer back to the MMA issuer
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(slab_empty + 8 * buf);
 #pragma unroll
-                for (int c = 0; c < CK / 4; ++c) {
-                    const float4 d4 = dxs[c];
-                    acc[2 * c] = ffma2(fmul2(dw2, pack2(d4.x, d4.y)),
-                                       pack2(__uint_as_float(r[4 * c]), __uint_as_float(r[4 * c + 1])), acc[2 * c]);
-                    acc[2 * c + 1] = ffma2(fmul2(dw2, pack2(d4.z, d4.w)),
-                                           pack2(__uint_as_float(r[4 * c + 2]), __uint_as_float(r[4 * c + 3])),
-                                           acc[2 * c + 1]);
+                for (int j = 0; j < 2; ++j) {
+                    const int g = 2 * i + j, buf = g % NBUF;
+                    uint32_t r[CK];
+                    tmem_ld_chunk<CK>(tq + (uint32_t)(buf * NT + col0), r);
+                    const float dwm = dw_s[(s * 2 + j) * BM + row];
+                    const uint64_t dw2 = pack2(dwm, dwm);
+                    const float4* dxs = reinterpret_cast<const float4*>(dx_s + (s * 2 + j) * NT + col0);
+                    tmem_ld_wait();
+                    // the slab is in registers: hand its TMEM buffer back to the MMA issuer
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(slab_empty + 8 * buf);
+#pragma unroll
+                    for (int c = 0; c < CK / 4; ++c) {
+                        const float4 d4 = dxs[c];
+                        acc[2 * c] = ffma2(fmul2(dw2, pack2(d4.x, d4.y)),
+                                           pack2(__uint_as_float(r[4 * c]), __uint_as_float(r[4 * c + 1])), acc[2 * c]);
+                        acc[2 * c + 1] = ffma2(fmul2(dw2, pack2(d4.z, d4.w)),
+                                               pack2(__uint_as_float(r[4 * c + 2]), __uint_as_float(r[4 * c + 3])),
+                                               acc[2 * c + 1]);
+                    }
                 }
                 // the stage's scales have been read for both of its slabs
-                if (j == 1) {
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(ab_empty + 8 * s);
-                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ab_empty + 8 * s);
             }
             if (!aborted && !*abort_flag && m < p.M) {
 #pragma unroll
