@@ -199,7 +199,10 @@ def run_ours(args, rank, world, local_rank):
     # rotate weight copies so that every step reads its weights from HBM, not L2
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     copies = max(1, -(-3 * l2 // wbytes)) if wbytes < 3 * l2 else 1
-    copies = max(copies, 2)
+    # A decode token runs every layer's projections back to back in one graph; here a
+    # graph holds one step per weight copy (4 for a decode set), so the programmatic
+    # dependent launch chain also runs across step boundaries inside it.
+    copies = max(copies, 4 if ne11 < 8 else 2)
     wsets = [wq] + [[t.clone() for t in wq] for _ in range(copies - 1)]
     ws_bytes = max(q4q.q4q_mul_mat_workspace_size(k, n, ne11) for k, n in shapes)
     workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
@@ -223,7 +226,24 @@ def run_ours(args, rank, world, local_rank):
         with torch.cuda.graph(g, stream=stream):
             step(c)
         graphs.append(g)
+    multi = torch.cuda.CUDAGraph()          # one step per weight copy, in order
+    with torch.cuda.graph(multi, stream=stream):
+        for c in range(copies):
+            step(c)
     torch.cuda.synchronize()
+
+    graph_steps = copies if ne11 < 8 else 1
+
+    def run_steps(multi_graph, single_graphs, k_steps):
+        """Exactly k_steps steps: whole multi-step graphs, then single steps."""
+        if graph_steps == 1:
+            for k in range(k_steps):
+                single_graphs[k % copies].replay()
+            return
+        for _ in range(k_steps // graph_steps):
+            multi_graph.replay()
+        for k in range(k_steps % graph_steps):
+            single_graphs[k].replay()
 
     def barrier():
         if world > 1:
@@ -251,8 +271,7 @@ def run_ours(args, rank, world, local_rank):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         e0.record(stream)
-        for k in range(args.steps):
-            graphs[k % copies].replay()
+        run_steps(multi, graphs, args.steps)
         e1.record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -327,6 +346,10 @@ def run_ours(args, rank, world, local_rank):
         with torch.cuda.graph(g, stream=stream):
             e2e_step(c)
         egraphs.append(g)
+    emulti = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(emulti, stream=stream):
+        for c in range(copies):
+            e2e_step(c)
     with torch.cuda.stream(stream):
         for k in range(args.warmup):
             egraphs[k % copies].replay()
@@ -334,8 +357,7 @@ def run_ours(args, rank, world, local_rank):
     barrier()
     with torch.cuda.stream(stream):
         e0.record(stream)
-        for k in range(args.steps):
-            egraphs[k % copies].replay()
+        run_steps(emulti, egraphs, args.steps)
         e1.record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -374,7 +396,10 @@ def run_ours(args, rank, world, local_rank):
             "q4_0_weight_bytes_per_step": wbytes,
             "l2_policy": "inputs larger than L2: %d rotating copies of the Q4_0 weights (%.0f MB, L2 %.0f MB)" % (
                 copies, copies * wbytes / 1e6, l2 / 1e6),
-            "launch": "one CUDA graph per weight copy, %d q4q_mul_mat calls per step" % nmat,
+            "launch": "%d q4q_mul_mat calls per step; CUDA graphs of %d consecutive steps (one per weight copy), "
+                      "programmatic dependent launch between all calls of a graph" % (nmat, copies)
+                      if ne11 < 8 else "%d q4q_mul_mat calls per step, one CUDA graph per step" % nmat,
+            "graph_steps": graph_steps,
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
         "gpu_launches": nmat * args.steps * (1 if ne11 < 8 else 2),
@@ -447,6 +472,7 @@ def measure_decode(dev, stream, name, steps=300):
         for c in range(copies):
             step(c)
     torch.cuda.synchronize()
+    # one graph per step: the 49-matrix set is a whole model's decode step already
     graphs = []
     for c in range(copies):
         g = torch.cuda.CUDAGraph()
@@ -468,6 +494,7 @@ def measure_decode(dev, stream, name, steps=300):
     out = {"workload": name, "description": wl.description, "value": round(gbs, 1), "unit": "GB/s",
            "ms_per_step": round(ms, 5), "frac_of_hbm": round(gbs / peak, 4), "matrices": len(shapes),
            "us_per_matrix": round(ms * 1e3 / len(shapes), 3),
+           "graph_steps": 1,
            "note": "dependent-chain launch (PDL), one kernel per matrix; small matrices are launch-latency bound"}
     del wsets, wq, xs, ds
     torch.cuda.empty_cache()
