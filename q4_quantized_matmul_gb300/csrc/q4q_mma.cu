@@ -42,8 +42,6 @@ __device__ unsigned int g_mma_status = 0;
 constexpr int BM = 128;                 // weight rows per CTA tile (MMA M)
 constexpr int KRAW = 256;               // K per raw-weight stage (8 blocks = 144 bytes per row)
 constexpr int KAB = 64;                 // K per A/B stage (2 blocks, one 128-byte swizzle row)
-constexpr int RAW_STAGES = 3;
-constexpr int AB_STAGES = 4;
 constexpr int RAW_BYTES = BM * 144;     // 18432
 constexpr int A_BYTES = BM * KAB * 2;   // 16384
 constexpr int NPAD = 128;               // activation-scale rows are padded to this
@@ -224,6 +222,12 @@ template <int NT>
 struct Cfg {
     // epilogue warps: NT/32 per TMEM lane quadrant (each owns 32 columns), at least one
     static constexpr int EPI_WARPS = NT >= 128 ? 16 : (NT >= 64 ? 8 : 4);
+    // Narrow token tiles do little work per 32-K block, so a CTA is bound by the
+    // latency of its per-block hand-offs: with shallower rings two CTAs fit on an
+    // SM (shared memory, registers, TMEM) and their chains overlap.
+    static constexpr int MIN_BLOCKS = NT <= 32 ? 2 : 1;
+    static constexpr int RAW_STAGES = NT <= 32 ? 2 : 3;
+    static constexpr int AB_STAGES = NT <= 32 ? 3 : 4;
     static constexpr int CPW = NT * 4 / EPI_WARPS;       // columns per epilogue warp
     static constexpr int THREADS = (8 + EPI_WARPS) * 32;
     static constexpr int B_BYTES = NT * KAB * 2;
@@ -233,7 +237,7 @@ struct Cfg {
     static constexpr int DX_BYTES = 2 * NT * 4;           // activation scales of one A/B stage
     // shared memory map (offsets from a 1024-aligned base)
     static constexpr int OFF_RAW = 0;
-    static constexpr int OFF_A = OFF_RAW + RAW_STAGES * RAW_BYTES;                  // 55296 (1024-aligned)
+    static constexpr int OFF_A = OFF_RAW + RAW_STAGES * RAW_BYTES;                  // 1024-aligned
     static constexpr int OFF_B = OFF_A + AB_STAGES * A_BYTES;
     static constexpr int OFF_DW = OFF_B + AB_STAGES * B_STRIDE;
     static constexpr int OFF_DX = OFF_DW + AB_STAGES * 2 * BM * 4;
@@ -244,11 +248,13 @@ struct Cfg {
 };
 
 template <int NT, bool DEBUG>
-__global__ void __launch_bounds__(Cfg<NT>::THREADS, 1)
+__global__ void __launch_bounds__(Cfg<NT>::THREADS, Cfg<NT>::MIN_BLOCKS)
 mma_q4_0_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_b,
                 const MmaParams p) {
     using C = Cfg<NT>;
     constexpr int NBUF = C::NBUF;
+    constexpr int RAW_STAGES = C::RAW_STAGES;
+    constexpr int AB_STAGES = C::AB_STAGES;
     extern __shared__ uint8_t smem_raw[];
     // align to 1024 bytes by pointer arithmetic on the shared array itself, so the
     // compiler keeps every derived pointer in the shared address space
