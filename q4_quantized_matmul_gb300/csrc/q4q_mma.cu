@@ -228,6 +228,10 @@ struct Cfg {
     static constexpr int MIN_BLOCKS = NT <= 32 ? 2 : 1;
     static constexpr int RAW_STAGES = NT <= 32 ? 2 : 3;
     static constexpr int AB_STAGES = NT <= 32 ? 3 : 4;
+    // Narrow tiles are bound by the single MMA-issuing thread: it hands TMEM over in
+    // slab pairs (one check and one commit per A/B stage).  The widest tile is bound
+    // by its epilogue, which frees each slab as soon as it has read it.
+    static constexpr bool PAIRWISE = NT <= 64;
     static constexpr int CPW = NT * 4 / EPI_WARPS;       // columns per epilogue warp
     static constexpr int THREADS = (8 + EPI_WARPS) * 32;
     static constexpr int B_BYTES = NT * KAB * 2;
@@ -285,7 +289,10 @@ mma_q4_0_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
         }
         for (int s = 0; s < AB_STAGES; ++s) {
             mbar_init(ab_full + 8 * s, 4 + 1);
-            mbar_init(ab_empty + 8 * s, 1 + C::EPI_WARPS);
+            // released by the MMA issuer's commit and every epilogue warp; with pairwise
+            // hand-off by the epilogue warps alone (they release a stage only after
+            // seeing the commit that follows its MMAs)
+            mbar_init(ab_empty + 8 * s, (C::PAIRWISE && !DEBUG ? 0 : 1) + C::EPI_WARPS);
         }
         for (int s = 0; s < NBUF; ++s) {
             mbar_init(slab_full + 8 * s, 1);
@@ -339,7 +346,35 @@ mma_q4_0_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
             constexpr uint32_t IDESC = idesc_f16(BM, NT);
             int g = 0;
             bool ok = true;
-            for (int i = 0; i < n_ab && ok; ++i) {
+            constexpr bool PAIRWISE = C::PAIRWISE && !DEBUG;
+            if constexpr (PAIRWISE) {
+                // One hand-off per A/B stage: its two K blocks go to the two slab buffers
+                // of one pair, with one empty check and one commit for the pair (the
+                // issuing thread is on the critical path when the token tile is narrow).
+                constexpr int NPAIR = NBUF / 2;
+                for (int i = 0; i < n_ab && ok; ++i) {
+                    const int s = i % AB_STAGES, pr = i % NPAIR;
+                    if (!wait_or_abort(ab_full + 8 * s, (i / AB_STAGES) & 1, abort_flag) ||
+                        (i >= NPAIR && !wait_or_abort(slab_empty + 8 * pr, ((i / NPAIR) + 1) & 1, abort_flag))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_base = sbase + C::OFF_A + s * A_BYTES;
+                    const uint32_t b_base = sbase + C::OFF_B + s * C::B_STRIDE;
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+#pragma unroll
+                        for (int kk = 0; kk < 2; ++kk) {
+                            const uint32_t koff = (uint32_t)(64 * j + 32 * kk);   // bytes along the swizzled row
+                            mma_f16(tmem + (uint32_t)((2 * pr + j) * NT), smem_desc_sw128(a_base + koff),
+                                    smem_desc_sw128(b_base + koff), IDESC, (uint32_t)kk);
+                        }
+                    }
+                    mma_commit(slab_full + 8 * pr);
+                }
+            }
+            for (int i = 0; i < n_ab && ok && !PAIRWISE; ++i) {
                 const int s = i % AB_STAGES;
                 if (!wait_or_abort(ab_full + 8 * s, (i / AB_STAGES) & 1, abort_flag)) { ok = false; break; }
                 tc_fence_after();
@@ -459,16 +494,20 @@ mma_q4_0_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
 #pragma unroll
             for (int c = 0; c < C::CPW / 2; ++c) acc[c] = 0;
             bool aborted = false;
+            constexpr int NPAIR = NBUF / 2;
+            constexpr bool PAIRWISE = C::PAIRWISE;
             for (int i = 0; i < n_ab && !aborted; ++i) {
-                const int s = i % AB_STAGES;
+                const int s = i % AB_STAGES, pr = i % NPAIR;
                 // One check per stage with both polls in flight together: the stage's
-                // activation scales, and its second slab.  The MMA issuer commits the
-                // second slab after the first, and a commit completes only once every
-                // earlier MMA of that thread has, so the second slab implies the first.
+                // activation scales, and its slabs.  Pairwise: the commit of its slab
+                // pair (issued after the stage's MMAs).  Otherwise: its second slab; the
+                // issuer commits it after the first, and a commit completes only once
+                // every earlier MMA of that thread has, so it implies the first.
                 {
                     const int g1 = 2 * i + 1;
                     const uint32_t bar_a = ab_full + 8 * s, par_a = (uint32_t)((i / AB_STAGES) & 1);
-                    const uint32_t bar_b = slab_full + 8 * (g1 % NBUF), par_b = (uint32_t)((g1 / NBUF) & 1);
+                    const uint32_t bar_b = PAIRWISE ? slab_full + 8 * pr : slab_full + 8 * (g1 % NBUF);
+                    const uint32_t par_b = PAIRWISE ? (uint32_t)((i / NPAIR) & 1) : (uint32_t)((g1 / NBUF) & 1);
                     const bool ra = mbar_try_wait(bar_a, par_a);
                     const bool rb = mbar_try_wait(bar_b, par_b);
                     if (!__all_sync(0xffffffffu, ra && rb) &&
@@ -480,17 +519,19 @@ mma_q4_0_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                 tc_fence_after();
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
-                    const int g = 2 * i + j, buf = g % NBUF;
+                    const int buf = 2 * pr + j;
                     uint32_t r[CK];
                     tmem_ld_chunk<CK>(tq + (uint32_t)(buf * NT + col0), r);
                     const float dwm = dw_s[(s * 2 + j) * BM + row];
                     const uint64_t dw2 = pack2(dwm, dwm);
                     const float4* dxs = reinterpret_cast<const float4*>(dx_s + (s * 2 + j) * NT + col0);
                     tmem_ld_wait();
-                    // the slab is in registers: hand its TMEM buffer back to the MMA issuer
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(slab_empty + 8 * buf);
+                    if (!PAIRWISE || j == 1) {
+                        // the slab (pairwise: both slabs) is in registers: hand it back
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(slab_empty + 8 * (PAIRWISE ? pr : buf));
+                    }
 #pragma unroll
                     for (int c = 0; c < CK / 4; ++c) {
                         const float4 d4 = dxs[c];
