@@ -354,8 +354,13 @@ mma_q4_0_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                 constexpr int NPAIR = NBUF / 2;
                 for (int i = 0; i < n_ab && ok; ++i) {
                     const int s = i % AB_STAGES, pr = i % NPAIR;
-                    if (!wait_or_abort(ab_full + 8 * s, (i / AB_STAGES) & 1, abort_flag) ||
-                        (i >= NPAIR && !wait_or_abort(slab_empty + 8 * pr, ((i / NPAIR) + 1) & 1, abort_flag))) {
+                    // both polls in flight together; the bounded waits only when one is not done
+                    const uint32_t par_a = (uint32_t)((i / AB_STAGES) & 1), par_e = (uint32_t)(((i / NPAIR) + 1) & 1);
+                    const bool ra = mbar_try_wait(ab_full + 8 * s, par_a);
+                    const bool re = i < NPAIR || mbar_try_wait(slab_empty + 8 * pr, par_e);
+                    if (!(ra && re) &&
+                        (!wait_or_abort(ab_full + 8 * s, par_a, abort_flag) ||
+                         (i >= NPAIR && !wait_or_abort(slab_empty + 8 * pr, par_e, abort_flag)))) {
                         ok = false;
                         break;
                     }
