@@ -8,8 +8,8 @@ a CUDA graph and replayed).  Weight quantization (Q4_0 encode) happens once
 before timing, as a model load would do it, and is timed separately.
 
 Default workload: the Llama-3-8B-shaped decode projections at 1 token (q, k, v,
-o, gate, up, down, lm_head; 418 MB of Q4_0 weights), seed 2 -- the set the 1-token
-GEMV target is judged on.  The same JSON line also carries the GPT-2 117M
+o, gate, up, down, lm_head; 418 MB of Q4_0 weights), seed 2: the set the 1-token
+GEMV is measured on.  The same JSON line also carries the GPT-2 117M
 decode-step weight set (49 small matrices, launch-latency bound) and the
 tensor-core path at 512 tokens.
 
