@@ -72,6 +72,23 @@ def _load():
         lib.orc_mul_mat_q8.argtypes = [P, I64, I64, P, I64, P, P, ctypes.c_int]
         lib.orc_mul_mat_decoded_f64.argtypes = [P, I64, I64, P, I64, P]
         lib.orc_max_threads.restype = ctypes.c_int
+        lib.orc_get_rows_q4_0.restype = ctypes.c_int
+        lib.orc_get_rows_q4_0.argtypes = [P, I64, I64, P, I64, P]
+        lib.orc_get_rows_q8_0.restype = ctypes.c_int
+        lib.orc_get_rows_q8_0.argtypes = [P, I64, I64, P, I64, P]
+        lib.orc_silu.restype = ctypes.c_double
+        lib.orc_silu.argtypes = [ctypes.c_double]
+        lib.orc_gelu.restype = ctypes.c_double
+        lib.orc_gelu.argtypes = [ctypes.c_double]
+        lib.orc_bias_act.argtypes = [P, P, ctypes.c_int, I64, I64]
+        lib.orc_swiglu.argtypes = [P, P, P, I64]
+        lib.orc_vec_dot_q8_0_q8_0.restype = ctypes.c_float
+        lib.orc_vec_dot_q8_0_q8_0.argtypes = [I64, P, P]
+        lib.orc_block_isums_w8.argtypes = [P, P, I64, I64, I64, P]
+        lib.orc_mul_mat_w8_q8.restype = ctypes.c_int
+        lib.orc_mul_mat_w8_q8.argtypes = [P, I64, I64, P, I64, P, P, ctypes.c_int]
+        lib.orc_mul_mat_w8.restype = ctypes.c_int
+        lib.orc_mul_mat_w8.argtypes = [P, I64, I64, P, I64, I64, P, P, ctypes.c_int]
         _lib = lib
         return lib
 
@@ -201,3 +218,111 @@ def mul_mat_decoded_f64(src0_q4_0, ne00: int, ne01: int, src1_q8_0, ne11: int) -
     dst = np.empty((ne11, ne01), dtype=np.float64)
     _load().orc_mul_mat_decoded_f64(_ptr(a), ne00, ne01, _ptr(b), ne11, _ptr(dst))
     return dst
+
+
+# ------------------------------------------------------------ row gather --
+
+def get_rows(table, ncols: int, ids, kind: str = "q4_0"):
+    """ggml_get_rows on a quantized table: fp32 [len(ids), ncols], row i = decode(table row ids[i]).
+    Returns (rows, ok): ok is False when some id was out of range (its row is zero)."""
+    t = _u8(table)
+    idx = np.ascontiguousarray(ids, dtype=np.int32).reshape(-1)
+    bpb = Q4_0_BYTES if kind == "q4_0" else Q8_0_BYTES
+    nrows = t.size // (ncols // QK * bpb)
+    out = np.empty((idx.size, ncols), dtype=np.float32)
+    fn = _load().orc_get_rows_q4_0 if kind == "q4_0" else _load().orc_get_rows_q8_0
+    rc = fn(_ptr(t), ncols, nrows, _ptr(idx), idx.size, _ptr(out))
+    if rc == -1:
+        raise ValueError("oracle get_rows: bad shapes")
+    return out, rc == 0
+
+
+# ------------------------------------------------------------- epilogues --
+
+ACT_NONE = 0
+ACT_GELU = 1
+
+
+def silu(x: float) -> float:
+    return float(_load().orc_silu(float(x)))
+
+
+def gelu(x: float) -> float:
+    return float(_load().orc_gelu(float(x)))
+
+
+def bias_act(y, bias=None, act: int = ACT_NONE) -> np.ndarray:
+    """fp32 [ne11, ne01]: act(fp32(y + bias)) with bias repeated over the rows of y."""
+    out = _f32(y).copy()
+    ne11, ne01 = out.shape
+    b = _f32(bias) if bias is not None else None
+    _load().orc_bias_act(_ptr(out), _ptr(b) if b is not None else None, int(act), ne01, ne11)
+    return out
+
+
+def swiglu(gate, up) -> np.ndarray:
+    """fp32(fp32(silu(gate)) * up), elementwise."""
+    g = _f32(gate)
+    u = _f32(up)
+    assert g.shape == u.shape
+    out = np.empty(g.shape, dtype=np.float32)
+    _load().orc_swiglu(_ptr(g), _ptr(u), _ptr(out), g.size)
+    return out
+
+
+def mul_mat_epilogue(src0_q4_0, ne00: int, ne01: int, src1, bias=None, act: int = ACT_NONE, nthreads: int = 1):
+    """act(mul_mat + bias): returns (dst, pre, scale) where pre = fp32(mul_mat + bias)
+    (the value the activation sees) and scale the per-element tolerance scale of mul_mat."""
+    y, scale = mul_mat(src0_q4_0, ne00, ne01, src1, nthreads=nthreads)
+    pre = bias_act(y, bias, ACT_NONE)
+    return bias_act(y, bias, act), pre, scale
+
+
+def mul_mat_swiglu(gate_q4_0, up_q4_0, ne00: int, ne01: int, src1, nthreads: int = 1):
+    """silu(gate x) * (up x): returns (dst, g, u, g_scale, u_scale)."""
+    g, sg = mul_mat(gate_q4_0, ne00, ne01, src1, nthreads=nthreads)
+    u, su = mul_mat(up_q4_0, ne00, ne01, src1, nthreads=nthreads)
+    return swiglu(g, u), g, u, sg, su
+
+
+# ---------------------------------------------------------- Q8_0 weights --
+
+def vec_dot_q8_0_q8_0(n: int, x_row, y_row) -> float:
+    x_row = _u8(x_row)
+    y_row = _u8(y_row)
+    return float(_load().orc_vec_dot_q8_0_q8_0(n, _ptr(x_row), _ptr(y_row)))
+
+
+def block_isums_w8(src0_q8_0, src1_q8_0, ne00: int, ne01: int, ne11: int) -> np.ndarray:
+    """int32 [ne11, ne01, ne00/32]: per-block integer dot products of Q8_0 weights and activations."""
+    a = _u8(src0_q8_0)
+    b = _u8(src1_q8_0)
+    out = np.empty((ne11, ne01, ne00 // QK), dtype=np.int32)
+    _load().orc_block_isums_w8(_ptr(a), _ptr(b), ne00, ne01, ne11, _ptr(out))
+    return out
+
+
+def mul_mat_w8(src0_q8_0, ne00: int, ne01: int, src1, nthreads: int = 1):
+    """ggml_mul_mat(Q8_0 [ne00, ne01], F32 [ne10, ne11]) -> (dst fp32 [ne11, ne01], scale fp64)."""
+    a = _u8(src0_q8_0)
+    x = _f32(src1)
+    if x.ndim == 1:
+        x = x.reshape(1, -1)
+    ne11, ne10 = x.shape
+    dst = np.empty((ne11, ne01), dtype=np.float32)
+    scale = np.empty((ne11, ne01), dtype=np.float64)
+    rc = _load().orc_mul_mat_w8(_ptr(a), ne00, ne01, _ptr(x), ne10, ne11, _ptr(dst), _ptr(scale), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle mul_mat_w8: bad shapes")
+    return dst, scale
+
+
+def mul_mat_w8_q8(src0_q8_0, ne00: int, ne01: int, src1_q8_0, ne11: int, nthreads: int = 1):
+    a = _u8(src0_q8_0)
+    b = _u8(src1_q8_0)
+    dst = np.empty((ne11, ne01), dtype=np.float32)
+    scale = np.empty((ne11, ne01), dtype=np.float64)
+    rc = _load().orc_mul_mat_w8_q8(_ptr(a), ne00, ne01, _ptr(b), ne11, _ptr(dst), _ptr(scale), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle mul_mat_w8_q8: bad shapes")
+    return dst, scale

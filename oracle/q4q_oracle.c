@@ -326,3 +326,173 @@ void orc_mul_mat_decoded_f64(const uint8_t* src0_q4_0, int64_t ne00, int64_t ne0
         }
     }
 }
+
+/* ------------------------------------------------------ row gather -- */
+
+/* ggml_get_rows on a quantized table: the embedding lookup at the start of
+ * the Llama graph of "llama.cpp 深度解读" §4 (ggml_get_rows(tok_embeddings,
+ * inp_tokens)), with the token-embedding tensor stored as Q4_0 (the GGUF
+ * tensor-info example of §1).  Output row i is the decode (§2) of table row
+ * ids[i].  An id outside [0, nrows) leaves a row of zeros and makes the call
+ * return -2; bad shapes return -1. */
+static int get_rows(const uint8_t* src, int64_t ncols, int64_t nrows, const int32_t* ids, int64_t n,
+                    float* dst, int64_t block_bytes, int q4)
+{
+    if (ncols <= 0 || ncols % ORC_QK != 0 || nrows < 0 || n < 0) return -1;
+    int64_t row_bytes = ncols / ORC_QK * block_bytes;
+    int bad = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t id = ids[i];
+        if (id < 0 || id >= nrows) {
+            memset(dst + i * ncols, 0, (size_t)ncols * sizeof(float));
+            bad = 1;
+            continue;
+        }
+        if (q4) orc_dequantize_q4_0(src + id * row_bytes, dst + i * ncols, ncols, 1);
+        else    orc_dequantize_q8_0(src + id * row_bytes, dst + i * ncols, ncols, 1);
+    }
+    return bad ? -2 : 0;
+}
+
+int orc_get_rows_q4_0(const uint8_t* src, int64_t ncols, int64_t nrows, const int32_t* ids, int64_t n, float* dst)
+{
+    return get_rows(src, ncols, nrows, ids, n, dst, ORC_Q4_0_BYTES, 1);
+}
+
+int orc_get_rows_q8_0(const uint8_t* src, int64_t ncols, int64_t nrows, const int32_t* ids, int64_t n, float* dst)
+{
+    return get_rows(src, ncols, nrows, ids, n, dst, ORC_Q8_0_BYTES, 0);
+}
+
+/* ------------------------------------------------------- epilogues -- */
+
+/* SiLU(x) = x * sigmoid(x), as the Llama MLP of "llama.cpp 深度解读" §4
+ * (Step I) defines it, in fp64. */
+double orc_silu(double x)
+{
+    return x * (1.0 / (1.0 + exp(-x)));
+}
+
+/* GELU, named by the GPT-2 MLP of the "ggml GPT-2 117M inference
+ * walkthrough" (§3.5, F1 = GELU(Y W_fc + b_fc)) without a formula: taken as
+ * its definition x * Phi(x), Phi the standard normal CDF = erfc(-x/sqrt 2)/2. */
+double orc_gelu(double x)
+{
+    return 0.5 * x * erfc(-x / sqrt(2.0));
+}
+
+/* The bias add after a projection (ggml_add(ggml_repeat(b, cur), cur) in the
+ * GPT-2 walkthrough §3.2/§3.5: the [ne01] bias is repeated over the ne11
+ * tokens and added in fp32), then optionally GELU (act == 1), rounded to fp32.
+ * y is [ne11][ne01], updated in place; bias may be NULL. */
+void orc_bias_act(float* y, const float* bias, int act, int64_t ne01, int64_t ne11)
+{
+    for (int64_t t = 0; t < ne11; ++t) {
+        for (int64_t r = 0; r < ne01; ++r) {
+            float v = y[t * ne01 + r];
+            if (bias) v = v + bias[r];
+            if (act == 1) v = (float)orc_gelu((double)v);
+            y[t * ne01 + r] = v;
+        }
+    }
+}
+
+/* SwiGLU of the Llama MLP (§4 Step I): gate_silu = silu(gate) as an fp32
+ * tensor, then cur = gate_silu * up, an fp32 elementwise product. */
+void orc_swiglu(const float* gate, const float* up, float* y, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        float s = (float)orc_silu((double)gate[i]);
+        y[i] = s * up[i];
+    }
+}
+
+/* ------------------------------------------------ Q8_0 weights -- */
+
+/* Integer part of one block of the Q8_0 x Q8_0 dot: both blocks hold 32
+ * signed 8-bit codes in element order (the Q8_0 type listed beside Q4_0 in
+ * "llama.cpp 深度解读" §2's type table; block layout as for the activations). */
+static int32_t block_isum_w8(const uint8_t* xb, const uint8_t* yb)
+{
+    const int8_t* x = (const int8_t*)(xb + 2);
+    const int8_t* y = (const int8_t*)(yb + 2);
+    int32_t sumi = 0;
+    for (int k = 0; k < ORC_QK; ++k) sumi += (int32_t)x[k] * (int32_t)y[k];
+    return sumi;
+}
+
+/* The same block loop as §3's vec_dot with Q8_0 weights:
+ * sumf += fp32(d0 * d1) * sumi over blocks in order. */
+float orc_vec_dot_q8_0_q8_0(int64_t n, const uint8_t* vx, const uint8_t* vy)
+{
+    int64_t nb = n / ORC_QK;
+    float sumf = 0.0f;
+    for (int64_t i = 0; i < nb; ++i) {
+        const uint8_t* xb = vx + i * ORC_Q8_0_BYTES;
+        const uint8_t* yb = vy + i * ORC_Q8_0_BYTES;
+        float d = orc_f32_from_fp16(load_u16le(xb)) * orc_f32_from_fp16(load_u16le(yb));
+        sumf += d * (float)block_isum_w8(xb, yb);
+    }
+    return sumf;
+}
+
+static double vec_dot_w8_abs_scale(int64_t n, const uint8_t* vx, const uint8_t* vy)
+{
+    int64_t nb = n / ORC_QK;
+    double s = 0.0;
+    for (int64_t i = 0; i < nb; ++i) {
+        const uint8_t* xb = vx + i * ORC_Q8_0_BYTES;
+        const uint8_t* yb = vy + i * ORC_Q8_0_BYTES;
+        float d = orc_f32_from_fp16(load_u16le(xb)) * orc_f32_from_fp16(load_u16le(yb));
+        s += fabs((double)d * (double)block_isum_w8(xb, yb));
+    }
+    return s;
+}
+
+void orc_block_isums_w8(const uint8_t* src0_q8_0, const uint8_t* src1_q8_0,
+                        int64_t ne00, int64_t ne01, int64_t ne11, int32_t* out)
+{
+    int64_t nb = ne00 / ORC_QK;
+    for (int64_t i11 = 0; i11 < ne11; ++i11)
+        for (int64_t i01 = 0; i01 < ne01; ++i01)
+            for (int64_t b = 0; b < nb; ++b)
+                out[(i11 * ne01 + i01) * nb + b] =
+                    block_isum_w8(src0_q8_0 + (i01 * nb + b) * ORC_Q8_0_BYTES,
+                                  src1_q8_0 + (i11 * nb + b) * ORC_Q8_0_BYTES);
+}
+
+int orc_mul_mat_w8_q8(const uint8_t* src0_q8_0, int64_t ne00, int64_t ne01,
+                      const uint8_t* src1_q8_0, int64_t ne11,
+                      float* dst, double* abs_scale, int nthreads)
+{
+    if (ne00 <= 0 || ne00 % ORC_QK != 0 || ne01 < 0 || ne11 < 0) return -1;
+    int64_t nb = ne00 / ORC_QK;
+    for (int64_t i11 = 0; i11 < ne11; ++i11) {
+        const uint8_t* yrow = src1_q8_0 + i11 * nb * ORC_Q8_0_BYTES;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static) num_threads(nthreads > 1 ? nthreads : 1) if (nthreads > 1)
+#endif
+        for (int64_t i01 = 0; i01 < ne01; ++i01) {
+            const uint8_t* xrow = src0_q8_0 + i01 * nb * ORC_Q8_0_BYTES;
+            dst[i11 * ne01 + i01] = orc_vec_dot_q8_0_q8_0(ne00, xrow, yrow);
+            if (abs_scale) abs_scale[i11 * ne01 + i01] = vec_dot_w8_abs_scale(ne00, xrow, yrow);
+        }
+    }
+    return 0;
+}
+
+/* ggml_mul_mat(Q8_0 src0, F32 src1): src1 rows quantized to Q8_0, then one
+ * Q8_0 x Q8_0 vec_dot per output. */
+int orc_mul_mat_w8(const uint8_t* src0_q8_0, int64_t ne00, int64_t ne01,
+                   const float* src1, int64_t ne10, int64_t ne11,
+                   float* dst, double* abs_scale, int nthreads)
+{
+    if (ne00 <= 0 || ne00 % ORC_QK != 0 || ne10 != ne00 || ne01 < 0 || ne11 < 0) return -1;
+    int64_t nb = ne00 / ORC_QK;
+    uint8_t* q8 = (uint8_t*)malloc((size_t)(ne11 > 0 ? ne11 : 1) * (size_t)nb * ORC_Q8_0_BYTES);
+    if (!q8) return -1;
+    orc_quantize_q8_0(src1, q8, ne10, ne11);
+    int rc = orc_mul_mat_w8_q8(src0_q8_0, ne00, ne01, q8, ne11, dst, abs_scale, nthreads);
+    free(q8);
+    return rc;
+}

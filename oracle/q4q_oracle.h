@@ -85,6 +85,32 @@ int orc_mul_mat_q8(const uint8_t* src0_q4_0, int64_t ne00, int64_t ne01,
 void orc_mul_mat_decoded_f64(const uint8_t* src0_q4_0, int64_t ne00, int64_t ne01,
                              const uint8_t* src1_q8_0, int64_t ne11, double* dst);
 
+/* ggml_get_rows on a Q4_0 / Q8_0 table [nrows][ncols]: dst[i] = decode(row ids[i]).
+ * Returns 0; -2 if some id is outside [0, nrows) (that output row is zeroed);
+ * -1 on bad shapes. */
+int orc_get_rows_q4_0(const uint8_t* src, int64_t ncols, int64_t nrows, const int32_t* ids, int64_t n, float* dst);
+int orc_get_rows_q8_0(const uint8_t* src, int64_t ncols, int64_t nrows, const int32_t* ids, int64_t n, float* dst);
+
+/* Epilogues next to the matmul, fp64 activations rounded to fp32:
+ * silu(x) = x * sigmoid(x); gelu(x) = x * Phi(x) (a reading: the pages name GELU only). */
+double orc_silu(double x);
+double orc_gelu(double x);
+/* y[t][r] = act(fp32(y[t][r] + bias[r])), act 0 = identity, 1 = gelu; bias may be NULL. */
+void orc_bias_act(float* y, const float* bias, int act, int64_t ne01, int64_t ne11);
+/* y[i] = fp32(fp32(silu(gate[i])) * up[i]). */
+void orc_swiglu(const float* gate, const float* up, float* y, int64_t n);
+
+/* Q8_0 weights: the same contraction with 34-byte weight blocks, isum = sum_k qw_k * qx_k. */
+float orc_vec_dot_q8_0_q8_0(int64_t n, const uint8_t* vx, const uint8_t* vy);
+void orc_block_isums_w8(const uint8_t* src0_q8_0, const uint8_t* src1_q8_0,
+                        int64_t ne00, int64_t ne01, int64_t ne11, int32_t* out);
+int orc_mul_mat_w8_q8(const uint8_t* src0_q8_0, int64_t ne00, int64_t ne01,
+                      const uint8_t* src1_q8_0, int64_t ne11,
+                      float* dst, double* abs_scale, int nthreads);
+int orc_mul_mat_w8(const uint8_t* src0_q8_0, int64_t ne00, int64_t ne01,
+                   const float* src1, int64_t ne10, int64_t ne11,
+                   float* dst, double* abs_scale, int nthreads);
+
 int orc_max_threads(void);
 
 #ifdef __cplusplus
