@@ -61,9 +61,10 @@ def _measured_peaks():
 
 def kernel_source_hash(kernel_file: str) -> str:
     """First 16 hex digits of the sha256 of a kernel's source file followed by the
-    shared device header it includes (either change invalidates a profile)."""
+    shared device headers it includes (any change invalidates a profile)."""
     h = hashlib.sha256()
-    for f in (kernel_file, "q4q_common.cuh"):
+    headers = ("q4q_gemv.cuh", "q4q_common.cuh") if kernel_file.startswith("q4q_gemv") else ("q4q_common.cuh",)
+    for f in (kernel_file,) + headers:
         with open(os.path.join(ROOT, "q4_quantized_matmul_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -368,6 +369,7 @@ def run_ours(args, rank, world, local_rank):
     second = (measure_decode(dev, stream, args.secondary_decode)
               if (rank == 0 and args.secondary_decode not in ("", "none") and args.secondary_decode != args.workload)
               else None)
+    nxt = measure_next(dev, stream) if (rank == 0 and args.next_rows) else None
 
     # ---- CPU baseline: the oracle on this host's cores, bounded sample
     cpu = cpu_baseline(args.workload, ne11, budget_s=args.cpu_seconds) if (rank == 0 and args.cpu_seconds > 0) else None
@@ -438,6 +440,7 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clocks,
         "batched": batched,
         "secondary_decode": second,
+        "next_rows": nxt,
     }
     return line
 
@@ -574,6 +577,175 @@ def measure_batched(dev, stream, args):
     return out
 
 
+def _replay_ms(stream, graph, reps, calls_per_replay):
+    """Average ms per call of `graph` (calls_per_replay calls) over `reps` replays, after 3 warm-ups."""
+    import torch
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            graph.replay()
+        e0.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / (reps * calls_per_replay)
+
+
+def _capture(stream, fn):
+    import torch
+    with torch.cuda.stream(stream):
+        fn()                       # first call outside capture (one-time set-up per kernel)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def measure_next(dev, stream):
+    """The operations next to the matmul, each timed on its own with weights rotated
+    over more than 3 x L2 (CUDA graphs, CUDA events on the launching stream):
+      * swiglu: the Llama-3-8B gate and up projections (4096 -> 14336, Q4_0) at one
+        token through q4q_mul_mat_swiglu (one dual-weight GEMV), against the two
+        plain q4q_mul_mat calls it replaces;
+      * gpt2_bias_gelu: the GPT-2 117M decode-step set (49 matrices) with a bias on
+        every projection but the lm_head and GELU on c_mlp_fc (q4q_mul_mat_bias_act);
+      * get_rows: the Llama-3-8B-shaped token embedding (4096 x 128256, Q4_0): 512
+        token ids, and the whole-table decode (HBM-bound);
+      * q8_0_decode: the Llama-3-8B decode set with Q8_0 weights at one token
+        (q4q_mul_mat_q8_0), PDL-chained like the main workload."""
+    import torch
+
+    import q4_quantized_matmul_gb300 as q4q
+    from q4_quantized_matmul_gb300 import workloads
+    peak, kind = _measured_peaks()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    PDL = q4q.Q4Q_MUL_MAT_PDL
+    out = {}
+
+    # ---- one pass over the Llama set: Q8_0 copies of all 8, Q4_0 gate / up / lm_head
+    llama = list(workloads.WORKLOADS["llama3_8b_decode"].shapes)
+    w8, xs, q4 = [], [], {}
+    for i, (ne00, ne01) in enumerate(llama):
+        w, x = workloads.problem("llama3_8b_decode", i)
+        wd = torch.from_numpy(w).to(dev)
+        w8.append(q4q.q4q_quantize_q8_0(wd))
+        if i in (4, 5, 7):
+            q4[i] = q4q.q4q_quantize_q4_0(wd)
+        del wd
+        xs.append(torch.from_numpy(x).to(dev))
+
+    # ---- SwiGLU: gate + up fused vs two plain calls
+    ne00, ne01 = llama[4]
+    wb = 2 * q4[4].numel()
+    copies = max(2, -(-3 * l2 // wb))
+    gates = [q4[4]] + [q4[4].clone() for _ in range(copies - 1)]
+    ups = [q4[5]] + [q4[5].clone() for _ in range(copies - 1)]
+    x = xs[4]
+    y = torch.empty((1, ne01), dtype=torch.float32, device=dev)
+    yg = torch.empty_like(y)
+    ws = torch.empty(q4q.q4q_mul_mat_swiglu_workspace_size(ne00, ne01, 1), dtype=torch.uint8, device=dev)
+    reps = 50
+    g_f = _capture(stream, lambda: [q4q.q4q_mul_mat_swiglu(gates[c], ups[c], ne00, ne01, x, dst=y, workspace=ws,
+                                                           flags=PDL)
+                                    for c in range(copies)])
+    ms_f = _replay_ms(stream, g_f, reps, copies)
+    g_u = _capture(stream, lambda: [(q4q.q4q_mul_mat(gates[c], ne00, ne01, x, dst=yg, workspace=ws, flags=PDL),
+                                     q4q.q4q_mul_mat(ups[c], ne00, ne01, x, dst=y, workspace=ws, flags=PDL))
+                                    for c in range(copies)])
+    ms_u = _replay_ms(stream, g_u, reps, copies)
+    alg = wb + 4 * ne00 + 4 * ne01
+    out["swiglu"] = {
+        "shape": "gate, up %d->%d (Q4_0), 1 token" % (ne00, ne01), "kernel": "gemv_q4_0_swiglu_kernel",
+        "us_per_call": round(ms_f * 1e3, 2), "unfused_us_per_pair": round(ms_u * 1e3, 2),
+        "roofline": {"bound": "hbm", "achieved": round(alg / (ms_f * 1e-3) / 1e9, 1), "peak": peak,
+                     "peak_kind": kind, "unit": "GB/s", "frac": round(alg / (ms_f * 1e-3) / 1e9 / peak, 4),
+                     "algorithmic_bytes_per_launch": alg},
+        "note": "graph of %d PDL-chained calls over rotating weight copies; the unfused figure is two "
+                "q4q_mul_mat calls (gate, up) without the elementwise SwiGLU" % copies}
+    del gates, ups, g_f, g_u
+
+    # ---- get_rows on the token embedding
+    ne00, ne01 = llama[7]
+    table = q4[7]
+    rng = np.random.default_rng(5)
+    ids = torch.from_numpy(rng.integers(0, ne01, size=512).astype(np.int32)).to(dev)
+    rows = torch.empty((512, ne00), dtype=torch.float32, device=dev)
+    g_r = _capture(stream, lambda: [q4q.q4q_get_rows_q4_0(table, ne00, ne01, ids=ids, dst=rows) for _ in range(20)])
+    ms_r = _replay_ms(stream, g_r, 20, 20)
+    full = torch.empty((ne01, ne00), dtype=torch.float32, device=dev)
+    g_a = _capture(stream, lambda: q4q.q4q_get_rows_q4_0(table, ne00, ne01, dst=full))
+    ms_a = _replay_ms(stream, g_a, 10, 1)
+    rb = ne00 // 32 * 18
+    alg_a = ne01 * rb + 4 * ne01 * ne00
+    out["get_rows"] = {
+        "table": "token embedding %d x %d Q4_0 (%.1f MB)" % (ne01, ne00, ne01 * rb / 1e6), "kernel": "get_rows_kernel",
+        "ids_512": {"us_per_call": round(ms_r * 1e3, 2),
+                    "gb_s": round((512 * rb + 512 * ne00 * 4) / (ms_r * 1e-3) / 1e9, 1)},
+        "whole_table": {"us_per_call": round(ms_a * 1e3, 1),
+                        "roofline": {"bound": "hbm", "achieved": round(alg_a / (ms_a * 1e-3) / 1e9, 1),
+                                     "peak": peak, "peak_kind": kind, "unit": "GB/s",
+                                     "frac": round(alg_a / (ms_a * 1e-3) / 1e9 / peak, 4),
+                                     "algorithmic_bytes_per_launch": alg_a}},
+        "note": "512 random ids: 20 calls per graph, launch-latency bound; whole table: Q4_0 read + fp32 write"}
+    del full, rows, g_r, g_a, q4
+
+    # ---- Q8_0-weight decode set
+    wb8 = sum(t.numel() for t in w8)
+    copies = max(2, -(-3 * l2 // wb8))
+    sets = [w8] + [[t.clone() for t in w8] for _ in range(copies - 1)]
+    ys = [torch.empty((1, n), dtype=torch.float32, device=dev) for _, n in llama]
+    ws = torch.empty(max(q4q.q4q_mul_mat_q8_0_workspace_size(k, n, 1) for k, n in llama), dtype=torch.uint8,
+                     device=dev)
+    g_8 = _capture(stream, lambda: [q4q.q4q_mul_mat_q8_0(sets[c][i], k, n, xs[i], dst=ys[i], workspace=ws,
+                                                         flags=PDL)
+                                    for c in range(copies) for i, (k, n) in enumerate(llama)])
+    ms_8 = _replay_ms(stream, g_8, 100, copies)
+    alg8 = wb8 + sum(4 * k + 4 * n for k, n in llama)
+    out["q8_0_decode"] = {
+        "workload": "llama3_8b_decode with Q8_0 weights (%.1f MB)" % (wb8 / 1e6), "kernel": "gemv_q8_0_kernel",
+        "ms_per_step": round(ms_8, 5), "weight_gb_s": round(wb8 / (ms_8 * 1e-3) / 1e9, 1),
+        "roofline": {"bound": "hbm", "achieved": round(alg8 / (ms_8 * 1e-3) / 1e9, 1), "peak": peak,
+                     "peak_kind": kind, "unit": "GB/s", "frac": round(alg8 / (ms_8 * 1e-3) / 1e9 / peak, 4),
+                     "algorithmic_bytes_per_launch": alg8 / len(llama)},
+        "note": "8 PDL-chained q4q_mul_mat_q8_0 calls per step, graph of %d steps over weight copies" % copies}
+    del sets, w8, g_8, xs, ys
+
+    # ---- GPT-2 decode step with bias (+ GELU on c_mlp_fc)
+    name = "gpt2_decode_step"
+    shapes = list(workloads.WORKLOADS[name].shapes)
+    wq, gx, bs, ds, acts = [], [], [], [], []
+    for i, (ne00, ne01) in enumerate(shapes):
+        w, xx = workloads.problem(name, i, 1)
+        wd = torch.from_numpy(w).to(dev)
+        wq.append(q4q.q4q_quantize_q4_0(wd))
+        del wd
+        gx.append(torch.from_numpy(xx).to(dev))
+        last = i == len(shapes) - 1
+        bs.append(None if last else torch.from_numpy(workloads.gen_bias(ne01, 1, i)).to(dev))
+        acts.append(q4q.Q4Q_ACT_GELU if (not last and i % 4 == 2) else q4q.Q4Q_ACT_NONE)
+        ds.append(torch.empty((1, ne01), dtype=torch.float32, device=dev))
+    wbg = _weights_bytes(shapes)
+    copies = max(2, -(-3 * l2 // wbg))
+    wsets = [wq] + [[t.clone() for t in wq] for _ in range(copies - 1)]
+    ws = torch.empty(max(q4q.q4q_mul_mat_workspace_size(k, n, 1) for k, n in shapes), dtype=torch.uint8, device=dev)
+    g_b = _capture(stream, lambda: [q4q.q4q_mul_mat_bias_act(wsets[c][i], k, n, gx[i], bias=bs[i], act=acts[i],
+                                                             dst=ds[i], workspace=ws, flags=PDL)
+                                    for c in range(copies) for i, (k, n) in enumerate(shapes)])
+    ms_b = _replay_ms(stream, g_b, 50, copies)
+    out["gpt2_bias_gelu"] = {
+        "workload": "gpt2_decode_step with bias on 48 projections and GELU on the 12 c_mlp_fc",
+        "kernel": "gemv_q4_0_kernel (bias / GELU in the output write)",
+        "ms_per_step": round(ms_b, 5), "weight_gb_s": round(wbg / (ms_b * 1e-3) / 1e9, 1),
+        "us_per_matrix": round(ms_b * 1e3 / len(shapes), 3),
+        "note": "49 PDL-chained q4q_mul_mat_bias_act calls per step; compare secondary_decode (no epilogue)"}
+    del wsets, wq, gx, bs, ds, g_b
+    torch.cuda.empty_cache()
+    return out
+
+
 def _measured_bf16():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -703,6 +875,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline budget (0 = skip)")
     ap.add_argument("--batched-tokens", type=int, default=512,
                     help="also measure the tensor-core path on the Llama-3-8B set at this many tokens (0 = skip)")
+    ap.add_argument("--next-rows", type=int, default=1,
+                    help="also time SwiGLU, bias/GELU, get_rows and Q8_0 weights (0 = skip)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 

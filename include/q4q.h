@@ -132,6 +132,92 @@ Q4Q_API q4q_status q4q_mul_mat_ex(const void* src0, int64_t ne00, int64_t ne01,
                           float* dst, void* workspace, size_t workspace_bytes,
                           unsigned int flags, q4q_stream_t stream);
 
+/* ------------------------------------------------ next to the matmul ---- */
+
+/* Activations of q4q_mul_mat_bias_act. */
+#define Q4Q_ACT_NONE 0
+#define Q4Q_ACT_GELU 1   /* GELU(v) = v * Phi(v), Phi the standard normal CDF */
+
+/* The projection, its bias and its activation in one call: the GPT-2 graph of
+ * the "ggml GPT-2 117M inference walkthrough" adds a bias after every projection
+ * (§3.2, §3.5: ggml_add(ggml_repeat(b, cur), cur)) and applies GELU after the
+ * MLP's first one (§3.5, F1 = GELU(Y W_fc + b_fc)); "llama.cpp 深度解读" §4 names
+ * "matmul + bias + activation" as the fusion a graph allows.  The page names
+ * GELU without a formula; this library uses its definition v * Phi(v).
+ *   dst[i11*ne01 + i01] = act(fp32(mul_mat[i11][i01] + bias[i01]))
+ * with mul_mat exactly as q4q_mul_mat computes it.  bias: device fp32 [ne01]
+ * (4-byte aligned) or NULL for none; act: Q4Q_ACT_NONE or Q4Q_ACT_GELU, else
+ * Q4Q_ERR_ARG.  Everything else (arguments, workspace, flags, limits, errors)
+ * as q4q_mul_mat_ex.  For ne11 < 8 the epilogue runs inside the GEMV (one launch);
+ * other paths apply it with one elementwise kernel over dst after the matmul. */
+Q4Q_API q4q_status q4q_mul_mat_bias_act(const void* src0, int64_t ne00, int64_t ne01,
+                                const float* src1, int64_t ne10, int64_t ne11,
+                                const float* bias, int act, float* dst,
+                                void* workspace, size_t workspace_bytes,
+                                unsigned int flags, q4q_stream_t stream);
+
+/* Bytes of device workspace q4q_mul_mat_swiglu needs: q4q_mul_mat_workspace_size
+ * rounded up to 256, plus 4 * ne01 * ne11 for the gate projection on the paths
+ * that do not fuse it. */
+Q4Q_API q4q_status q4q_mul_mat_swiglu_workspace_size(int64_t ne00, int64_t ne01, int64_t ne11, size_t* bytes);
+
+/* The Llama MLP's gate and up projections with SwiGLU ("llama.cpp 深度解读" §4,
+ * Step I: up = ffn_up x, gate = ffn_gate x, cur = silu(gate) * up with SiLU(x) =
+ * x * sigmoid(x)):
+ *   dst[i11*ne01 + i01] = fp32(silu(g) * u),  g = mul_mat(gate)[i11][i01],
+ *                                             u = mul_mat(up)[i11][i01].
+ * gate, up: Q4_0 weights of the same shape [ne00, ne01] (layout and alignment as
+ * q4q_mul_mat's src0); src1, dst, flags, limits and errors as q4q_mul_mat_ex;
+ * workspace: q4q_mul_mat_swiglu_workspace_size bytes, 256-byte aligned (the fused
+ * path does not touch it).  For ne11 < 8 with 16-byte aligned operands and
+ * ne00 % 256 == 0 both matrices stream through one GEMV launch and only the
+ * product is written; otherwise the two projections run as q4q_mul_mat calls
+ * (gate into the workspace) followed by one elementwise kernel. */
+Q4Q_API q4q_status q4q_mul_mat_swiglu(const void* gate, const void* up, int64_t ne00, int64_t ne01,
+                              const float* src1, int64_t ne10, int64_t ne11, float* dst,
+                              void* workspace, size_t workspace_bytes, unsigned int flags,
+                              q4q_stream_t stream);
+
+/* ggml_get_rows on a quantized table (the embedding lookup that starts the Llama
+ * graph of "llama.cpp 深度解读" §4, ggml_get_rows(tok_embeddings, inp_tokens), with
+ * the token-embedding tensor stored as Q4_0 as §1's GGUF example shows):
+ *   dst[i*ne00 + k] = decode(src0 row ids[i])[k],  decode as §2: (nibble - 8) * d
+ *   (Q4_0) or q * d (Q8_0), exact in fp32.
+ * src0: ne01 rows of ne00/32 blocks (2-byte aligned); ids: device int32 [n_ids]
+ * (4-byte aligned), or NULL for rows 0 .. n_ids-1 (the whole-table decode, which
+ * then requires n_ids <= ne01); dst: device fp32 [n_ids][ne00], 16-byte aligned.
+ * An id outside [0, ne01) is not read: its output row is written as zeros and
+ * Q4Q_ERR_ARG is recorded in the device status word (q4q_device_status).
+ * Limits: 0 < ne00 < 2^20, ne00 % 32 == 0, 0 <= ne01, n_ids < 2^31. */
+Q4Q_API q4q_status q4q_get_rows_q4_0(const void* src0, int64_t ne00, int64_t ne01, const int32_t* ids,
+                             int64_t n_ids, float* dst, q4q_stream_t stream);
+Q4Q_API q4q_status q4q_get_rows_q8_0(const void* src0, int64_t ne00, int64_t ne01, const int32_t* ids,
+                             int64_t n_ids, float* dst, q4q_stream_t stream);
+
+/* Bytes of device workspace q4q_mul_mat_q8_0 needs (the Q8_0 activations of the
+ * generic path: ne11 * ne00/32 * 34). */
+Q4Q_API q4q_status q4q_mul_mat_q8_0_workspace_size(int64_t ne00, int64_t ne01, int64_t ne11, size_t* bytes);
+
+/* ggml_mul_mat with Q8_0 weights (the Q8_0 type of "llama.cpp 深度解读" §2's type
+ * table; block {fp16 d; int8 qs[32]}, element k = qs[k] * d):
+ *   dst[i11*ne01 + i01] = sum_b fp32(d_w * d_x) * isum,  isum = sum_k qw_k * qx_k,
+ * src1 rows quantized to Q8_0 as q4q_quantize_q8_0 does.  src0: ne01 rows of
+ * ne00/32 34-byte blocks (2-byte aligned); everything else as q4q_mul_mat_ex.
+ * With ne00 % 256 == 0 and 16-byte aligned src0 / src1 every launch is the GEMV
+ * (batches of more than 7 tokens run in chunks of 7, each streaming the weights:
+ * there is no tensor-core path for Q8_0 weights); otherwise a generic kernel
+ * over Q8_0 activations in the workspace. */
+Q4Q_API q4q_status q4q_mul_mat_q8_0(const void* src0, int64_t ne00, int64_t ne01,
+                            const float* src1, int64_t ne10, int64_t ne11,
+                            float* dst, void* workspace, size_t workspace_bytes,
+                            unsigned int flags, q4q_stream_t stream);
+
+/* Debug: per-block integer sums of Q8_0 weights and Q8_0 activations from the
+ * Q8_0 GEMV's block-dot routine: out int32 [ne11][ne01][ne00/32].  Requires
+ * ne00 % 64 == 0 and 2-byte aligned inputs.  Small shapes only (tests). */
+Q4Q_API q4q_status q4q_debug_block_isums_q8_0(const void* src0_q8_0, const void* src1_q8_0, int64_t ne00,
+                                      int64_t ne01, int64_t ne11, int32_t* out, q4q_stream_t stream);
+
 /* Size of the library-owned scratch array used by q4q_mul_mat_noalloc (per GPU). */
 #define Q4Q_NOALLOC_SCRATCH_BYTES (8u << 20)
 

@@ -22,6 +22,9 @@ __all__ = [
     "q4q_mul_mat", "q4q_debug_block_isums", "q4q_debug_workspace_size", "Q4Q_MUL_MAT_PDL",
     "q4q_mul_mat_noalloc", "Q4Q_NOALLOC_SCRATCH_BYTES", "q4q_device_status", "q4q_status_string",
     "q4q_version", "q4_0_row_bytes", "q8_0_row_bytes", "mul_mat_host",
+    "Q4Q_ACT_NONE", "Q4Q_ACT_GELU", "q4q_mul_mat_bias_act", "q4q_mul_mat_swiglu_workspace_size",
+    "q4q_mul_mat_swiglu", "q4q_get_rows_q4_0", "q4q_get_rows_q8_0", "q4q_mul_mat_q8_0_workspace_size",
+    "q4q_mul_mat_q8_0", "q4q_debug_block_isums_q8_0",
 ]
 
 QK = 32
@@ -207,3 +210,135 @@ def mul_mat_host(src0: torch.Tensor, ne00: int, ne01: int, src1_host: torch.Tens
     q4q_mul_mat(src0, ne00, ne01, src1_dev, dst=dst_dev, workspace=workspace, stream=stream)
     dst_host.copy_(dst_dev, non_blocking=True)
     return dst_host
+
+
+# ------------------------------------------------------ next to the matmul --
+
+Q4Q_ACT_NONE = 0
+Q4Q_ACT_GELU = 1
+
+
+def _acts_2d(src1: torch.Tensor) -> torch.Tensor:
+    if src1.dtype != torch.float32:
+        raise TypeError("src1 must be float32")
+    return src1.reshape(-1, src1.shape[-1]) if src1.dim() != 2 else src1
+
+
+def _workspace(need: int, workspace: Optional[torch.Tensor], device):
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=device)
+    if workspace is not None and workspace.numel() > 0:
+        return _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
+    return None, 0
+
+
+def q4q_mul_mat_bias_act(src0: torch.Tensor, ne00: int, ne01: int, src1: torch.Tensor,
+                         bias: Optional[torch.Tensor] = None, act: int = Q4Q_ACT_NONE,
+                         dst: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                         stream=None, flags: int = 0) -> torch.Tensor:
+    """act(ggml_mul_mat(Q4_0 src0, F32 src1) + bias) -> F32 [ne11, ne01]; bias fp32 [ne01] or None."""
+    x = _acts_2d(src1)
+    ne11, ne10 = x.shape
+    if dst is None:
+        dst = torch.empty((ne11, ne01), dtype=torch.float32, device=x.device)
+    if ne01 * ne11 == 0:
+        return dst
+    if bias is not None and (bias.dtype != torch.float32 or bias.numel() != ne01):
+        raise ValueError("bias must be float32 with ne01 elements")
+    ws_ptr, ws_bytes = _workspace(q4q_mul_mat_workspace_size(ne00, ne01, ne11), workspace, x.device)
+    _check("q4q_mul_mat_bias_act", _lib.load().q4q_mul_mat_bias_act(
+        _dev(src0, "src0", ne01 * q4_0_row_bytes(ne00)), ne00, ne01, _dev(x, "src1"), ne10, ne11,
+        _dev(bias, "bias", 4 * ne01) if bias is not None else None, int(act), _dev(dst, "dst", 4 * ne01 * ne11),
+        ws_ptr, ws_bytes, int(flags), _stream(stream)))
+    return dst
+
+
+def q4q_mul_mat_swiglu_workspace_size(ne00: int, ne01: int, ne11: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check("q4q_mul_mat_swiglu_workspace_size",
+           _lib.load().q4q_mul_mat_swiglu_workspace_size(ne00, ne01, ne11, ctypes.byref(n)))
+    return int(n.value)
+
+
+def q4q_mul_mat_swiglu(gate: torch.Tensor, up: torch.Tensor, ne00: int, ne01: int, src1: torch.Tensor,
+                       dst: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                       stream=None, flags: int = 0) -> torch.Tensor:
+    """silu(ggml_mul_mat(gate, src1)) * ggml_mul_mat(up, src1) -> F32 [ne11, ne01] (Q4_0 gate and up)."""
+    x = _acts_2d(src1)
+    ne11, ne10 = x.shape
+    if dst is None:
+        dst = torch.empty((ne11, ne01), dtype=torch.float32, device=x.device)
+    if ne01 * ne11 == 0:
+        return dst
+    ws_ptr, ws_bytes = _workspace(q4q_mul_mat_swiglu_workspace_size(ne00, ne01, ne11), workspace, x.device)
+    nbytes = ne01 * q4_0_row_bytes(ne00)
+    _check("q4q_mul_mat_swiglu", _lib.load().q4q_mul_mat_swiglu(
+        _dev(gate, "gate", nbytes), _dev(up, "up", nbytes), ne00, ne01, _dev(x, "src1"), ne10, ne11,
+        _dev(dst, "dst", 4 * ne01 * ne11), ws_ptr, ws_bytes, int(flags), _stream(stream)))
+    return dst
+
+
+def _get_rows(fn: str, row_bytes, src0: torch.Tensor, ne00: int, ne01: int, ids: Optional[torch.Tensor],
+              n_ids: Optional[int], dst: Optional[torch.Tensor], stream) -> torch.Tensor:
+    if ids is not None:
+        if ids.dtype != torch.int32:
+            raise TypeError("ids must be int32")
+        n_ids = ids.numel()
+    elif n_ids is None:
+        n_ids = ne01
+    if dst is None:
+        dst = torch.empty((n_ids, ne00), dtype=torch.float32, device=src0.device)
+    if n_ids == 0:
+        return dst
+    _check(fn, getattr(_lib.load(), fn)(_dev(src0, "src0", ne01 * row_bytes(ne00)), ne00, ne01,
+                                         _dev(ids, "ids", 4 * n_ids) if ids is not None else None, n_ids,
+                                         _dev(dst, "dst", 4 * n_ids * ne00), _stream(stream)))
+    return dst
+
+
+def q4q_get_rows_q4_0(src0: torch.Tensor, ne00: int, ne01: int, ids: Optional[torch.Tensor] = None,
+                      n_ids: Optional[int] = None, dst: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """ggml_get_rows on a Q4_0 table [ne01 rows of ne00]: fp32 [n_ids, ne00]; ids None = rows 0..n_ids-1."""
+    return _get_rows("q4q_get_rows_q4_0", q4_0_row_bytes, src0, ne00, ne01, ids, n_ids, dst, stream)
+
+
+def q4q_get_rows_q8_0(src0: torch.Tensor, ne00: int, ne01: int, ids: Optional[torch.Tensor] = None,
+                      n_ids: Optional[int] = None, dst: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """ggml_get_rows on a Q8_0 table [ne01 rows of ne00]: fp32 [n_ids, ne00]; ids None = rows 0..n_ids-1."""
+    return _get_rows("q4q_get_rows_q8_0", q8_0_row_bytes, src0, ne00, ne01, ids, n_ids, dst, stream)
+
+
+def q4q_mul_mat_q8_0_workspace_size(ne00: int, ne01: int, ne11: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check("q4q_mul_mat_q8_0_workspace_size",
+           _lib.load().q4q_mul_mat_q8_0_workspace_size(ne00, ne01, ne11, ctypes.byref(n)))
+    return int(n.value)
+
+
+def q4q_mul_mat_q8_0(src0: torch.Tensor, ne00: int, ne01: int, src1: torch.Tensor,
+                     dst: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                     stream=None, flags: int = 0) -> torch.Tensor:
+    """ggml_mul_mat(Q8_0 src0 [ne00, ne01], F32 src1 [ne00, ne11]) -> F32 [ne11, ne01]."""
+    x = _acts_2d(src1)
+    ne11, ne10 = x.shape
+    if dst is None:
+        dst = torch.empty((ne11, ne01), dtype=torch.float32, device=x.device)
+    if ne01 * ne11 == 0:
+        return dst
+    ws_ptr, ws_bytes = _workspace(q4q_mul_mat_q8_0_workspace_size(ne00, ne01, ne11), workspace, x.device)
+    _check("q4q_mul_mat_q8_0", _lib.load().q4q_mul_mat_q8_0(
+        _dev(src0, "src0", ne01 * q8_0_row_bytes(ne00)), ne00, ne01, _dev(x, "src1"), ne10, ne11,
+        _dev(dst, "dst", 4 * ne01 * ne11), ws_ptr, ws_bytes, int(flags), _stream(stream)))
+    return dst
+
+
+def q4q_debug_block_isums_q8_0(src0_q8_0: torch.Tensor, src1_q8_0: torch.Tensor, ne00: int, ne01: int, ne11: int,
+                               out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """int32 [ne11, ne01, ne00/32] block sums of Q8_0 weights x Q8_0 activations (GEMV routine)."""
+    if out is None:
+        out = torch.empty((ne11, ne01, ne00 // QK), dtype=torch.int32, device=src0_q8_0.device)
+    _check("q4q_debug_block_isums_q8_0", _lib.load().q4q_debug_block_isums_q8_0(
+        _dev(src0_q8_0, "src0_q8_0", ne01 * q8_0_row_bytes(ne00)),
+        _dev(src1_q8_0, "src1_q8_0", ne11 * q8_0_row_bytes(ne00)), ne00, ne01, ne11,
+        _dev(out, "out", 4 * ne11 * ne01 * (ne00 // QK)), _stream(stream)))
+    return out

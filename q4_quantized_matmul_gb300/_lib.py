@@ -27,6 +27,15 @@ _SIGNATURES = {
     "q4q_mul_mat": (STATUS, [P, I64, I64, P, I64, I64, P, P, ctypes.c_size_t, P]),
     "q4q_mul_mat_ex": (STATUS, [P, I64, I64, P, I64, I64, P, P, ctypes.c_size_t, ctypes.c_uint, P]),
     "q4q_mul_mat_noalloc": (STATUS, [P, I64, I64, P, I64, I64, P, P]),
+    "q4q_mul_mat_bias_act": (STATUS, [P, I64, I64, P, I64, I64, P, ctypes.c_int, P, P, ctypes.c_size_t,
+                                      ctypes.c_uint, P]),
+    "q4q_mul_mat_swiglu_workspace_size": (STATUS, [I64, I64, I64, ctypes.POINTER(ctypes.c_size_t)]),
+    "q4q_mul_mat_swiglu": (STATUS, [P, P, I64, I64, P, I64, I64, P, P, ctypes.c_size_t, ctypes.c_uint, P]),
+    "q4q_get_rows_q4_0": (STATUS, [P, I64, I64, P, I64, P, P]),
+    "q4q_get_rows_q8_0": (STATUS, [P, I64, I64, P, I64, P, P]),
+    "q4q_mul_mat_q8_0_workspace_size": (STATUS, [I64, I64, I64, ctypes.POINTER(ctypes.c_size_t)]),
+    "q4q_mul_mat_q8_0": (STATUS, [P, I64, I64, P, I64, I64, P, P, ctypes.c_size_t, ctypes.c_uint, P]),
+    "q4q_debug_block_isums_q8_0": (STATUS, [P, P, I64, I64, I64, P, P]),
     "q4q_debug_workspace_size": (STATUS, [I64, I64, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]),
     "q4q_debug_block_isums": (STATUS, [P, P, I64, I64, I64, ctypes.c_int, P, P, ctypes.c_size_t, P]),
     "q4q_device_status": (STATUS, [ctypes.POINTER(ctypes.c_int)]),

@@ -43,8 +43,6 @@ q4q_status launch_status() {
     return cudaGetLastError() == cudaSuccess ? Q4Q_OK : Q4Q_ERR_CUDA;
 }
 
-namespace {
-
 q4q_status check_mul_mat_shapes(int64_t ne00, int64_t ne01, int64_t ne10, int64_t ne11) {
     if (ne00 <= 0 || ne00 % QK != 0 || ne00 >= (1 << 20)) return Q4Q_ERR_SHAPE;
     if (ne10 != ne00) return Q4Q_ERR_SHAPE;
@@ -52,7 +50,6 @@ q4q_status check_mul_mat_shapes(int64_t ne00, int64_t ne01, int64_t ne10, int64_
     return Q4Q_OK;
 }
 
-}  // namespace
 }  // namespace q4q
 
 using namespace q4q;
@@ -130,9 +127,15 @@ extern "C" q4q_status q4q_debug_block_isums(const void* src0, const void* src1_q
 extern "C" q4q_status q4q_device_status(q4q_status* status) {
     if (!status) return Q4Q_ERR_NULL;
     if (cudaDeviceSynchronize() != cudaSuccess) return Q4Q_ERR_CUDA;
-    unsigned int a = gemv_take_device_status();
-    unsigned int b = mma_take_device_status();
-    *status = (q4q_status)(a ? a : b);
+    // every translation unit that records device errors has its own word: read
+    // and clear all of them, report the first one set
+    const unsigned int words[] = {gemv_take_device_status(), mma_take_device_status(),
+                                  gemv_swiglu_take_device_status(), gemv_w8_take_device_status(),
+                                  rows_take_device_status()};
+    unsigned int first = 0;
+    for (unsigned int w : words)
+        if (!first) first = w;
+    *status = (q4q_status)first;
     return Q4Q_OK;
 }
 
@@ -150,4 +153,4 @@ extern "C" const char* q4q_status_string(q4q_status s) {
     return "unknown status";
 }
 
-extern "C" int q4q_version(void) { return (1 << 16) | 0; }
+extern "C" int q4q_version(void) { return (1 << 16) | 1; }

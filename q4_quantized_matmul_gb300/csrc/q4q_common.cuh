@@ -162,6 +162,27 @@ __device__ __forceinline__ uint32_t pack_q4_word(const float (&v)[8], float d) {
     return w;
 }
 
+// ------------------------------------------------------ output activations --
+
+// GELU(v) = v * Phi(v), Phi the standard normal CDF, written with erfc so that
+// the small tail values keep their relative accuracy (1 + erf(v / sqrt 2) would
+// cancel for negative v).  The pages name GELU for the GPT-2 MLP without a
+// formula; this is its definition.
+__device__ __forceinline__ float gelu_f32(float v) {
+    return __fmul_rn(__fmul_rn(0.5f, v), erfcf(__fmul_rn(-v, 0.70710678118654752f)));
+}
+
+// SiLU(g) = g * sigmoid(g) = g / (1 + exp(-g)) ("llama.cpp 深度解读" §4, the Llama
+// MLP); exp(-g) overflowing to infinity gives -0 for very negative g.
+__device__ __forceinline__ float silu_f32(float g) {
+    return __fdiv_rn(g, __fadd_rn(1.0f, expf(-g)));
+}
+
+// SwiGLU of the same MLP: silu(gate) * up.
+__device__ __forceinline__ float swiglu_f32(float gate, float up) {
+    return __fmul_rn(silu_f32(gate), up);
+}
+
 // ------------------------------------------------------------- async copy --
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

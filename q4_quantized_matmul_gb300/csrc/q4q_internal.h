@@ -42,13 +42,40 @@ q4q_status mma_debug_isums(const void* src0, const void* src1_q8_0, int64_t ne00
 bool gemv_supported(const void* src0, int64_t ne00, int64_t ne01, const float* src1, int64_t ne11,
                     const DeviceInfo& info);
 q4q_status gemv_mul_mat(const void* src0, int64_t ne00, int64_t ne01, const float* src1, int64_t ne11,
-                        float* dst, cudaStream_t stream, const DeviceInfo& info, bool pdl);
+                        float* dst, cudaStream_t stream, const DeviceInfo& info, bool pdl,
+                        const float* bias = nullptr, int act = Q4Q_ACT_NONE);
 size_t generic_workspace_bytes(int64_t ne00, int64_t ne11);
 q4q_status generic_mul_mat(const void* src0, int64_t ne00, int64_t ne01, const float* src1, int64_t ne11,
                            float* dst, void* workspace, size_t workspace_bytes, cudaStream_t stream,
                            const DeviceInfo& info);
 q4q_status gemv_debug_isums(const void* src0, const void* src1_q8_0, int64_t ne00, int64_t ne01,
                             int64_t ne11, int32_t* out, cudaStream_t stream, const DeviceInfo& info);
+
+// dual-weight GEMV with the SwiGLU epilogue (q4q_gemv_swiglu.cu)
+unsigned int gemv_swiglu_take_device_status();
+bool gemv_swiglu_supported(const void* gate, const void* up, int64_t ne00, int64_t ne01, const float* src1,
+                           int64_t ne11, const DeviceInfo& info);
+q4q_status gemv_mul_mat_swiglu(const void* gate, const void* up, int64_t ne00, int64_t ne01, const float* src1,
+                               int64_t ne11, float* dst, cudaStream_t stream, const DeviceInfo& info, bool pdl);
+
+// Q8_0 weights (q4q_gemv_w8.cu)
+unsigned int gemv_w8_take_device_status();
+bool gemv_w8_supported(const void* src0, int64_t ne00, int64_t ne01, const float* src1, int64_t ne11,
+                       const DeviceInfo& info);
+q4q_status gemv_mul_mat_w8(const void* src0, int64_t ne00, int64_t ne01, const float* src1, int64_t ne11,
+                           float* dst, cudaStream_t stream, const DeviceInfo& info, bool pdl, const float* bias,
+                           int act);
+q4q_status generic_mul_mat_w8(const void* src0, int64_t ne00, int64_t ne01, const float* src1, int64_t ne11,
+                              float* dst, void* workspace, size_t workspace_bytes, cudaStream_t stream,
+                              const DeviceInfo& info, const float* bias, int act);
+q4q_status gemv_w8_debug_isums(const void* src0, const void* src1_q8_0, int64_t ne00, int64_t ne01, int64_t ne11,
+                               int32_t* out, cudaStream_t stream, const DeviceInfo& info);
+
+// row gather (q4q_rows.cu)
+unsigned int rows_take_device_status();
+
+// Shape rules shared by every matmul entry point (q4q_api.cu).
+q4q_status check_mul_mat_shapes(int64_t ne00, int64_t ne01, int64_t ne10, int64_t ne11);
 
 // quantizers (q4q_quant.cu), also used by the GEMM / generic paths
 q4q_status launch_quantize(bool q4, const float* src, void* dst, int64_t ncols, int64_t nrows,

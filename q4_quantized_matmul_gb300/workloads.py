@@ -144,3 +144,11 @@ def random_problem(ne00: int, ne01: int, ne11: int, seed: int, wscale: float = 0
     w = rng.standard_normal((ne01, ne00), dtype=np.float32) * np.float32(wscale)
     x = rng.standard_normal((ne11, ne00), dtype=np.float32)
     return w, x
+
+
+def gen_bias(ne01: int, seed: int, index: int, scale: float = 0.1) -> np.ndarray:
+    """fp32 [ne01] projection bias ~ N(0, scale), for the bias epilogues (its own stream)."""
+    rng = _rng(seed, index, 1 << 20)
+    b = rng.standard_normal(ne01, dtype=np.float32)
+    b *= np.float32(scale)
+    return b

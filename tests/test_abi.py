@@ -112,3 +112,49 @@ def test_binding_fails_loudly_without_cuda_tensors(lib):
     import q4_quantized_matmul_gb300 as q4q
     with pytest.raises(TypeError):
         q4q.q4q_quantize_q4_0(torch.zeros(2, 32))
+
+
+def test_argument_errors_of_the_entry_points_next_to_the_matmul(lib):
+    P = ctypes.c_void_p
+    fake = P(0x1000)
+    n = ctypes.c_size_t(0)
+    # bias / activation
+    assert lib.q4q_mul_mat_bias_act(fake, 33, 4, fake, 33, 1, fake, 0, fake, None, 0, 0, None) == 2
+    assert lib.q4q_mul_mat_bias_act(fake, 64, 4, fake, 64, 1, fake, 2, fake, None, 0, 0, None) == 7
+    assert lib.q4q_mul_mat_bias_act(fake, 64, 4, fake, 64, 1, fake, 0, fake, None, 0, 4, None) == 7
+    assert lib.q4q_mul_mat_bias_act(fake, 64, 4, fake, 64, 1, P(0x1002), 1, fake, None, 0, 0, None) == 3
+    assert lib.q4q_mul_mat_bias_act(fake, 64, 4, fake, 64, 1, None, 0, None, None, 0, 0, None) == 1
+    assert lib.q4q_mul_mat_bias_act(None, 64, 0, None, 64, 1, None, 1, None, None, 0, 0, None) == 0
+    # SwiGLU
+    assert lib.q4q_mul_mat_swiglu(fake, fake, 64, 4, fake, 96, 1, fake, None, 0, 0, None) == 2
+    assert lib.q4q_mul_mat_swiglu(fake, None, 64, 4, fake, 64, 1, fake, None, 0, 0, None) == 1
+    assert lib.q4q_mul_mat_swiglu(fake, P(0x1001), 64, 4, fake, 64, 1, fake, None, 0, 0, None) == 3
+    assert lib.q4q_mul_mat_swiglu(fake, fake, 64, 4, fake, 64, 1, fake, None, 0, 8, None) == 7
+    assert lib.q4q_mul_mat_swiglu(None, None, 64, 4, None, 64, 0, None, None, 0, 0, None) == 0
+    assert lib.q4q_mul_mat_swiglu_workspace_size(64, 4, 3, None) == 1
+    # get_rows
+    for fn in (lib.q4q_get_rows_q4_0, lib.q4q_get_rows_q8_0):
+        assert fn(fake, 48, 10, fake, 3, fake, None) == 2
+        assert fn(fake, 64, 10, None, 11, fake, None) == 2      # whole-table decode past the end
+        assert fn(fake, 64, 10, fake, -1, fake, None) == 2
+        assert fn(fake, 64, 10, fake, 0, fake, None) == 0
+        assert fn(None, 64, 10, fake, 3, fake, None) == 1
+        assert fn(fake, 64, 10, fake, 3, P(0x1004), None) == 3   # dst not 16-byte aligned
+        assert fn(fake, 64, 10, P(0x1002), 3, fake, None) == 3
+    # Q8_0 weights
+    assert lib.q4q_mul_mat_q8_0(fake, 33, 4, fake, 33, 1, fake, None, 0, 0, None) == 2
+    assert lib.q4q_mul_mat_q8_0(P(0x1001), 64, 4, fake, 64, 1, fake, None, 0, 0, None) == 3
+    assert lib.q4q_mul_mat_q8_0(fake, 64, 4, fake, 64, 1, fake, None, 0, 2, None) == 7
+    assert lib.q4q_mul_mat_q8_0(None, 64, 0, None, 64, 1, None, None, 0, 0, None) == 0
+    assert lib.q4q_mul_mat_q8_0_workspace_size(64, 4, 3, ctypes.byref(n)) == 0
+    assert n.value == 3 * 2 * 34
+    assert lib.q4q_debug_block_isums_q8_0(fake, fake, 48, 2, 1, fake, None) == 2
+    assert lib.q4q_debug_block_isums_q8_0(fake, None, 64, 2, 1, fake, None) == 1
+
+
+def test_new_bindings_fail_loudly_without_cuda_tensors(lib):
+    import torch
+    import q4_quantized_matmul_gb300 as q4q
+    w = torch.zeros(4 * 18 * 2, dtype=torch.uint8)
+    with pytest.raises(TypeError):
+        q4q.q4q_get_rows_q4_0(w, 64, 4, ids=torch.zeros(2, dtype=torch.int32))
