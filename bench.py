@@ -615,7 +615,9 @@ def measure_next(dev, stream):
       * get_rows: the Llama-3-8B-shaped token embedding (4096 x 128256, Q4_0): 512
         token ids, and the whole-table decode (HBM-bound);
       * q8_0_decode: the Llama-3-8B decode set with Q8_0 weights at one token
-        (q4q_mul_mat_q8_0), PDL-chained like the main workload."""
+        (q4q_mul_mat_q8_0), PDL-chained like the main workload;
+      * llama3_8b_decode_fused: the main workload's weights with q/k/v as one
+        group launch and gate/up as one SwiGLU launch (5 launches per step)."""
     import torch
 
     import q4_quantized_matmul_gb300 as q4q
@@ -711,7 +713,45 @@ def measure_next(dev, stream):
                      "peak_kind": kind, "unit": "GB/s", "frac": round(alg8 / (ms_8 * 1e-3) / 1e9 / peak, 4),
                      "algorithmic_bytes_per_launch": alg8 / len(llama)},
         "note": "8 PDL-chained q4q_mul_mat_q8_0 calls per step, graph of %d steps over weight copies" % copies}
-    del sets, w8, g_8, xs, ys
+    del sets, w8, g_8, ys
+
+    # ---- the Llama decode set with the fused launches: q, k, v as one group launch, o,
+    #      gate and up as one SwiGLU launch, down, lm_head (5 launches instead of 8); the
+    #      q/k/v group shares one input and the SwiGLU reads both gate and up, as in a layer
+    q4s = []
+    for i, (k, n) in enumerate(llama):
+        w, _ = workloads.problem("llama3_8b_decode", i)
+        wd = torch.from_numpy(w).to(dev)
+        q4s.append(q4q.q4q_quantize_q4_0(wd))
+        del wd
+    wb4 = _weights_bytes(llama)
+    copies = max(4, -(-3 * l2 // wb4))
+    fsets = [q4s] + [[t.clone() for t in q4s] for _ in range(copies - 1)]
+    h, f = llama[0][0], llama[4][1]
+    xq = xs[0]
+    outs = [torch.empty((1, n), dtype=torch.float32, device=dev) for _, n in llama]
+    ws = torch.empty(max(q4q.q4q_mul_mat_swiglu_workspace_size(k, n, 1) for k, n in llama), dtype=torch.uint8,
+                     device=dev)
+
+    def fused_step(c):
+        W = fsets[c]
+        q4q.q4q_mul_mat_group([W[0], W[1], W[2]], [llama[0][1], llama[1][1], llama[2][1]], h, xq,
+                              dsts=outs[0:3], workspace=ws, flags=PDL)
+        q4q.q4q_mul_mat(W[3], h, llama[3][1], xs[3], dst=outs[3], workspace=ws, flags=PDL)
+        q4q.q4q_mul_mat_swiglu(W[4], W[5], h, f, xs[4], dst=outs[4], workspace=ws, flags=PDL)
+        q4q.q4q_mul_mat(W[6], llama[6][0], llama[6][1], xs[6], dst=outs[6], workspace=ws, flags=PDL)
+        q4q.q4q_mul_mat(W[7], h, llama[7][1], xs[7], dst=outs[7], workspace=ws, flags=PDL)
+
+    g_fs = _capture(stream, lambda: [fused_step(c) for c in range(copies)])
+    ms_fs = _replay_ms(stream, g_fs, 250, copies)
+    out["llama3_8b_decode_fused"] = {
+        "workload": "llama3_8b_decode weights (%.1f MB Q4_0) with q/k/v grouped (one input) and gate/up fused "
+                    "into SwiGLU: 5 launches per step" % (wb4 / 1e6),
+        "kernels": "gemv_q4_0_group_kernel, gemv_q4_0_kernel, gemv_q4_0_swiglu_kernel",
+        "ms_per_step": round(ms_fs, 5), "weight_gb_s": round(wb4 / (ms_fs * 1e-3) / 1e9, 1),
+        "frac_of_hbm": round(wb4 / (ms_fs * 1e-3) / 1e9 / peak, 4),
+        "note": "same weight bytes as the main workload; graph of %d PDL-chained steps over weight copies" % copies}
+    del fsets, q4s, g_fs, outs, xs
 
     # ---- GPT-2 decode step with bias (+ GELU on c_mlp_fc)
     name = "gpt2_decode_step"

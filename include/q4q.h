@@ -178,6 +178,32 @@ Q4Q_API q4q_status q4q_mul_mat_swiglu(const void* gate, const void* up, int64_t 
                               void* workspace, size_t workspace_bytes, unsigned int flags,
                               q4q_stream_t stream);
 
+/* Most matrices one q4q_mul_mat_group call takes. */
+#define Q4Q_GROUP_MAX 4
+
+/* Bytes of device workspace q4q_mul_mat_group needs: the largest
+ * q4q_mul_mat_workspace_size over the n matrices. */
+Q4Q_API q4q_status q4q_mul_mat_group_workspace_size(int n, const int64_t* ne01, int64_t ne00, int64_t ne11,
+                                            size_t* bytes);
+
+/* Several Q4_0 projections of one input: for m < n,
+ *   dst[m] = ggml_mul_mat(src0[m] [ne00, ne01[m]], src1 [ne10, ne11]),  dst[m] F32 [ne01[m], ne11],
+ * each exactly as q4q_mul_mat computes it.  This is the q, k and v projections
+ * of a layer with separate wq / wk / wv weights ("llama.cpp 深度解读" §3.2 of the
+ * Gemma3 graph: llm_build_mul_mat_qkv takes either a fused wqkv or the three
+ * tensors); a fused wqkv is a single q4q_mul_mat over concatenated rows.
+ * n: 1 .. Q4Q_GROUP_MAX, else Q4Q_ERR_ARG.  src0, ne01, dst: HOST arrays of n
+ * entries (src0[m], dst[m] are device pointers, aligned as q4q_mul_mat requires;
+ * the outputs must not overlap each other or src1).  Matrices with ne01[m] == 0
+ * are skipped.  workspace: q4q_mul_mat_group_workspace_size bytes.  flags and
+ * errors as q4q_mul_mat_ex.  For ne11 < 8 with ne00 % 256 == 0 and 16-byte aligned
+ * weights and src1, all matrices stream through one GEMV launch that quantizes
+ * src1 once; otherwise one q4q_mul_mat_ex call per matrix. */
+Q4Q_API q4q_status q4q_mul_mat_group(int n, const void* const* src0, const int64_t* ne01, int64_t ne00,
+                             const float* src1, int64_t ne10, int64_t ne11, float* const* dst,
+                             void* workspace, size_t workspace_bytes, unsigned int flags,
+                             q4q_stream_t stream);
+
 /* ggml_get_rows on a quantized table (the embedding lookup that starts the Llama
  * graph of "llama.cpp 深度解读" §4, ggml_get_rows(tok_embeddings, inp_tokens), with
  * the token-embedding tensor stored as Q4_0 as §1's GGUF example shows):

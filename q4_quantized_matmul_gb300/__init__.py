@@ -24,7 +24,8 @@ __all__ = [
     "q4q_version", "q4_0_row_bytes", "q8_0_row_bytes", "mul_mat_host",
     "Q4Q_ACT_NONE", "Q4Q_ACT_GELU", "q4q_mul_mat_bias_act", "q4q_mul_mat_swiglu_workspace_size",
     "q4q_mul_mat_swiglu", "q4q_get_rows_q4_0", "q4q_get_rows_q8_0", "q4q_mul_mat_q8_0_workspace_size",
-    "q4q_mul_mat_q8_0", "q4q_debug_block_isums_q8_0",
+    "q4q_mul_mat_q8_0", "q4q_debug_block_isums_q8_0", "Q4Q_GROUP_MAX", "q4q_mul_mat_group_workspace_size",
+    "q4q_mul_mat_group",
 ]
 
 QK = 32
@@ -342,3 +343,36 @@ def q4q_debug_block_isums_q8_0(src0_q8_0: torch.Tensor, src1_q8_0: torch.Tensor,
         _dev(src1_q8_0, "src1_q8_0", ne11 * q8_0_row_bytes(ne00)), ne00, ne01, ne11,
         _dev(out, "out", 4 * ne11 * ne01 * (ne00 // QK)), _stream(stream)))
     return out
+
+
+Q4Q_GROUP_MAX = 4
+
+
+def q4q_mul_mat_group_workspace_size(ne01s, ne00: int, ne11: int) -> int:
+    n = len(ne01s)
+    arr = (ctypes.c_int64 * max(n, 1))(*ne01s)
+    out = ctypes.c_size_t(0)
+    _check("q4q_mul_mat_group_workspace_size",
+           _lib.load().q4q_mul_mat_group_workspace_size(n, arr, ne00, ne11, ctypes.byref(out)))
+    return int(out.value)
+
+
+def q4q_mul_mat_group(src0s, ne01s, ne00: int, src1: torch.Tensor, dsts=None,
+                      workspace: Optional[torch.Tensor] = None, stream=None, flags: int = 0):
+    """[ggml_mul_mat(src0s[m] (Q4_0 [ne00, ne01s[m]]), src1) for m] in one call: F32 [ne11, ne01s[m]] each."""
+    x = _acts_2d(src1)
+    ne11, ne10 = x.shape
+    n = len(src0s)
+    if n != len(ne01s):
+        raise ValueError("one row count per matrix")
+    if dsts is None:
+        dsts = [torch.empty((ne11, r), dtype=torch.float32, device=x.device) for r in ne01s]
+    if ne11 == 0 or n == 0:
+        return dsts
+    ws_ptr, ws_bytes = _workspace(q4q_mul_mat_group_workspace_size(ne01s, ne00, ne11), workspace, x.device)
+    ptrs = (ctypes.c_void_p * n)(*[_dev(w, "src0", r * q4_0_row_bytes(ne00)).value for w, r in zip(src0s, ne01s)])
+    outs = (ctypes.c_void_p * n)(*[_dev(d, "dst", 4 * r * ne11).value for d, r in zip(dsts, ne01s)])
+    rows = (ctypes.c_int64 * n)(*ne01s)
+    _check("q4q_mul_mat_group", _lib.load().q4q_mul_mat_group(n, ptrs, rows, ne00, _dev(x, "src1"), ne10, ne11, outs,
+                                                             ws_ptr, ws_bytes, int(flags), _stream(stream)))
+    return dsts

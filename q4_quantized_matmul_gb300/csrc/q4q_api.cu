@@ -131,6 +131,7 @@ extern "C" q4q_status q4q_device_status(q4q_status* status) {
     // and clear all of them, report the first one set
     const unsigned int words[] = {gemv_take_device_status(), mma_take_device_status(),
                                   gemv_swiglu_take_device_status(), gemv_w8_take_device_status(),
+                                  gemv_group_take_device_status(), gemv_epi_take_device_status(),
                                   rows_take_device_status()};
     unsigned int first = 0;
     for (unsigned int w : words)

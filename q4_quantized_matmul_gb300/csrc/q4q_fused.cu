@@ -5,7 +5,8 @@
 //    cur), then GELU on the MLP's first projection) -- "matmul + bias +
 //    activation", the fusion "llama.cpp 深度解读" §4 names as a graph benefit;
 //  * the Llama MLP's SwiGLU, silu(ffn_gate x) * (ffn_up x) (same page, §4 Step I);
-//  * ggml_mul_mat with Q8_0 weights (the Q8_0 type of that page's §2 table).
+//  * ggml_mul_mat with Q8_0 weights (the Q8_0 type of that page's §2 table);
+//  * several projections of one input (q, k, v) in one launch.
 // For 1..7 tokens the epilogues run inside the GEMV (q4q_gemv*.cu); other paths
 // run the matmul and then one elementwise kernel over its output.
 #include <algorithm>
@@ -64,8 +65,8 @@ extern "C" q4q_status q4q_mul_mat_bias_act(const void* src0, int64_t ne00, int64
     if ((st = current_device_info(&info)) != Q4Q_OK) return st;
     cudaStream_t stream = (cudaStream_t)stream_;
     if (ne11 < 8 && gemv_supported(src0, ne00, ne01, src1, ne11, info))
-        return gemv_mul_mat(src0, ne00, ne01, src1, ne11, dst, stream, info, (flags & Q4Q_MUL_MAT_PDL) != 0,
-                            bias, act);
+        return gemv_mul_mat_epi(src0, ne00, ne01, src1, ne11, dst, stream, info, (flags & Q4Q_MUL_MAT_PDL) != 0,
+                                bias, act);
     st = q4q_mul_mat_ex(src0, ne00, ne01, src1, ne10, ne11, dst, workspace, workspace_bytes, 0u, stream_);
     if (st != Q4Q_OK || (!bias && act == Q4Q_ACT_NONE)) return st;
     const int64_t total = ne01 * ne11;
@@ -141,13 +142,12 @@ extern "C" q4q_status q4q_mul_mat_q8_0(const void* src0, int64_t ne00, int64_t n
         for (int64_t t0 = 0; t0 < ne11; t0 += 7) {
             const int64_t nt = std::min<int64_t>(7, ne11 - t0);
             st = gemv_mul_mat_w8(src0, ne00, ne01, src1 + t0 * ne00, nt, dst + t0 * ne01, stream, info,
-                                 pdl && t0 == 0, nullptr, Q4Q_ACT_NONE);
+                                 pdl && t0 == 0);
             if (st != Q4Q_OK) return st;
         }
         return Q4Q_OK;
     }
-    return generic_mul_mat_w8(src0, ne00, ne01, src1, ne11, dst, workspace, workspace_bytes, stream, info, nullptr,
-                              Q4Q_ACT_NONE);
+    return generic_mul_mat_w8(src0, ne00, ne01, src1, ne11, dst, workspace, workspace_bytes, stream, info);
 }
 
 extern "C" q4q_status q4q_debug_block_isums_q8_0(const void* src0_q8_0, const void* src1_q8_0, int64_t ne00,
@@ -160,4 +160,57 @@ extern "C" q4q_status q4q_debug_block_isums_q8_0(const void* src0_q8_0, const vo
     DeviceInfo info;
     if ((st = current_device_info(&info)) != Q4Q_OK) return st;
     return gemv_w8_debug_isums(src0_q8_0, src1_q8_0, ne00, ne01, ne11, out, (cudaStream_t)stream_, info);
+}
+
+extern "C" q4q_status q4q_mul_mat_group_workspace_size(int n, const int64_t* ne01, int64_t ne00, int64_t ne11,
+                                                       size_t* bytes) {
+    if (!bytes || !ne01) return Q4Q_ERR_NULL;
+    if (n < 1 || n > Q4Q_GROUP_MAX) return Q4Q_ERR_ARG;
+    size_t need = 0;
+    for (int m = 0; m < n; ++m) {
+        size_t b = 0;
+        q4q_status st = q4q_mul_mat_workspace_size(ne00, ne01[m], ne11, &b);
+        if (st != Q4Q_OK) return st;
+        need = std::max(need, b);
+    }
+    *bytes = need;
+    return Q4Q_OK;
+}
+
+extern "C" q4q_status q4q_mul_mat_group(int n, const void* const* src0, const int64_t* ne01, int64_t ne00,
+                                        const float* src1, int64_t ne10, int64_t ne11, float* const* dst,
+                                        void* workspace, size_t workspace_bytes, unsigned int flags,
+                                        q4q_stream_t stream_) {
+    if (flags & ~Q4Q_MUL_MAT_PDL) return Q4Q_ERR_ARG;
+    if (n < 1 || n > Q4Q_GROUP_MAX) return Q4Q_ERR_ARG;
+    if (!src0 || !ne01 || !dst) return Q4Q_ERR_NULL;
+    q4q_status st;
+    // the non-empty matrices, in order
+    const void* w[Q4Q_GROUP_MAX];
+    int64_t rows[Q4Q_GROUP_MAX];
+    float* out[Q4Q_GROUP_MAX];
+    int k = 0;
+    for (int m = 0; m < n; ++m) {
+        if ((st = check_mul_mat_shapes(ne00, ne01[m], ne10, ne11)) != Q4Q_OK) return st;
+        if (ne01[m] == 0 || ne11 == 0) continue;
+        if (!src0[m] || !dst[m]) return Q4Q_ERR_NULL;
+        if (!aligned(src0[m], 2) || !aligned(dst[m], 4)) return Q4Q_ERR_ALIGN;
+        w[k] = src0[m];
+        rows[k] = ne01[m];
+        out[k] = dst[m];
+        ++k;
+    }
+    if (k == 0) return Q4Q_OK;
+    if (!src1) return Q4Q_ERR_NULL;
+    if (!aligned(src1, 4)) return Q4Q_ERR_ALIGN;
+    DeviceInfo info;
+    if ((st = current_device_info(&info)) != Q4Q_OK) return st;
+    cudaStream_t stream = (cudaStream_t)stream_;
+    if (ne11 < 8 && gemv_group_supported(k, w, rows, ne00, src1, ne11, info))
+        return gemv_mul_mat_group(k, w, rows, ne00, src1, ne11, out, stream, info, (flags & Q4Q_MUL_MAT_PDL) != 0);
+    for (int m = 0; m < k; ++m)
+        if ((st = q4q_mul_mat_ex(w[m], ne00, rows[m], src1, ne10, ne11, out[m], workspace, workspace_bytes, flags,
+                                 stream_)) != Q4Q_OK)
+            return st;
+    return Q4Q_OK;
 }

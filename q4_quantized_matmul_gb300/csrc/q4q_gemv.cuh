@@ -49,6 +49,20 @@ constexpr int MAX_STAGES = 8;
 constexpr int PLAIN_THREADS = 256;      // generic and debug kernels
 constexpr int WQ4_0 = 0;                 // weight block types
 constexpr int WQ8_0 = 1;
+constexpr int M_SINGLE = 0;              // kernel modes: one matrix,
+constexpr int M_DUAL = 1;                //   two matrices, SwiGLU of the pair,
+constexpr int M_GROUP = 2;               //   up to GROUP_MAX matrices with one input,
+constexpr int M_EPI = 3;                 //   one matrix with the bias / activation epilogue
+constexpr int GROUP_MAX = Q4Q_GROUP_MAX;
+
+// Group mode: matrix m owns the units [unit0[m], unit0[m+1]) (unit0[n] = all units).
+struct GemvGroup {
+    int n;
+    int unit0[GROUP_MAX + 1];
+    int rows[GROUP_MAX];
+    const uint8_t* w[GROUP_MAX];
+    float* dst[GROUP_MAX];
+};
 constexpr int64_t CLUSTER_MIN_X = 8192;  // activations (elements) from which CTA pairs share the quantization
 
 struct GemvParams {
@@ -62,7 +76,39 @@ struct GemvParams {
     int half_off;      // dual-weight ring: offset of the second matrix's rows in a stage
     int act;           // Q4Q_ACT_* applied to every output (after the bias)
     const float* bias; // [ne01] added to every output row, or null
+    GemvGroup grp;     // group mode only
 };
+
+// The rows a unit covers: its matrix's weights, output and row count, and its
+// first row there.  Group mode picks the matrix with static indices only (a
+// dynamic index into the parameter struct would copy it to local memory).
+struct UnitRows {
+    const uint8_t* w;
+    float* dst;
+    int rows, r0;
+};
+
+template <int MODE>
+__device__ __forceinline__ UnitRows unit_rows(const GemvParams& p, const uint8_t* w, float* dst, int u) {
+    UnitRows r{w, dst, p.ne01, u * p.G};
+    if constexpr (MODE == M_GROUP) {
+        r.w = p.grp.w[0];
+        r.dst = p.grp.dst[0];
+        r.rows = p.grp.rows[0];
+        int base = 0;
+#pragma unroll
+        for (int q = 1; q < GROUP_MAX; ++q) {
+            if (q < p.grp.n && u >= p.grp.unit0[q]) {
+                r.w = p.grp.w[q];
+                r.dst = p.grp.dst[q];
+                r.rows = p.grp.rows[q];
+                base = p.grp.unit0[q];
+            }
+        }
+        r.r0 = (u - base) * p.G;
+    }
+    return r;
+}
 
 // Integer dot of one pair of Q4_0 blocks (9 aligned words, block a at byte 0,
 // block b at byte 18) against Q8_0 activations in the even/odd quad layout.
@@ -325,13 +371,17 @@ __device__ __forceinline__ void consumer_sync() {
 // shared memory of every CTA of its cluster, so each SM loads only 1/CL of the
 // fp32 activations from L2.  DUAL: two weight matrices of the same shape (w and
 // w2) are streamed side by side, each unit's rows of both in one stage, and every
-// output is silu(w x) * (w2 x) (the SwiGLU of the Llama MLP); otherwise every
-// output is the bias / activation epilogue of p applied to w x.
-template <int WT, int T, int LPR, int PPL, int CL, bool DUAL>
+// output is silu(w x) * (w2 x) (the SwiGLU of the Llama MLP).  EPI: every output
+// is the bias / activation epilogue of p applied to w x (the plain kernel carries
+// no epilogue code at all).  GROUP: the units
+// run over up to GROUP_MAX matrices of rows that share the activations (the q, k
+// and v projections of one input), each written to its own output.
+template <int WT, int T, int LPR, int PPL, int CL, int MODE>
 __device__ __forceinline__ void gemv_body(const uint8_t* __restrict__ w, const uint8_t* __restrict__ w2,
                                           const float* __restrict__ x, float* __restrict__ dst,
                                           const GemvParams& p) {
     static_assert(PPL == 0 || T == 1, "register-resident activations are for one token");
+    constexpr bool DUAL = MODE == M_DUAL;
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem);              // full[0..7], empty[8..15]
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 128);
@@ -380,11 +430,12 @@ __device__ __forceinline__ void gemv_body(const uint8_t* __restrict__ w, const u
                         break;
                     }
                 }
-                const int r0 = u * p.G;
-                const int nr = min(p.G, p.ne01 - r0);
+                const UnitRows ur = unit_rows<MODE>(p, w, dst, u);
+                const int r0 = ur.r0;
+                const int nr = min(p.G, ur.rows - r0);
                 const uint32_t bytes = (uint32_t)nr * (uint32_t)p.row_bytes;
                 mbar_arrive_expect_tx(full0 + 8 * s, DUAL ? 2 * bytes : bytes);
-                bulk_g2s(smem_u32(stages + (size_t)s * p.stage_bytes), w + (int64_t)r0 * p.row_bytes, bytes,
+                bulk_g2s(smem_u32(stages + (size_t)s * p.stage_bytes), ur.w + (int64_t)r0 * p.row_bytes, bytes,
                          full0 + 8 * s);
                 if constexpr (DUAL)
                     bulk_g2s(smem_u32(stages + (size_t)s * p.stage_bytes + p.half_off),
@@ -463,8 +514,9 @@ __device__ __forceinline__ void gemv_body(const uint8_t* __restrict__ w, const u
             mbar_try_wait(bar, par);       // per-lane acquire of the completed phase
         }
         const uint8_t* stage = stages + (size_t)s * p.stage_bytes;
-        const int r0 = u * p.G;
-        const int nr = min(p.G, p.ne01 - r0);
+        const UnitRows ur = unit_rows<MODE>(p, w, dst, u);
+        const int r0 = ur.r0;
+        const int nr = min(p.G, ur.rows - r0);
         for (int pass = 0; pass < passes; ++pass) {
             const int j = rr + pass * RP;
             const bool valid = j < nr;
@@ -505,8 +557,9 @@ __device__ __forceinline__ void gemv_body(const uint8_t* __restrict__ w, const u
                 for (int t = 0; t < T; ++t) {
                     float v;
                     if constexpr (DUAL) v = swiglu_f32(acc[t], acc2[t]);
-                    else v = output_epilogue(acc[t], p, r0 + j);
-                    dst[(int64_t)t * p.ne01 + r0 + j] = v;
+                    else if constexpr (MODE == M_EPI) v = output_epilogue(acc[t], p, r0 + j);
+                    else v = acc[t];
+                    ur.dst[(int64_t)t * ur.rows + r0 + j] = v;
                 }
             }
         }
@@ -516,34 +569,51 @@ __device__ __forceinline__ void gemv_body(const uint8_t* __restrict__ w, const u
 }
 
 
-// The three kernels share one body and one signature (w2 is unused unless DUAL).
+// The kernels share one body and one signature (w2 is unused unless dual; the
+// group kernel takes its pointers from p.grp).
 template <int T, int LPR, int PPL, int CL>
 __global__ void __launch_bounds__(THREADS, PPL <= 3 ? 2 : 1)
 gemv_q4_0_kernel(const uint8_t* __restrict__ w, const uint8_t* __restrict__ w2, const float* __restrict__ x,
                  float* __restrict__ dst, const GemvParams p) {
-    gemv_body<WQ4_0, T, LPR, PPL, CL, false>(w, w2, x, dst, p);
+    gemv_body<WQ4_0, T, LPR, PPL, CL, M_SINGLE>(w, w2, x, dst, p);
 }
 
 template <int T, int LPR, int PPL, int CL>
 __global__ void __launch_bounds__(THREADS, PPL <= 3 ? 2 : 1)
 gemv_q4_0_swiglu_kernel(const uint8_t* __restrict__ w, const uint8_t* __restrict__ w2, const float* __restrict__ x,
                         float* __restrict__ dst, const GemvParams p) {
-    gemv_body<WQ4_0, T, LPR, PPL, CL, true>(w, w2, x, dst, p);
+    gemv_body<WQ4_0, T, LPR, PPL, CL, M_DUAL>(w, w2, x, dst, p);
 }
 
 template <int T, int LPR, int PPL, int CL>
 __global__ void __launch_bounds__(THREADS, PPL <= 3 ? 2 : 1)
 gemv_q8_0_kernel(const uint8_t* __restrict__ w, const uint8_t* __restrict__ w2, const float* __restrict__ x,
                  float* __restrict__ dst, const GemvParams p) {
-    gemv_body<WQ8_0, T, LPR, PPL, CL, false>(w, w2, x, dst, p);
+    gemv_body<WQ8_0, T, LPR, PPL, CL, M_SINGLE>(w, w2, x, dst, p);
+}
+
+template <int T, int LPR, int PPL, int CL>
+__global__ void __launch_bounds__(THREADS, PPL <= 3 ? 2 : 1)
+gemv_q4_0_epi_kernel(const uint8_t* __restrict__ w, const uint8_t* __restrict__ w2, const float* __restrict__ x,
+                     float* __restrict__ dst, const GemvParams p) {
+    gemv_body<WQ4_0, T, LPR, PPL, CL, M_EPI>(w, w2, x, dst, p);
+}
+
+template <int T, int LPR, int PPL, int CL>
+__global__ void __launch_bounds__(THREADS, PPL <= 3 ? 2 : 1)
+gemv_q4_0_group_kernel(const uint8_t* __restrict__ w, const uint8_t* __restrict__ w2, const float* __restrict__ x,
+                       float* __restrict__ dst, const GemvParams p) {
+    gemv_body<WQ4_0, T, LPR, PPL, CL, M_GROUP>(w, w2, x, dst, p);
 }
 
 using GemvKernelFn = void (*)(const uint8_t*, const uint8_t*, const float*, float*, const GemvParams);
 
-template <int WT, bool DUAL, int T, int LPR, int PPL, int CL>
+template <int WT, int MODE, int T, int LPR, int PPL, int CL>
 GemvKernelFn gemv_kernel_fn() {
-    static_assert(!(DUAL && WT != WQ4_0), "the dual-weight kernel is built for Q4_0 weights");
-    if constexpr (DUAL) return gemv_q4_0_swiglu_kernel<T, LPR, PPL, CL>;
+    static_assert(MODE == M_SINGLE || WT == WQ4_0, "the dual, epilogue and group kernels are built for Q4_0");
+    if constexpr (MODE == M_DUAL) return gemv_q4_0_swiglu_kernel<T, LPR, PPL, CL>;
+    else if constexpr (MODE == M_EPI) return gemv_q4_0_epi_kernel<T, LPR, PPL, CL>;
+    else if constexpr (MODE == M_GROUP) return gemv_q4_0_group_kernel<T, LPR, PPL, CL>;
     else if constexpr (WT == WQ8_0) return gemv_q8_0_kernel<T, LPR, PPL, CL>;
     else return gemv_q4_0_kernel<T, LPR, PPL, CL>;
 }
@@ -556,6 +626,7 @@ struct GemvArgs {
     float* dst;
     const float* bias;      // may be null
     int act;
+    GemvGroup grp;          // group kernel only
 };
 
 struct GemvPlan {
@@ -563,6 +634,7 @@ struct GemvPlan {
     int lpr;
     int ppl_reg;       // > 0: activations in registers
     int grid;          // CTAs without clusters
+    int grid_cap;      // CTAs the device holds at once (grid = min(units, grid_cap))
     int cl;            // cluster size to try (1 or 2)
     int sms;
     size_t smem;
@@ -629,9 +701,11 @@ bool plan_gemv(int64_t ne00, int64_t ne01, int64_t ne11, const DeviceInfo& info,
     p.half_off = (int)(G * p.row_bytes);
     p.act = Q4Q_ACT_NONE;
     p.bias = nullptr;
+    p.grp = GemvGroup{};
     plan->smem = (size_t)(head + act_bytes + S * stage);
     plan->lpr = lpr;
     const int per_sm = (!small && plan->smem <= 113 * 1024 && two_per_sm) ? 2 : 1;
+    plan->grid_cap = (int)(sms * per_sm);
     plan->grid = (int)std::min<int64_t>(p.n_units, sms * per_sm);
     plan->sms = (int)sms;
     // Splitting the activation quantization over a pair of CTAs pays only where
@@ -671,12 +745,12 @@ cudaLaunchConfig_t gemv_config(const GemvPlan& plan, int grid, cudaStream_t stre
 // Raise the kernel's opt-in shared-memory size (once per device and size), and
 // return how many of its CTAs fit on the device at once in clusters of CL
 // (cached per device and shared-memory size; 0 if the query fails).
-template <int WT, bool DUAL, int T, int LPR, int PPL, int CL>
+template <int WT, int MODE, int T, int LPR, int PPL, int CL>
 int gemv_prepare(const GemvPlan& plan, int device) {
     static std::mutex mu;
     static std::map<std::pair<int, size_t>, int> resident;
     static int configured[64] = {};
-    const GemvKernelFn kern = gemv_kernel_fn<WT, DUAL, T, LPR, PPL, CL>();
+    const GemvKernelFn kern = gemv_kernel_fn<WT, MODE, T, LPR, PPL, CL>();
     std::lock_guard<std::mutex> lock(mu);
     if ((int)plan.smem > configured[device]) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem) != cudaSuccess) {
@@ -704,14 +778,15 @@ int gemv_prepare(const GemvPlan& plan, int device) {
     return n;
 }
 
-template <int WT, bool DUAL, int T, int LPR, int PPL, int CL>
+template <int WT, int MODE, int T, int LPR, int PPL, int CL>
 q4q_status gemv_launch_cl(const GemvPlan& plan, int grid, const GemvArgs& a, cudaStream_t stream, bool pdl) {
     cudaLaunchAttribute attr[2];
     const cudaLaunchConfig_t cfg = gemv_config<CL>(plan, grid, stream, pdl, attr);
     GemvParams p = plan.p;
     p.bias = a.bias;
     p.act = a.act;
-    if (cudaLaunchKernelEx(&cfg, gemv_kernel_fn<WT, DUAL, T, LPR, PPL, CL>(), a.w, a.w2, a.x, a.dst, p) != cudaSuccess) {
+    if constexpr (MODE == M_GROUP) p.grp = a.grp;
+    if (cudaLaunchKernelEx(&cfg, gemv_kernel_fn<WT, MODE, T, LPR, PPL, CL>(), a.w, a.w2, a.x, a.dst, p) != cudaSuccess) {
         (void)cudaGetLastError();
         return Q4Q_ERR_CUDA;
     }
@@ -725,62 +800,62 @@ inline int cluster_grid(int n_units, int resident, int cl) {
     return std::min(want, resident / cl * cl);
 }
 
-template <int WT, bool DUAL, int T, int LPR, int PPL>
+template <int WT, int MODE, int T, int LPR, int PPL>
 q4q_status launch_gemv_t(const GemvPlan& plan, const GemvArgs& a, cudaStream_t stream, int device, bool pdl) {
     if (device < 0 || device >= 64) return Q4Q_ERR_CUDA;
     // Clusters only where they keep (nearly) every planned CTA resident.
     const int need = plan.grid - plan.grid / 16;
-    if constexpr (!DUAL) {
+    if constexpr (MODE != M_DUAL) {
         if (plan.cl >= 2) {
-            const int g = cluster_grid(plan.p.n_units, gemv_prepare<WT, DUAL, T, LPR, PPL, 2>(plan, device), 2);
-            if (g >= 2 && g >= need) return gemv_launch_cl<WT, DUAL, T, LPR, PPL, 2>(plan, g, a, stream, pdl);
+            const int g = cluster_grid(plan.p.n_units, gemv_prepare<WT, MODE, T, LPR, PPL, 2>(plan, device), 2);
+            if (g >= 2 && g >= need) return gemv_launch_cl<WT, MODE, T, LPR, PPL, 2>(plan, g, a, stream, pdl);
         }
     }
-    if (gemv_prepare<WT, DUAL, T, LPR, PPL, 1>(plan, device) <= 0) return Q4Q_ERR_CUDA;
-    return gemv_launch_cl<WT, DUAL, T, LPR, PPL, 1>(plan, plan.grid, a, stream, pdl);
+    if (gemv_prepare<WT, MODE, T, LPR, PPL, 1>(plan, device) <= 0) return Q4Q_ERR_CUDA;
+    return gemv_launch_cl<WT, MODE, T, LPR, PPL, 1>(plan, plan.grid, a, stream, pdl);
 }
 
-template <int WT, bool DUAL, int T, int LPR>
+template <int WT, int MODE, int T, int LPR>
 q4q_status launch_gemv_ppl(const GemvPlan& plan, const GemvArgs& a, cudaStream_t stream, int device, bool pdl) {
     if (T == 1) {
         switch (plan.ppl_reg) {
-            case 1: return launch_gemv_t<WT, DUAL, T, LPR, (T == 1 ? 1 : 0)>(plan, a, stream, device, pdl);
-            case 2: return launch_gemv_t<WT, DUAL, T, LPR, (T == 1 ? 2 : 0)>(plan, a, stream, device, pdl);
-            case 3: return launch_gemv_t<WT, DUAL, T, LPR, (T == 1 ? 3 : 0)>(plan, a, stream, device, pdl);
-            case 4: return launch_gemv_t<WT, DUAL, T, LPR, (T == 1 ? 4 : 0)>(plan, a, stream, device, pdl);
-            case 5: return launch_gemv_t<WT, DUAL, T, LPR, (T == 1 ? 5 : 0)>(plan, a, stream, device, pdl);
-            case 6: return launch_gemv_t<WT, DUAL, T, LPR, (T == 1 ? 6 : 0)>(plan, a, stream, device, pdl);
-            case 7: return launch_gemv_t<WT, DUAL, T, LPR, (T == 1 ? 7 : 0)>(plan, a, stream, device, pdl);
-            case 8: return launch_gemv_t<WT, DUAL, T, LPR, (T == 1 ? 8 : 0)>(plan, a, stream, device, pdl);
+            case 1: return launch_gemv_t<WT, MODE, T, LPR, (T == 1 ? 1 : 0)>(plan, a, stream, device, pdl);
+            case 2: return launch_gemv_t<WT, MODE, T, LPR, (T == 1 ? 2 : 0)>(plan, a, stream, device, pdl);
+            case 3: return launch_gemv_t<WT, MODE, T, LPR, (T == 1 ? 3 : 0)>(plan, a, stream, device, pdl);
+            case 4: return launch_gemv_t<WT, MODE, T, LPR, (T == 1 ? 4 : 0)>(plan, a, stream, device, pdl);
+            case 5: return launch_gemv_t<WT, MODE, T, LPR, (T == 1 ? 5 : 0)>(plan, a, stream, device, pdl);
+            case 6: return launch_gemv_t<WT, MODE, T, LPR, (T == 1 ? 6 : 0)>(plan, a, stream, device, pdl);
+            case 7: return launch_gemv_t<WT, MODE, T, LPR, (T == 1 ? 7 : 0)>(plan, a, stream, device, pdl);
+            case 8: return launch_gemv_t<WT, MODE, T, LPR, (T == 1 ? 8 : 0)>(plan, a, stream, device, pdl);
             default: break;
         }
     }
-    return launch_gemv_t<WT, DUAL, T, LPR, 0>(plan, a, stream, device, pdl);
+    return launch_gemv_t<WT, MODE, T, LPR, 0>(plan, a, stream, device, pdl);
 }
 
-template <int WT, bool DUAL, int T>
+template <int WT, int MODE, int T>
 q4q_status launch_gemv_lpr(const GemvPlan& plan, const GemvArgs& a, cudaStream_t stream, int device, bool pdl) {
     switch (plan.lpr) {
-        case 32: return launch_gemv_ppl<WT, DUAL, T, 32>(plan, a, stream, device, pdl);
-        case 16: return launch_gemv_ppl<WT, DUAL, T, 16>(plan, a, stream, device, pdl);
-        case 8:  return launch_gemv_ppl<WT, DUAL, T, 8>(plan, a, stream, device, pdl);
-        default: return launch_gemv_ppl<WT, DUAL, T, 4>(plan, a, stream, device, pdl);
+        case 32: return launch_gemv_ppl<WT, MODE, T, 32>(plan, a, stream, device, pdl);
+        case 16: return launch_gemv_ppl<WT, MODE, T, 16>(plan, a, stream, device, pdl);
+        case 8:  return launch_gemv_ppl<WT, MODE, T, 8>(plan, a, stream, device, pdl);
+        default: return launch_gemv_ppl<WT, MODE, T, 4>(plan, a, stream, device, pdl);
     }
 }
 
 
-// One launch of the GEMV variant <WT, DUAL> for ne11 = 1..7 tokens.
-template <int WT, bool DUAL>
+// One launch of the GEMV variant <WT, MODE> for ne11 = 1..7 tokens.
+template <int WT, int MODE>
 q4q_status launch_gemv(const GemvPlan& plan, int64_t ne11, const GemvArgs& a, cudaStream_t stream, int device,
                        bool pdl) {
     switch (ne11) {
-        case 1: return launch_gemv_lpr<WT, DUAL, 1>(plan, a, stream, device, pdl);
-        case 2: return launch_gemv_lpr<WT, DUAL, 2>(plan, a, stream, device, pdl);
-        case 3: return launch_gemv_lpr<WT, DUAL, 3>(plan, a, stream, device, pdl);
-        case 4: return launch_gemv_lpr<WT, DUAL, 4>(plan, a, stream, device, pdl);
-        case 5: return launch_gemv_lpr<WT, DUAL, 5>(plan, a, stream, device, pdl);
-        case 6: return launch_gemv_lpr<WT, DUAL, 6>(plan, a, stream, device, pdl);
-        default: return launch_gemv_lpr<WT, DUAL, 7>(plan, a, stream, device, pdl);
+        case 1: return launch_gemv_lpr<WT, MODE, 1>(plan, a, stream, device, pdl);
+        case 2: return launch_gemv_lpr<WT, MODE, 2>(plan, a, stream, device, pdl);
+        case 3: return launch_gemv_lpr<WT, MODE, 3>(plan, a, stream, device, pdl);
+        case 4: return launch_gemv_lpr<WT, MODE, 4>(plan, a, stream, device, pdl);
+        case 5: return launch_gemv_lpr<WT, MODE, 5>(plan, a, stream, device, pdl);
+        case 6: return launch_gemv_lpr<WT, MODE, 6>(plan, a, stream, device, pdl);
+        default: return launch_gemv_lpr<WT, MODE, 7>(plan, a, stream, device, pdl);
     }
 }
 

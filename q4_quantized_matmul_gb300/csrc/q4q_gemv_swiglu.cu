@@ -24,8 +24,8 @@ q4q_status gemv_mul_mat_swiglu(const void* gate, const void* up, int64_t ne00, i
     GemvPlan plan;
     if (!plan_gemv(ne00, ne01, ne11, info, &plan, Q4_0_BYTES, 2)) return Q4Q_ERR_SHAPE;
     const GemvArgs a{static_cast<const uint8_t*>(gate), static_cast<const uint8_t*>(up), src1, dst, nullptr,
-                     Q4Q_ACT_NONE};
-    return launch_gemv<WQ4_0, true>(plan, ne11, a, stream, info.device, pdl);
+                     Q4Q_ACT_NONE, GemvGroup{}};
+    return launch_gemv<WQ4_0, M_DUAL>(plan, ne11, a, stream, info.device, pdl);
 }
 
 }  // namespace q4q

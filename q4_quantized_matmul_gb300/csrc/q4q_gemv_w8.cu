@@ -15,12 +15,9 @@ namespace {
 // public Q8_0 blocks in the workspace first; one warp per output row.
 __global__ void __launch_bounds__(PLAIN_THREADS)
 generic_q8_0_q8_0_kernel(const uint8_t* __restrict__ w, const uint8_t* __restrict__ yq, float* __restrict__ dst,
-                         int nb, int ne01, int ne11, const float* __restrict__ bias, int act) {
+                         int nb, int ne01, int ne11) {
     const int lane = threadIdx.x & 31;
     const int warps = (gridDim.x * PLAIN_THREADS) >> 5;
-    GemvParams ep{};
-    ep.bias = bias;
-    ep.act = act;
     for (int row = (blockIdx.x * PLAIN_THREADS + threadIdx.x) >> 5; row < ne01; row += warps) {
         const uint8_t* wr = w + (int64_t)row * nb * Q8_0_BYTES;
         for (int t = 0; t < ne11; ++t) {
@@ -42,7 +39,7 @@ generic_q8_0_q8_0_kernel(const uint8_t* __restrict__ w, const uint8_t* __restric
             }
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-            if (lane == 0) dst[(int64_t)t * ne01 + row] = output_epilogue(acc, ep, row);
+            if (lane == 0) dst[(int64_t)t * ne01 + row] = acc;
         }
     }
 }
@@ -101,17 +98,16 @@ bool gemv_w8_supported(const void* src0, int64_t ne00, int64_t ne01, const float
 }
 
 q4q_status gemv_mul_mat_w8(const void* src0, int64_t ne00, int64_t ne01, const float* src1, int64_t ne11,
-                           float* dst, cudaStream_t stream, const DeviceInfo& info, bool pdl, const float* bias,
-                           int act) {
+                           float* dst, cudaStream_t stream, const DeviceInfo& info, bool pdl) {
     GemvPlan plan;
     if (!plan_gemv(ne00, ne01, ne11, info, &plan, Q8_0_BYTES, 1)) return Q4Q_ERR_SHAPE;
-    const GemvArgs a{static_cast<const uint8_t*>(src0), nullptr, src1, dst, bias, act};
-    return launch_gemv<WQ8_0, false>(plan, ne11, a, stream, info.device, pdl);
+    const GemvArgs a{static_cast<const uint8_t*>(src0), nullptr, src1, dst, nullptr, Q4Q_ACT_NONE, GemvGroup{}};
+    return launch_gemv<WQ8_0, M_SINGLE>(plan, ne11, a, stream, info.device, pdl);
 }
 
 q4q_status generic_mul_mat_w8(const void* src0, int64_t ne00, int64_t ne01, const float* src1, int64_t ne11,
                               float* dst, void* workspace, size_t workspace_bytes, cudaStream_t stream,
-                              const DeviceInfo& info, const float* bias, int act) {
+                              const DeviceInfo& info) {
     if (workspace_bytes < generic_workspace_bytes(ne00, ne11)) return Q4Q_ERR_WORKSPACE;
     if (!workspace) return Q4Q_ERR_NULL;
     if (!aligned(workspace, 2)) return Q4Q_ERR_ALIGN;
@@ -120,7 +116,7 @@ q4q_status generic_mul_mat_w8(const void* src0, int64_t ne00, int64_t ne01, cons
     const int grid = (int)std::min<int64_t>((ne01 + 7) / 8, (int64_t)info.sm_count * 8);
     generic_q8_0_q8_0_kernel<<<grid, PLAIN_THREADS, 0, stream>>>(static_cast<const uint8_t*>(src0),
                                                                  static_cast<const uint8_t*>(workspace), dst,
-                                                                 (int)(ne00 / QK), (int)ne01, (int)ne11, bias, act);
+                                                                 (int)(ne00 / QK), (int)ne01, (int)ne11);
     return launch_status();
 }
 

@@ -42,8 +42,13 @@ q4q_status mma_debug_isums(const void* src0, const void* src1_q8_0, int64_t ne00
 bool gemv_supported(const void* src0, int64_t ne00, int64_t ne01, const float* src1, int64_t ne11,
                     const DeviceInfo& info);
 q4q_status gemv_mul_mat(const void* src0, int64_t ne00, int64_t ne01, const float* src1, int64_t ne11,
-                        float* dst, cudaStream_t stream, const DeviceInfo& info, bool pdl,
-                        const float* bias = nullptr, int act = Q4Q_ACT_NONE);
+                        float* dst, cudaStream_t stream, const DeviceInfo& info, bool pdl);
+
+// the same GEMV with the bias / activation epilogue (q4q_gemv_epi.cu)
+unsigned int gemv_epi_take_device_status();
+q4q_status gemv_mul_mat_epi(const void* src0, int64_t ne00, int64_t ne01, const float* src1, int64_t ne11,
+                            float* dst, cudaStream_t stream, const DeviceInfo& info, bool pdl, const float* bias,
+                            int act);
 size_t generic_workspace_bytes(int64_t ne00, int64_t ne11);
 q4q_status generic_mul_mat(const void* src0, int64_t ne00, int64_t ne01, const float* src1, int64_t ne11,
                            float* dst, void* workspace, size_t workspace_bytes, cudaStream_t stream,
@@ -63,13 +68,20 @@ unsigned int gemv_w8_take_device_status();
 bool gemv_w8_supported(const void* src0, int64_t ne00, int64_t ne01, const float* src1, int64_t ne11,
                        const DeviceInfo& info);
 q4q_status gemv_mul_mat_w8(const void* src0, int64_t ne00, int64_t ne01, const float* src1, int64_t ne11,
-                           float* dst, cudaStream_t stream, const DeviceInfo& info, bool pdl, const float* bias,
-                           int act);
+                           float* dst, cudaStream_t stream, const DeviceInfo& info, bool pdl);
 q4q_status generic_mul_mat_w8(const void* src0, int64_t ne00, int64_t ne01, const float* src1, int64_t ne11,
                               float* dst, void* workspace, size_t workspace_bytes, cudaStream_t stream,
-                              const DeviceInfo& info, const float* bias, int act);
+                              const DeviceInfo& info);
 q4q_status gemv_w8_debug_isums(const void* src0, const void* src1_q8_0, int64_t ne00, int64_t ne01, int64_t ne11,
                                int32_t* out, cudaStream_t stream, const DeviceInfo& info);
+
+// several projections of one input in one launch (q4q_gemv_group.cu)
+unsigned int gemv_group_take_device_status();
+bool gemv_group_supported(int n, const void* const* src0, const int64_t* ne01, int64_t ne00, const float* src1,
+                          int64_t ne11, const DeviceInfo& info);
+q4q_status gemv_mul_mat_group(int n, const void* const* src0, const int64_t* ne01, int64_t ne00, const float* src1,
+                              int64_t ne11, float* const* dst, cudaStream_t stream, const DeviceInfo& info,
+                              bool pdl);
 
 // row gather (q4q_rows.cu)
 unsigned int rows_take_device_status();

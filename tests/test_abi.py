@@ -158,3 +158,23 @@ def test_new_bindings_fail_loudly_without_cuda_tensors(lib):
     w = torch.zeros(4 * 18 * 2, dtype=torch.uint8)
     with pytest.raises(TypeError):
         q4q.q4q_get_rows_q4_0(w, 64, 4, ids=torch.zeros(2, dtype=torch.int32))
+
+
+def test_argument_errors_of_the_group_entry(lib):
+    P = ctypes.c_void_p
+    I64 = ctypes.c_int64
+    fake = 0x1000
+    ptrs = (P * 4)(fake, fake, fake, fake)
+    rows = (I64 * 4)(4, 4, 4, 4)
+    n = ctypes.c_size_t(0)
+    assert lib.q4q_mul_mat_group(0, ptrs, rows, 64, P(fake), 64, 1, ptrs, None, 0, 0, None) == 7
+    assert lib.q4q_mul_mat_group(5, ptrs, rows, 64, P(fake), 64, 1, ptrs, None, 0, 0, None) == 7
+    assert lib.q4q_mul_mat_group(2, None, rows, 64, P(fake), 64, 1, ptrs, None, 0, 0, None) == 1
+    assert lib.q4q_mul_mat_group(2, ptrs, rows, 48, P(fake), 48, 1, ptrs, None, 0, 0, None) == 2
+    assert lib.q4q_mul_mat_group(2, ptrs, rows, 64, P(fake), 64, 1, ptrs, None, 0, 2, None) == 7
+    bad = (P * 2)(fake, fake + 1)
+    assert lib.q4q_mul_mat_group(2, bad, rows, 64, P(fake), 64, 1, ptrs, None, 0, 0, None) == 3
+    zero = (I64 * 2)(0, 0)
+    assert lib.q4q_mul_mat_group(2, ptrs, zero, 64, None, 64, 1, ptrs, None, 0, 0, None) == 0
+    assert lib.q4q_mul_mat_group_workspace_size(2, rows, 64, 3, None) == 1
+    assert lib.q4q_mul_mat_group_workspace_size(9, rows, 64, 3, ctypes.byref(n)) == 7

@@ -325,3 +325,44 @@ def test_mul_mat_q8_0_full_size_decode_set(q4q):
         _assert_close(got[:, rows], ref, scale)
         del wq_d
     assert q4q.q4q_device_status() == 0
+
+
+# ----------------------------------------------- projections of one input --
+
+GROUP_CASES = [(4096, [4096, 1024, 1024]), (768, [2304]), (768, [768, 3072, 50257]), (3072, [768, 100, 1, 37]),
+               (14336, [64, 4096]), (1024, [4099, 33])]
+
+
+@pytest.mark.parametrize("ne00,rows", GROUP_CASES)
+@pytest.mark.parametrize("ne11", [1, 3, 7, 16])
+def test_mul_mat_group(q4q, ne00, rows, ne11):
+    rng = np.random.default_rng([ne00, len(rows), ne11, 90])
+    ws = [_weights(rng, r, ne00) for r in rows]
+    x = rng.standard_normal((ne11, ne00)).astype(np.float32)
+    wqs = [q4q.q4q_quantize_q4_0(dev(w)) for w in ws]
+    outs = q4q.q4q_mul_mat_group(wqs, rows, ne00, dev(x))
+    for m, r in enumerate(rows):
+        got = outs[m].cpu().numpy()
+        # the same per-row arithmetic as a call of its own
+        np.testing.assert_array_equal(got, q4q.q4q_mul_mat(wqs[m], ne00, r, dev(x)).cpu().numpy())
+        sel = _sample_rows(r, 2048, m) if r > 2048 else np.arange(r)
+        ref, scale = oracle.mul_mat(oracle.quantize_q4_0(ws[m][sel]), ne00, sel.size, x, nthreads=8)
+        _assert_close(got[:, sel], ref, scale)
+    assert q4q.q4q_device_status() == 0
+
+
+def test_mul_mat_group_skips_empty_and_takes_misaligned(q4q):
+    rng = np.random.default_rng(91)
+    ne00 = 512
+    rows = [40, 0, 7]
+    ws = [_weights(rng, r, ne00) if r else np.zeros((0, ne00), np.float32) for r in rows]
+    x = rng.standard_normal((2, ne00)).astype(np.float32)
+    wq = [oracle.quantize_q4_0(w) for w in ws]
+    buf = torch.zeros(wq[2].size + 2, dtype=torch.uint8, device="cuda")
+    buf[2:] = dev(wq[2].reshape(-1))
+    src = [dev(wq[0]), torch.zeros(16, dtype=torch.uint8, device="cuda"), buf[2:]]
+    outs = q4q.q4q_mul_mat_group(src, rows, ne00, dev(x))
+    assert outs[1].shape == (2, 0)
+    for m in (0, 2):
+        ref, scale = oracle.mul_mat(wq[m], ne00, rows[m], x)
+        _assert_close(outs[m].cpu().numpy(), ref, scale)
