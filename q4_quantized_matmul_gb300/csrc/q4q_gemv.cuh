@@ -678,9 +678,13 @@ bool plan_gemv(int64_t ne00, int64_t ne01, int64_t ne11, const DeviceInfo& info,
         small = head + act_bytes + S * stage <= std::min<int64_t>(limit, 110 * 1024);
     }
     if (!small) {
-        // rows per unit: aim at ~32 KB stages, but keep >= 2 units per SM when the matrix allows
+        // rows per unit: aim at ~16 KB stages, but keep >= 2 units per SM when the matrix
+        // allows.  Small stages let two CTAs share an SM with >= 3 stages each (16
+        // consumer warps): K = 4096 rows of 2304 bytes stage 8 at a time, 5 stages per
+        // CTA; timed on the Llama-3-8B decode set, 32 KB stages (one CTA per SM, 6
+        // stages) were 1.5% slower.
         const int64_t rp_bytes = (int64_t)RP * urow;
-        G = RP * std::max<int64_t>(1, (32768 + rp_bytes / 2) / rp_bytes);
+        G = RP * std::max<int64_t>(1, (16384 + rp_bytes / 2) / rp_bytes);
         while (G > 8 && (ne01 + G - 1) / G < 2 * sms) G = std::max<int64_t>(8, G / 2);
         G = std::min<int64_t>(G, ne01);
         stage = ((G * urow) + 127) / 128 * 128;
