@@ -615,7 +615,8 @@ def measure_next(dev, stream):
       * get_rows: the Llama-3-8B-shaped token embedding (4096 x 128256, Q4_0): 512
         token ids, and the whole-table decode (HBM-bound);
       * q8_0_decode: the Llama-3-8B decode set with Q8_0 weights at one token
-        (q4q_mul_mat_q8_0), PDL-chained like the main workload;
+        (q4q_mul_mat_q8_0), PDL-chained like the main workload, and the same
+        weights at 512 tokens on the tensor-core path (q8_0_batched_512);
       * llama3_8b_decode_fused: the main workload's weights with q/k/v as one
         group launch and gate/up as one SwiGLU launch (5 launches per step)."""
     import torch
@@ -713,7 +714,27 @@ def measure_next(dev, stream):
                      "peak_kind": kind, "unit": "GB/s", "frac": round(alg8 / (ms_8 * 1e-3) / 1e9 / peak, 4),
                      "algorithmic_bytes_per_launch": alg8 / len(llama)},
         "note": "8 PDL-chained q4q_mul_mat_q8_0 calls per step, graph of %d steps over weight copies" % copies}
-    del sets, w8, g_8, ys
+    del sets, g_8, ys
+
+    # ---- Q8_0 weights at 512 tokens: the tensor-core GEMM with the Q8_0 dequantizer
+    ne11b = 512
+    xb = [torch.from_numpy(workloads.gen_acts("normal", ne11b, k, 3, i)).to(dev) for i, (k, n) in enumerate(llama)]
+    yb = [torch.empty((ne11b, n), dtype=torch.float32, device=dev) for _, n in llama]
+    wsb = torch.empty(max(q4q.q4q_mul_mat_q8_0_workspace_size(k, n, ne11b) for k, n in llama), dtype=torch.uint8,
+                      device=dev)
+    g_8b = _capture(stream, lambda: [q4q.q4q_mul_mat_q8_0(w8[i], k, n, xb[i], dst=yb[i], workspace=wsb)
+                                     for i, (k, n) in enumerate(llama)])
+    ms_8b = _replay_ms(stream, g_8b, 10, 1)
+    ops = sum(2.0 * k * n * ne11b for k, n in llama)
+    tops = ops / (ms_8b * 1e-3) / 1e12
+    bf16 = _measured_bf16()
+    out["q8_0_batched_512"] = {
+        "workload": "llama3_8b_decode weights as Q8_0, 512 tokens (activations N(0,1))", "kernel": "mma_gemm_kernel<128, 0, 1>",
+        "ms_per_step": round(ms_8b, 4), "int8_equiv_tops": round(tops, 1),
+        "roofline": {"bound": "tensor", "achieved": round(tops, 1), "peak": bf16[0], "peak_kind": bf16[1],
+                     "unit": "TFLOP/s", "frac": round(tops / bf16[0], 4)},
+        "note": "8 q4q_mul_mat_q8_0 calls per step (activation operands + tcgen05 GEMM), one graph"}
+    del w8, xb, yb, wsb, g_8b
 
     # ---- the Llama decode set with the fused launches: q, k, v as one group launch, o,
     #      gate and up as one SwiGLU launch, down, lm_head (5 launches instead of 8); the

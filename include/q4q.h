@@ -220,8 +220,9 @@ Q4Q_API q4q_status q4q_get_rows_q4_0(const void* src0, int64_t ne00, int64_t ne0
 Q4Q_API q4q_status q4q_get_rows_q8_0(const void* src0, int64_t ne00, int64_t ne01, const int32_t* ids,
                              int64_t n_ids, float* dst, q4q_stream_t stream);
 
-/* Bytes of device workspace q4q_mul_mat_q8_0 needs (the Q8_0 activations of the
- * generic path: ne11 * ne00/32 * 34). */
+/* Bytes of device workspace q4q_mul_mat_q8_0 needs for this problem on the current
+ * device (the tensor-core GEMM's operands for ne11 >= 8, the Q8_0 activations of
+ * the generic path otherwise; the GEMV needs none). */
 Q4Q_API q4q_status q4q_mul_mat_q8_0_workspace_size(int64_t ne00, int64_t ne01, int64_t ne11, size_t* bytes);
 
 /* ggml_mul_mat with Q8_0 weights (the Q8_0 type of "llama.cpp 深度解读" §2's type
@@ -229,20 +230,24 @@ Q4Q_API q4q_status q4q_mul_mat_q8_0_workspace_size(int64_t ne00, int64_t ne01, i
  *   dst[i11*ne01 + i01] = sum_b fp32(d_w * d_x) * isum,  isum = sum_k qw_k * qx_k,
  * src1 rows quantized to Q8_0 as q4q_quantize_q8_0 does.  src0: ne01 rows of
  * ne00/32 34-byte blocks (2-byte aligned); everything else as q4q_mul_mat_ex.
- * With ne00 % 256 == 0 and 16-byte aligned src0 / src1 every launch is the GEMV
- * (batches of more than 7 tokens run in chunks of 7, each streaming the weights:
- * there is no tensor-core path for Q8_0 weights); otherwise a generic kernel
- * over Q8_0 activations in the workspace. */
+ * With ne00 % 256 == 0 and 16-byte aligned src0 / src1: ne11 < 8 runs the GEMV,
+ * ne11 >= 8 the tensor-core GEMM of q4q_mul_mat with a Q8_0 dequantizer (256-byte
+ * aligned workspace of q4q_mul_mat_q8_0_workspace_size bytes); otherwise a generic
+ * kernel over Q8_0 activations in the workspace. */
 Q4Q_API q4q_status q4q_mul_mat_q8_0(const void* src0, int64_t ne00, int64_t ne01,
                             const float* src1, int64_t ne10, int64_t ne11,
                             float* dst, void* workspace, size_t workspace_bytes,
                             unsigned int flags, q4q_stream_t stream);
 
-/* Debug: per-block integer sums of Q8_0 weights and Q8_0 activations from the
- * Q8_0 GEMV's block-dot routine: out int32 [ne11][ne01][ne00/32].  Requires
- * ne00 % 64 == 0 and 2-byte aligned inputs.  Small shapes only (tests). */
+/* Debug: per-block integer sums of Q8_0 weights and Q8_0 activations, out int32
+ * [ne11][ne01][ne00/32], from the device routine of `path`: 0 = the Q8_0 GEMV's
+ * block dot (requires ne00 % 64 == 0, 2-byte aligned inputs; no workspace),
+ * 1 = the tensor-core GEMM with the Q8_0 dequantizer (requires ne00 % 256 == 0,
+ * a 16-byte aligned src0 and q4q_debug_workspace_size(ne00, ne11, 1) bytes of
+ * 256-byte aligned workspace).  Small shapes only (tests). */
 Q4Q_API q4q_status q4q_debug_block_isums_q8_0(const void* src0_q8_0, const void* src1_q8_0, int64_t ne00,
-                                      int64_t ne01, int64_t ne11, int32_t* out, q4q_stream_t stream);
+                                      int64_t ne01, int64_t ne11, int path, int32_t* out,
+                                      void* workspace, size_t workspace_bytes, q4q_stream_t stream);
 
 /* Size of the library-owned scratch array used by q4q_mul_mat_noalloc (per GPU). */
 #define Q4Q_NOALLOC_SCRATCH_BYTES (8u << 20)

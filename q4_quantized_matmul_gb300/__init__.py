@@ -334,14 +334,18 @@ def q4q_mul_mat_q8_0(src0: torch.Tensor, ne00: int, ne01: int, src1: torch.Tenso
 
 
 def q4q_debug_block_isums_q8_0(src0_q8_0: torch.Tensor, src1_q8_0: torch.Tensor, ne00: int, ne01: int, ne11: int,
-                               out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """int32 [ne11, ne01, ne00/32] block sums of Q8_0 weights x Q8_0 activations (GEMV routine)."""
+                               path: int = 0, out: Optional[torch.Tensor] = None,
+                               workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """int32 [ne11, ne01, ne00/32] block sums of Q8_0 weights x Q8_0 activations from the device
+    routine of `path` (0 = GEMV, 1 = tensor-core GEMM)."""
     if out is None:
         out = torch.empty((ne11, ne01, ne00 // QK), dtype=torch.int32, device=src0_q8_0.device)
+    need = q4q_debug_workspace_size(ne00, ne11, path)
+    ws_ptr, ws_bytes = _workspace(need, workspace, src0_q8_0.device)
     _check("q4q_debug_block_isums_q8_0", _lib.load().q4q_debug_block_isums_q8_0(
         _dev(src0_q8_0, "src0_q8_0", ne01 * q8_0_row_bytes(ne00)),
-        _dev(src1_q8_0, "src1_q8_0", ne11 * q8_0_row_bytes(ne00)), ne00, ne01, ne11,
-        _dev(out, "out", 4 * ne11 * ne01 * (ne00 // QK)), _stream(stream)))
+        _dev(src1_q8_0, "src1_q8_0", ne11 * q8_0_row_bytes(ne00)), ne00, ne01, ne11, int(path),
+        _dev(out, "out", 4 * ne11 * ne01 * (ne00 // QK)), ws_ptr, ws_bytes, _stream(stream)))
     return out
 
 

@@ -35,7 +35,7 @@ _SIGNATURES = {
     "q4q_get_rows_q8_0": (STATUS, [P, I64, I64, P, I64, P, P]),
     "q4q_mul_mat_q8_0_workspace_size": (STATUS, [I64, I64, I64, ctypes.POINTER(ctypes.c_size_t)]),
     "q4q_mul_mat_q8_0": (STATUS, [P, I64, I64, P, I64, I64, P, P, ctypes.c_size_t, ctypes.c_uint, P]),
-    "q4q_debug_block_isums_q8_0": (STATUS, [P, P, I64, I64, I64, P, P]),
+    "q4q_debug_block_isums_q8_0": (STATUS, [P, P, I64, I64, I64, ctypes.c_int, P, P, ctypes.c_size_t, P]),
     "q4q_mul_mat_group_workspace_size": (STATUS, [ctypes.c_int, ctypes.POINTER(I64), I64, I64,
                                                   ctypes.POINTER(ctypes.c_size_t)]),
     "q4q_mul_mat_group": (STATUS, [ctypes.c_int, ctypes.POINTER(P), ctypes.POINTER(I64), I64, P, I64, I64,

@@ -118,7 +118,13 @@ extern "C" q4q_status q4q_mul_mat_q8_0_workspace_size(int64_t ne00, int64_t ne01
     if (!bytes) return Q4Q_ERR_NULL;
     q4q_status st = check_mul_mat_shapes(ne00, ne01, ne00, ne11);
     if (st != Q4Q_OK) return st;
-    *bytes = generic_workspace_bytes(ne00, ne11);
+    size_t need = generic_workspace_bytes(ne00, ne11);
+    if (ne11 >= 8) {
+        DeviceInfo info;
+        if ((st = current_device_info(&info)) != Q4Q_OK) return st;
+        if (mma_supported(ne00, ne01, ne11, info)) need = std::max(need, mma_workspace_bytes(ne00, ne11));
+    }
+    *bytes = need;
     return Q4Q_OK;
 }
 
@@ -136,9 +142,16 @@ extern "C" q4q_status q4q_mul_mat_q8_0(const void* src0, int64_t ne00, int64_t n
     if ((st = current_device_info(&info)) != Q4Q_OK) return st;
     cudaStream_t stream = (cudaStream_t)stream_;
     const bool pdl = (flags & Q4Q_MUL_MAT_PDL) != 0;
+    if (ne11 >= 8 && mma_supported(ne00, ne01, ne11, info) && aligned(src0, 16) && aligned(src1, 16)) {
+        // the tensor-core GEMM with the Q8_0 dequantizer
+        if (workspace_bytes < mma_workspace_bytes(ne00, ne11)) return Q4Q_ERR_WORKSPACE;
+        if (!workspace) return Q4Q_ERR_NULL;
+        if (!aligned(workspace, 256)) return Q4Q_ERR_ALIGN;
+        return mma_mul_mat(src0, ne00, ne01, src1, ne11, dst, workspace, workspace_bytes, stream, info, true);
+    }
     if (gemv_w8_supported(src0, ne00, ne01, src1, std::min<int64_t>(ne11, 7), info)) {
-        // 1..7 tokens per launch; larger batches in chunks of 7 tokens (each chunk
-        // streams the weights again: there is no tensor-core path for Q8_0 weights)
+        // 1..7 tokens per launch; a batch the GEMM does not take runs in chunks of 7
+        // tokens, each streaming the weights again
         for (int64_t t0 = 0; t0 < ne11; t0 += 7) {
             const int64_t nt = std::min<int64_t>(7, ne11 - t0);
             st = gemv_mul_mat_w8(src0, ne00, ne01, src1 + t0 * ne00, nt, dst + t0 * ne01, stream, info,
@@ -151,15 +164,19 @@ extern "C" q4q_status q4q_mul_mat_q8_0(const void* src0, int64_t ne00, int64_t n
 }
 
 extern "C" q4q_status q4q_debug_block_isums_q8_0(const void* src0_q8_0, const void* src1_q8_0, int64_t ne00,
-                                                 int64_t ne01, int64_t ne11, int32_t* out, q4q_stream_t stream_) {
+                                                 int64_t ne01, int64_t ne11, int path, int32_t* out,
+                                                 void* workspace, size_t workspace_bytes, q4q_stream_t stream_) {
     q4q_status st = check_mul_mat_shapes(ne00, ne01, ne00, ne11);
     if (st != Q4Q_OK) return st;
+    if (path != 0 && path != 1) return Q4Q_ERR_ARG;
     if (ne01 == 0 || ne11 == 0) return Q4Q_OK;
     if (!src0_q8_0 || !src1_q8_0 || !out) return Q4Q_ERR_NULL;
     if (!aligned(src0_q8_0, 2) || !aligned(src1_q8_0, 2) || !aligned(out, 4)) return Q4Q_ERR_ALIGN;
     DeviceInfo info;
     if ((st = current_device_info(&info)) != Q4Q_OK) return st;
-    return gemv_w8_debug_isums(src0_q8_0, src1_q8_0, ne00, ne01, ne11, out, (cudaStream_t)stream_, info);
+    if (path == 0) return gemv_w8_debug_isums(src0_q8_0, src1_q8_0, ne00, ne01, ne11, out, (cudaStream_t)stream_, info);
+    return mma_debug_isums(src0_q8_0, src1_q8_0, ne00, ne01, ne11, out, workspace, workspace_bytes,
+                           (cudaStream_t)stream_, info, true);
 }
 
 extern "C" q4q_status q4q_mul_mat_group_workspace_size(int n, const int64_t* ne01, int64_t ne00, int64_t ne11,

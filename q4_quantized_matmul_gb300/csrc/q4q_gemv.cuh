@@ -349,10 +349,11 @@ __device__ __forceinline__ float pair_dot(const uint8_t* rowp, int pr, const Pai
     return acc;
 }
 
-// What the write of one output applies: the bias of its row, then the activation.
-__device__ __forceinline__ float output_epilogue(float v, const GemvParams& p, int row) {
-    if (p.bias) v = __fadd_rn(v, __ldg(p.bias + row));
-    if (p.act == Q4Q_ACT_GELU) v = gelu_f32(v);
+// What the write of one output applies: the bias of its row (loaded ahead by the
+// caller), then the activation.
+__device__ __forceinline__ float output_epilogue(float v, bool has_bias, float bias, int act) {
+    if (has_bias) v = __fadd_rn(v, bias);
+    if (act == Q4Q_ACT_GELU) v = gelu_f32(v);
     return v;
 }
 
@@ -498,6 +499,14 @@ __device__ __forceinline__ void gemv_body(const uint8_t* __restrict__ w, const u
     int k = 0;
     for (int u = blockIdx.x; u < p.n_units; u += grid, ++k) {
         const int s = k % p.S;
+        const UnitRows ur = unit_rows<MODE>(p, w, dst, u);
+        const int r0 = ur.r0;
+        const int nr = min(p.G, ur.rows - r0);
+        // epilogue: the bias of this lane group's first row is loaded before the wait
+        // for the weights, so its latency hides behind theirs
+        float bias_cur = 0.0f;
+        if constexpr (MODE == M_EPI)
+            if (p.bias && sl == 0 && rr < nr) bias_cur = __ldg(p.bias + r0 + rr);
         {
             const uint32_t bar = full0 + 8 * s, par = (uint32_t)((k / p.S) & 1);
             int ok = 1;
@@ -514,12 +523,12 @@ __device__ __forceinline__ void gemv_body(const uint8_t* __restrict__ w, const u
             mbar_try_wait(bar, par);       // per-lane acquire of the completed phase
         }
         const uint8_t* stage = stages + (size_t)s * p.stage_bytes;
-        const UnitRows ur = unit_rows<MODE>(p, w, dst, u);
-        const int r0 = ur.r0;
-        const int nr = min(p.G, ur.rows - r0);
         for (int pass = 0; pass < passes; ++pass) {
             const int j = rr + pass * RP;
             const bool valid = j < nr;
+            float bias_next = 0.0f;      // the next pass's bias, in flight during this pass's dot
+            if constexpr (MODE == M_EPI)
+                if (p.bias && sl == 0 && j + RP < nr) bias_next = __ldg(p.bias + r0 + j + RP);
             float acc[T], acc2[T];
 #pragma unroll
             for (int t = 0; t < T; ++t) acc[t] = acc2[t] = 0.0f;
@@ -557,11 +566,12 @@ __device__ __forceinline__ void gemv_body(const uint8_t* __restrict__ w, const u
                 for (int t = 0; t < T; ++t) {
                     float v;
                     if constexpr (DUAL) v = swiglu_f32(acc[t], acc2[t]);
-                    else if constexpr (MODE == M_EPI) v = output_epilogue(acc[t], p, r0 + j);
+                    else if constexpr (MODE == M_EPI) v = output_epilogue(acc[t], p.bias != nullptr, bias_cur, p.act);
                     else v = acc[t];
                     ur.dst[(int64_t)t * ur.rows + r0 + j] = v;
                 }
             }
+            bias_cur = bias_next;
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(empty0 + 8 * s);

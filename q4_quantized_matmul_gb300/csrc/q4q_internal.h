@@ -31,12 +31,13 @@ unsigned int mma_take_device_status();
 // tensor-core path (q4q_mma.cu)
 bool mma_supported(int64_t ne00, int64_t ne01, int64_t ne11, const DeviceInfo& info);
 size_t mma_workspace_bytes(int64_t ne00, int64_t ne11);
+// q8_weights: src0 holds Q8_0 blocks instead of Q4_0 ones
 q4q_status mma_mul_mat(const void* src0, int64_t ne00, int64_t ne01, const float* src1, int64_t ne11,
                        float* dst, void* workspace, size_t workspace_bytes, cudaStream_t stream,
-                       const DeviceInfo& info);
+                       const DeviceInfo& info, bool q8_weights = false);
 q4q_status mma_debug_isums(const void* src0, const void* src1_q8_0, int64_t ne00, int64_t ne01,
                            int64_t ne11, int32_t* out, void* workspace, size_t workspace_bytes,
-                           cudaStream_t stream, const DeviceInfo& info);
+                           cudaStream_t stream, const DeviceInfo& info, bool q8_weights = false);
 
 // GEMV path (q4q_gemv.cu)
 bool gemv_supported(const void* src0, int64_t ne00, int64_t ne01, const float* src1, int64_t ne11,

@@ -11,12 +11,13 @@
 // TMEM (tcgen05.ld), while the tensor core fills the other slab buffer.
 //
 // Warp roles (one CTA per 128-row x NT-token output tile, full K loop):
-//   warp 0      : TMA producer of raw Q4_0 bytes (2-D tensor map over the block rows,
-//                 box = 144 bytes (8 blocks, 256 K) x 128 rows) into a 3-deep ring
+//   warp 0      : TMA producer of raw weight bytes (2-D tensor map over the block rows,
+//                 box = 8 blocks (256 K; 144 bytes of Q4_0 or 272 of Q8_0) x 128 rows)
+//                 into a 3-deep ring (2-deep for Q8_0)
 //   warp 1      : TMEM allocator and the single MMA-issuing thread
 //   warp 2      : TMA producer of the activation tile (fp16, 128-byte swizzle,
 //                 box = 64 K x NT tokens) into a 4-deep ring
-//   warps 4-7   : dequantizers: raw Q4_0 -> fp16 A tile (128 rows x 64 K) in the
+//   warps 4-7   : dequantizers: raw Q4_0 / Q8_0 -> fp16 A tile (128 rows x 64 K) in the
 //                 canonical K-major 128-byte-swizzle layout, plus the fp32 block scales
 //   warps 8..   : epilogue, NT/32 warps per TMEM lane quadrant: per 32-K slab each warp
 //                 loads its 32 columns with one tcgen05.ld and applies acc += d_w d_x S
@@ -40,10 +41,18 @@ namespace {
 __device__ unsigned int g_mma_status = 0;
 
 constexpr int BM = 128;                 // weight rows per CTA tile (MMA M)
-constexpr int KRAW = 256;               // K per raw-weight stage (8 blocks = 144 bytes per row)
+constexpr int KRAW = 256;               // K per raw-weight stage (8 blocks per row)
 constexpr int KAB = 64;                 // K per A/B stage (2 blocks, one 128-byte swizzle row)
-constexpr int RAW_BYTES = BM * 144;     // 18432
 constexpr int A_BYTES = BM * KAB * 2;   // 16384
+constexpr int WQ4_0 = 0;                // weight block types
+constexpr int WQ8_0 = 1;
+
+// Bytes of one raw-stage row: 8 blocks of 18 (Q4_0) or 34 (Q8_0) bytes, a multiple
+// of 16 either way (the TMA box's inner extent).
+__host__ __device__ constexpr int raw_row_bytes(int wt) { return wt == WQ8_0 ? 8 * 34 : 8 * 18; }
+// Bytes per element of the weight tensor map: a box dimension holds at most 256
+// elements, so the 272-byte Q8_0 rows are mapped as 136 two-byte elements.
+__host__ __device__ constexpr int raw_elem_bytes(int wt) { return wt == WQ8_0 ? 2 : 1; }
 constexpr int NPAD = 128;               // activation-scale rows are padded to this
 
 // ------------------------------------------------------------------ PTX ----
@@ -185,6 +194,28 @@ __device__ __forceinline__ uint4 nibbles_to_f16x8(uint32_t q) {
     return out;
 }
 
+// Two words of Q8_0 codes (elements e0..e3, e4..e7) -> 8 fp16 values in the same
+// order [e0, e4, e1, e5, e2, e6, e3, e7]: a byte permute puts e_k and e_{k+4} in
+// the low bytes of the two halves, flipping their sign bits makes them e + 128,
+// 0x64 in the high bytes makes the fp16 1024 + (e + 128), and subtracting 1152 is
+// exact.
+__device__ __forceinline__ uint4 codes_to_f16x8(uint32_t lo, uint32_t hi) {
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));   // 1152
+    uint32_t h[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t sel = (uint32_t)(k | (k << 4) | ((4 + k) << 8) | ((4 + k) << 12));
+        h[k] = (__byte_perm(lo, hi, sel) & 0x00FF00FFu) ^ 0x64806480u;
+    }
+    uint4 out;
+    __half2 r;
+    r = __hsub2(*reinterpret_cast<__half2*>(&h[0]), bias); out.x = *reinterpret_cast<uint32_t*>(&r);
+    r = __hsub2(*reinterpret_cast<__half2*>(&h[1]), bias); out.y = *reinterpret_cast<uint32_t*>(&r);
+    r = __hsub2(*reinterpret_cast<__half2*>(&h[2]), bias); out.z = *reinterpret_cast<uint32_t*>(&r);
+    r = __hsub2(*reinterpret_cast<__half2*>(&h[3]), bias); out.w = *reinterpret_cast<uint32_t*>(&r);
+    return out;
+}
+
 // position p of an 8-element group holds element PERM[p]
 __host__ __device__ constexpr int perm8(int p) { return (p & 1) ? 4 + (p >> 1) : (p >> 1); }
 
@@ -218,7 +249,7 @@ __device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
     return d;
 }
 
-template <int NT>
+template <int NT, int WT>
 struct Cfg {
     // epilogue warps: NT/32 per TMEM lane quadrant (each owns 32 columns), at least one
     static constexpr int EPI_WARPS = NT >= 128 ? 16 : (NT >= 64 ? 8 : 4);
@@ -226,7 +257,10 @@ struct Cfg {
     // latency of its per-block hand-offs: with shallower rings two CTAs fit on an
     // SM (shared memory, registers, TMEM) and their chains overlap.
     static constexpr int MIN_BLOCKS = NT <= 32 ? 2 : 1;
-    static constexpr int RAW_STAGES = NT <= 32 ? 2 : 3;
+    // Q8_0 raw stages are 34816 bytes: two of them keep the widest tile in 227 KB
+    static constexpr int RAW_STAGES = (NT <= 32 || WT == WQ8_0) ? 2 : 3;
+    static constexpr int RAW_ROW = raw_row_bytes(WT);
+    static constexpr int RAW_BYTES = BM * RAW_ROW;
     static constexpr int AB_STAGES = NT <= 32 ? 3 : 4;
     // Narrow tiles are bound by the single MMA-issuing thread: it hands TMEM over in
     // slab pairs (one check and one commit per A/B stage).  The widest tile is bound
@@ -251,11 +285,14 @@ struct Cfg {
     static constexpr int SMEM = OFF_MISC + 64 + 1024;                                // + alignment slack
 };
 
-template <int NT, bool DEBUG>
-__global__ void __launch_bounds__(Cfg<NT>::THREADS, Cfg<NT>::MIN_BLOCKS)
-mma_q4_0_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_b,
+// WT: the weight block type (WQ4_0 or WQ8_0); only the raw stage and the
+// dequantizers differ.
+template <int NT, bool DEBUG, int WT>
+__global__ void __launch_bounds__(Cfg<NT, WT>::THREADS, Cfg<NT, WT>::MIN_BLOCKS)
+mma_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_b,
                 const MmaParams p) {
-    using C = Cfg<NT>;
+    using C = Cfg<NT, WT>;
+    constexpr int RAW_BYTES = C::RAW_BYTES;
     constexpr int NBUF = C::NBUF;
     constexpr int RAW_STAGES = C::RAW_STAGES;
     constexpr int AB_STAGES = C::AB_STAGES;
@@ -316,7 +353,8 @@ mma_q4_0_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                 const int st = r % RAW_STAGES;
                 if (r >= RAW_STAGES && !wait_or_abort(raw_empty + 8 * st, ((r / RAW_STAGES) + 1) & 1, abort_flag)) break;
                 mbar_arrive_expect_tx(raw_full + 8 * st, RAW_BYTES);
-                tma_load_2d(sbase + C::OFF_RAW + st * RAW_BYTES, &tmap_w, r * 144, m0, raw_full + 8 * st);
+                tma_load_2d(sbase + C::OFF_RAW + st * RAW_BYTES, &tmap_w, r * (C::RAW_ROW / raw_elem_bytes(WT)), m0,
+                            raw_full + 8 * st);
             }
             if (*abort_flag)   // let the loads already issued land before the CTA exits
                 for (int r2 = max(0, r - RAW_STAGES); r2 < r; ++r2)
@@ -417,7 +455,7 @@ mma_q4_0_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
         for (int r = 0; r < n_raw && ok; ++r) {
             const int st = r % RAW_STAGES;
             if (!warp_wait(raw_full + 8 * st, (r / RAW_STAGES) & 1, abort_flag, lane)) { ok = false; break; }
-            const uint4* rowp = reinterpret_cast<const uint4*>(smem + C::OFF_RAW + st * RAW_BYTES + t * 144);
+            const uint4* rowp = reinterpret_cast<const uint4*>(smem + C::OFF_RAW + st * RAW_BYTES + t * C::RAW_ROW);
 #pragma unroll
             for (int a = 0; a < KRAW / KAB; ++a) {
                 const int i = r * (KRAW / KAB) + a;
@@ -426,27 +464,50 @@ mma_q4_0_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                     ok = false;
                     break;
                 }
-                // pair a = blocks 2a, 2a+1 = words 9a .. 9a+8 of the row, inside the three
-                // 16-byte chunks (9a)/4 .. (9a)/4 + 2 (16-byte loads keep the eight lanes
-                // of each load phase on distinct banks: the row pitch is 144 bytes)
-                uint32_t wv[12];
-#pragma unroll
-                for (int k = 0; k < 3; ++k) {
-                    const uint4 v4 = rowp[(9 * a) / 4 + k];
-                    wv[4 * k + 0] = v4.x; wv[4 * k + 1] = v4.y; wv[4 * k + 2] = v4.z; wv[4 * k + 3] = v4.w;
-                }
-                const int w0 = (9 * a) % 4;                  // first word of the pair (compile time)
-                uint32_t q[8];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) q[k] = __byte_perm(wv[w0 + k], wv[w0 + k + 1], 0x5432);   // block 2a
-#pragma unroll
-                for (int k = 0; k < 4; ++k) q[4 + k] = wv[w0 + 5 + k];                              // block 2a+1
                 uint8_t* atile = smem + C::OFF_A + s * A_BYTES + (t >> 3) * 1024 + rsw * 128;
+                if constexpr (WT == WQ4_0) {
+                    // pair a = blocks 2a, 2a+1 = words 9a .. 9a+8 of the row, inside the three
+                    // 16-byte chunks (9a)/4 .. (9a)/4 + 2 (16-byte loads keep the eight lanes
+                    // of each load phase on distinct banks: the row pitch is 144 bytes)
+                    uint32_t wv[12];
 #pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    *reinterpret_cast<uint4*>(atile + ((c ^ rsw) << 4)) = nibbles_to_f16x8(q[c]);
-                dw_s[(s * 2 + 0) * BM + t] = fp16_to_f32(wv[w0]);
-                dw_s[(s * 2 + 1) * BM + t] = fp16_to_f32(wv[w0 + 4] >> 16);
+                    for (int k = 0; k < 3; ++k) {
+                        const uint4 v4 = rowp[(9 * a) / 4 + k];
+                        wv[4 * k + 0] = v4.x; wv[4 * k + 1] = v4.y; wv[4 * k + 2] = v4.z; wv[4 * k + 3] = v4.w;
+                    }
+                    const int w0 = (9 * a) % 4;                  // first word of the pair (compile time)
+                    uint32_t q[8];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) q[k] = __byte_perm(wv[w0 + k], wv[w0 + k + 1], 0x5432);   // block 2a
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) q[4 + k] = wv[w0 + 5 + k];                              // block 2a+1
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4*>(atile + ((c ^ rsw) << 4)) = nibbles_to_f16x8(q[c]);
+                    dw_s[(s * 2 + 0) * BM + t] = fp16_to_f32(wv[w0]);
+                    dw_s[(s * 2 + 1) * BM + t] = fp16_to_f32(wv[w0 + 4] >> 16);
+                } else {
+                    // pair a = blocks 2a, 2a+1 = words 17a .. 17a+16 of the row, inside the five
+                    // 16-byte chunks (17a)/4 .. (17a)/4 + 4 (row pitch 272 bytes = 17 chunks:
+                    // the eight lanes of a load phase hit distinct banks)
+                    uint32_t wv[20];
+#pragma unroll
+                    for (int k = 0; k < 5; ++k) {
+                        const uint4 v4 = rowp[(17 * a) / 4 + k];
+                        wv[4 * k + 0] = v4.x; wv[4 * k + 1] = v4.y; wv[4 * k + 2] = v4.z; wv[4 * k + 3] = v4.w;
+                    }
+                    const int w0 = (17 * a) % 4;                 // first word of the pair (compile time)
+                    uint32_t q[16];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) q[k] = __byte_perm(wv[w0 + k], wv[w0 + k + 1], 0x5432);   // block 2a
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) q[8 + k] = wv[w0 + 9 + k];                              // block 2a+1
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4*>(atile + ((c ^ rsw) << 4)) = codes_to_f16x8(q[2 * c], q[2 * c + 1]);
+                    dw_s[(s * 2 + 0) * BM + t] = fp16_to_f32(wv[w0]);
+                    dw_s[(s * 2 + 1) * BM + t] = fp16_to_f32(wv[w0 + 8] >> 16);
+                }
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(ab_full + 8 * s);
@@ -679,12 +740,12 @@ int64_t npad_of(int64_t N) { return (N + NPAD - 1) / NPAD * NPAD; }
 
 size_t b_bytes_of(int64_t K, int64_t N) { return ((size_t)N * K * 2 + 255) / 256 * 256; }
 
-template <int NT, bool DEBUG>
+template <int NT, bool DEBUG, int WT>
 q4q_status launch_mma_t(const CUtensorMap& tw, const CUtensorMap& tb, const MmaParams& p, cudaStream_t stream,
                         int device) {
-    using C = Cfg<NT>;
+    using C = Cfg<NT, WT>;
     static std::atomic<int> configured[64];
-    auto kern = mma_q4_0_kernel<NT, DEBUG>;
+    auto kern = mma_gemm_kernel<NT, DEBUG, WT>;
     if (device < 0 || device >= 64) return Q4Q_ERR_CUDA;
     if (!configured[device].load()) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
@@ -696,18 +757,21 @@ q4q_status launch_mma_t(const CUtensorMap& tw, const CUtensorMap& tb, const MmaP
     return launch_status();
 }
 
-template <bool DEBUG>
+template <bool DEBUG, int WT>
 q4q_status run_mma(const void* src0, int64_t ne00, int64_t ne01, int64_t ne11, const __half* bmat, const float* dx,
                    float* dst, int32_t* isums, cudaStream_t stream, const DeviceInfo& info) {
     if (!get_encode()) return Q4Q_ERR_CUDA;
     const int NT = pick_nt(ne11);
+    const int64_t row_bytes = ne00 / QK * (WT == WQ8_0 ? Q8_0_BYTES : Q4_0_BYTES);
     CUtensorMap tw, tb;
     {
-        const cuuint64_t dims[2] = {(cuuint64_t)(ne00 / QK * Q4_0_BYTES), (cuuint64_t)ne01};
-        const cuuint64_t strides[1] = {(cuuint64_t)(ne00 / QK * Q4_0_BYTES)};
-        const cuuint32_t box[2] = {144, BM};
+        const int eb = raw_elem_bytes(WT);
+        const cuuint64_t dims[2] = {(cuuint64_t)(row_bytes / eb), (cuuint64_t)ne01};
+        const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+        const cuuint32_t box[2] = {(cuuint32_t)(raw_row_bytes(WT) / eb), BM};
         const cuuint32_t estr[2] = {1, 1};
-        if (g_encode(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(src0), dims, strides, box, estr,
+        const CUtensorMapDataType dt = eb == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+        if (g_encode(&tw, dt, 2, const_cast<void*>(src0), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return Q4Q_ERR_CUDA;
@@ -732,10 +796,10 @@ q4q_status run_mma(const void* src0, int64_t ne00, int64_t ne01, int64_t ne11, c
     p.dx = dx;
     p.isums = isums;
     switch (NT) {
-        case 16: return launch_mma_t<16, DEBUG>(tw, tb, p, stream, info.device);
-        case 32: return launch_mma_t<32, DEBUG>(tw, tb, p, stream, info.device);
-        case 64: return launch_mma_t<64, DEBUG>(tw, tb, p, stream, info.device);
-        default: return launch_mma_t<128, DEBUG>(tw, tb, p, stream, info.device);
+        case 16: return launch_mma_t<16, DEBUG, WT>(tw, tb, p, stream, info.device);
+        case 32: return launch_mma_t<32, DEBUG, WT>(tw, tb, p, stream, info.device);
+        case 64: return launch_mma_t<64, DEBUG, WT>(tw, tb, p, stream, info.device);
+        default: return launch_mma_t<128, DEBUG, WT>(tw, tb, p, stream, info.device);
     }
 }
 
@@ -752,7 +816,7 @@ bool mma_supported(int64_t ne00, int64_t ne01, int64_t ne11, const DeviceInfo& i
     if (info.cc_major != 10) return false;
     if (ne00 < KRAW || ne00 % KRAW != 0 || ne01 <= 0 || ne11 <= 0 || ne11 >= (1 << 20)) return false;
     if (ne01 >= (1ll << 31) || ne00 >= (1 << 20)) return false;
-    return Cfg<128>::SMEM <= info.max_smem_optin && get_encode();
+    return std::max(Cfg<128, WQ4_0>::SMEM, Cfg<128, WQ8_0>::SMEM) <= info.max_smem_optin && get_encode();
 }
 
 size_t mma_workspace_bytes(int64_t ne00, int64_t ne11) {
@@ -760,7 +824,8 @@ size_t mma_workspace_bytes(int64_t ne00, int64_t ne11) {
 }
 
 q4q_status mma_mul_mat(const void* src0, int64_t ne00, int64_t ne01, const float* src1, int64_t ne11, float* dst,
-                       void* workspace, size_t workspace_bytes, cudaStream_t stream, const DeviceInfo& info) {
+                       void* workspace, size_t workspace_bytes, cudaStream_t stream, const DeviceInfo& info,
+                       bool q8_weights) {
     if (workspace_bytes < mma_workspace_bytes(ne00, ne11)) return Q4Q_ERR_WORKSPACE;
     __half* bmat = static_cast<__half*>(workspace);
     float* dx = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + b_bytes_of(ne00, ne11));
@@ -769,14 +834,15 @@ q4q_status mma_mul_mat(const void* src0, int64_t ne00, int64_t ne01, const float
     act_to_mma_kernel<<<grid, 256, 0, stream>>>(src1, bmat, dx, (int)ne00, (int)ne11, (int)npad_of(ne11));
     q4q_status st = launch_status();
     if (st != Q4Q_OK) return st;
-    return run_mma<false>(src0, ne00, ne01, ne11, bmat, dx, dst, nullptr, stream, info);
+    return q8_weights ? run_mma<false, WQ8_0>(src0, ne00, ne01, ne11, bmat, dx, dst, nullptr, stream, info)
+                      : run_mma<false, WQ4_0>(src0, ne00, ne01, ne11, bmat, dx, dst, nullptr, stream, info);
 }
 
 size_t mma_debug_workspace_bytes(int64_t ne00, int64_t ne11) { return mma_workspace_bytes(ne00, ne11); }
 
 q4q_status mma_debug_isums(const void* src0, const void* src1_q8_0, int64_t ne00, int64_t ne01, int64_t ne11,
                            int32_t* out, void* workspace, size_t workspace_bytes, cudaStream_t stream,
-                           const DeviceInfo& info) {
+                           const DeviceInfo& info, bool q8_weights) {
     if (!mma_supported(ne00, ne01, std::max<int64_t>(ne11, 8), info)) return Q4Q_ERR_SHAPE;
     if (!aligned(src0, 16)) return Q4Q_ERR_ALIGN;
     if (workspace_bytes < mma_workspace_bytes(ne00, ne11)) return Q4Q_ERR_WORKSPACE;
@@ -790,7 +856,8 @@ q4q_status mma_debug_isums(const void* src0, const void* src1_q8_0, int64_t ne00
                                                (int)ne11, (int)npad_of(ne11));
     q4q_status st = launch_status();
     if (st != Q4Q_OK) return st;
-    return run_mma<true>(src0, ne00, ne01, ne11, bmat, dx, nullptr, out, stream, info);
+    return q8_weights ? run_mma<true, WQ8_0>(src0, ne00, ne01, ne11, bmat, dx, nullptr, out, stream, info)
+                      : run_mma<true, WQ4_0>(src0, ne00, ne01, ne11, bmat, dx, nullptr, out, stream, info);
 }
 
 }  // namespace q4q

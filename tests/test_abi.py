@@ -148,8 +148,9 @@ def test_argument_errors_of_the_entry_points_next_to_the_matmul(lib):
     assert lib.q4q_mul_mat_q8_0(None, 64, 0, None, 64, 1, None, None, 0, 0, None) == 0
     assert lib.q4q_mul_mat_q8_0_workspace_size(64, 4, 3, ctypes.byref(n)) == 0
     assert n.value == 3 * 2 * 34
-    assert lib.q4q_debug_block_isums_q8_0(fake, fake, 48, 2, 1, fake, None) == 2
-    assert lib.q4q_debug_block_isums_q8_0(fake, None, 64, 2, 1, fake, None) == 1
+    assert lib.q4q_debug_block_isums_q8_0(fake, fake, 48, 2, 1, 0, fake, None, 0, None) == 2
+    assert lib.q4q_debug_block_isums_q8_0(fake, None, 64, 2, 1, 0, fake, None, 0, None) == 1
+    assert lib.q4q_debug_block_isums_q8_0(fake, fake, 64, 2, 1, 3, fake, None, 0, None) == 7
 
 
 def test_new_bindings_fail_loudly_without_cuda_tensors(lib):

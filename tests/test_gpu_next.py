@@ -239,15 +239,20 @@ def _assert_close(got, ref, scale):
     assert np.all(np.asarray(got)[scale == 0] == 0)
 
 
-@pytest.mark.parametrize("ne00,ne01,ne11", [(64, 1, 1), (256, 5, 3), (768, 37, 2), (4096, 9, 1), (320, 4, 4)])
-def test_block_isums_w8_routine(q4q, ne00, ne01, ne11):
+@pytest.mark.parametrize("ne00,ne01,ne11,path", [(64, 1, 1, 0), (256, 5, 3, 0), (768, 37, 2, 0), (4096, 9, 1, 0),
+                                                 (320, 4, 4, 0), (256, 5, 3, 1), (512, 130, 9, 1), (4096, 64, 40, 1),
+                                                 (768, 37, 130, 1), (1024, 200, 17, 1)])
+def test_block_isums_w8_routine(q4q, ne00, ne01, ne11, path):
+    # path 0: the GEMV's block dot; path 1: the tensor-core GEMM with the Q8_0
+    # dequantizer (one 32-wide K block per fresh TMEM accumulator, read back exactly)
     rng = np.random.default_rng([ne00, ne01, ne11, 70])
     w = _weights(rng, ne01, ne00, scale=1.0)
     x = rng.standard_normal((ne11, ne00)).astype(np.float32)
     x[:, ::7] *= 30
     wq, xq = oracle.quantize_q8_0(w), oracle.quantize_q8_0(x)
-    got = q4q.q4q_debug_block_isums_q8_0(dev(wq), dev(xq), ne00, ne01, ne11).cpu().numpy()
+    got = q4q.q4q_debug_block_isums_q8_0(dev(wq), dev(xq), ne00, ne01, ne11, path=path).cpu().numpy()
     np.testing.assert_array_equal(got, oracle.block_isums_w8(wq, xq, ne00, ne01, ne11))
+    assert q4q.q4q_device_status() == 0
 
 
 def test_block_isums_w8_extremes(q4q):
@@ -262,6 +267,10 @@ def test_block_isums_w8_extremes(q4q):
     assert ref[0, 0, 0] == 32 * 127 * 127 and ref[1, 0, 0] == -32 * 127 * 127
     got = q4q.q4q_debug_block_isums_q8_0(dev(wq), dev(xq), ne00, ne01, ne11).cpu().numpy()
     np.testing.assert_array_equal(got, ref)
+    # the same extremes through the tensor-core routine (K = 256: four copies of the pair)
+    wq4, xq4 = np.tile(wq, (1, 4)), np.tile(xq, (1, 4))
+    got = q4q.q4q_debug_block_isums_q8_0(dev(wq4), dev(xq4), 256, ne01, ne11, path=1).cpu().numpy()
+    np.testing.assert_array_equal(got, oracle.block_isums_w8(wq4, xq4, 256, ne01, ne11))
 
 
 W8_SHAPES = [(256, 1), (256, 3), (768, 2304), (3072, 768), (4096, 1024), (14336, 64), (512, 33), (1024, 4099),
@@ -282,7 +291,8 @@ def test_mul_mat_q8_0_gemv(q4q, ne00, ne01, ne11):
 
 
 @pytest.mark.parametrize("ne00,ne01,ne11", [(1024, 300, 8), (768, 130, 15), (4096, 64, 64), (96, 17, 3),
-                                            (800, 65, 9), (32, 3, 1)])
+                                            (800, 65, 9), (32, 3, 1), (512, 130, 9), (4096, 257, 129),
+                                            (1024, 64, 200), (14336, 256, 512), (768, 37, 130)])
 def test_mul_mat_q8_0_batches_and_generic(q4q, ne00, ne01, ne11):
     rng = np.random.default_rng([ne00, ne01, ne11, 72])
     w = _weights(rng, ne01, ne00)
@@ -366,3 +376,22 @@ def test_mul_mat_group_skips_empty_and_takes_misaligned(q4q):
     for m in (0, 2):
         ref, scale = oracle.mul_mat(wq[m], ne00, rows[m], x)
         _assert_close(outs[m].cpu().numpy(), ref, scale)
+
+
+@pytest.mark.parametrize("ne11", [8, 64, 512])
+def test_mul_mat_q8_0_full_size_batched(q4q, ne11):
+    """The tensor-core path with Q8_0 weights at full size: the Llama-3-8B-shaped
+    lm_head (4096 -> 128256) and down (14336 -> 4096) projections, outputs on up to
+    1024 sampled rows (plus the first and last) for every token."""
+    for i in (7, 6):
+        ne00, ne01 = workloads.WORKLOADS["llama3_8b_batched"].shapes[i]
+        w, x = workloads.problem("llama3_8b_batched", i, ne11)
+        wq_d = q4q.q4q_quantize_q8_0(dev(w))
+        got = q4q.q4q_mul_mat_q8_0(wq_d, ne00, ne01, dev(x)).cpu().numpy()
+        rows = _sample_rows(ne01, 1024, 200 + i)
+        wq_rows = wq_d.view(ne01, -1)[torch.from_numpy(rows).cuda()].cpu().numpy()
+        np.testing.assert_array_equal(wq_rows, oracle.quantize_q8_0(w[rows]))
+        ref, scale = oracle.mul_mat_w8(wq_rows, ne00, rows.size, x, nthreads=16)
+        _assert_close(got[:, rows], ref, scale)
+        del wq_d
+    assert q4q.q4q_device_status() == 0
