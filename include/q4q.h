@@ -148,7 +148,9 @@ Q4Q_API q4q_status q4q_mul_mat_ex(const void* src0, int64_t ne00, int64_t ne01,
  * with mul_mat exactly as q4q_mul_mat computes it.  bias: device fp32 [ne01]
  * (4-byte aligned) or NULL for none; act: Q4Q_ACT_NONE or Q4Q_ACT_GELU, else
  * Q4Q_ERR_ARG.  Everything else (arguments, workspace, flags, limits, errors)
- * as q4q_mul_mat_ex.  For ne11 < 8 the epilogue runs inside the GEMV (one launch);
+ * as q4q_mul_mat_ex; under Q4Q_MUL_MAT_PDL the bias, like src0, may be read before
+ * the work queued ahead of the call completes, so no work still in flight on the
+ * stream may write it (true for a model's resident biases).  For ne11 < 8 the epilogue runs inside the GEMV (one launch);
  * other paths apply it with one elementwise kernel over dst after the matmul. */
 Q4Q_API q4q_status q4q_mul_mat_bias_act(const void* src0, int64_t ne00, int64_t ne01,
                                 const float* src1, int64_t ne10, int64_t ne11,

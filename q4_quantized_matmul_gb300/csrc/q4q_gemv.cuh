@@ -452,6 +452,26 @@ __device__ __forceinline__ void gemv_body(const uint8_t* __restrict__ w, const u
     }
 
     // ---------------- consumers: activations first (they may come from the previous kernel)
+    constexpr int RP = CONSUMERS / LPR;     // rows processed side by side
+    const int rr = tid / LPR, sl = tid % LPR;
+    // epilogue: the biases of the first two units' first rows are loaded before the
+    // wait for the previous kernel, like the weights (resident model parameters), so
+    // that small matrices, whose weights are in shared memory by then, do not wait
+    // for them after the dot
+    float bias_pre0 = 0.0f, bias_pre1 = 0.0f;
+    if constexpr (MODE == M_EPI) {
+        if (p.bias && sl == 0) {
+            const int u0 = blockIdx.x, u1 = blockIdx.x + grid;
+            if (u0 < p.n_units) {
+                const UnitRows a = unit_rows<MODE>(p, w, dst, u0);
+                if (rr < min(p.G, a.rows - a.r0)) bias_pre0 = __ldg(p.bias + a.r0 + rr);
+            }
+            if (u1 < p.n_units) {
+                const UnitRows b = unit_rows<MODE>(p, w, dst, u1);
+                if (rr < min(p.G, b.rows - b.r0)) bias_pre1 = __ldg(p.bias + b.r0 + rr);
+            }
+        }
+    }
     pdl_wait();
     {
         // this CTA's share: blocks [f0, f1) of the T * nb blocks (token-major)
@@ -485,8 +505,6 @@ __device__ __forceinline__ void gemv_body(const uint8_t* __restrict__ w, const u
         consumer_sync();
     }
 
-    constexpr int RP = CONSUMERS / LPR;     // rows processed side by side
-    const int rr = tid / LPR, sl = tid % LPR;
     const int passes = (p.G + RP - 1) / RP;
     PairActs areg[PPL > 0 ? PPL : 1];
     if (PPL > 0) {
@@ -502,11 +520,14 @@ __device__ __forceinline__ void gemv_body(const uint8_t* __restrict__ w, const u
         const UnitRows ur = unit_rows<MODE>(p, w, dst, u);
         const int r0 = ur.r0;
         const int nr = min(p.G, ur.rows - r0);
-        // epilogue: the bias of this lane group's first row is loaded before the wait
-        // for the weights, so its latency hides behind theirs
+        // epilogue: the bias of this lane group's first row (loaded ahead for the first
+        // two units, else before the wait for the weights, so its latency hides behind theirs)
         float bias_cur = 0.0f;
-        if constexpr (MODE == M_EPI)
-            if (p.bias && sl == 0 && rr < nr) bias_cur = __ldg(p.bias + r0 + rr);
+        if constexpr (MODE == M_EPI) {
+            if (k == 0) bias_cur = bias_pre0;
+            else if (k == 1) bias_cur = bias_pre1;
+            else if (p.bias && sl == 0 && rr < nr) bias_cur = __ldg(p.bias + r0 + rr);
+        }
         {
             const uint32_t bar = full0 + 8 * s, par = (uint32_t)((k / p.S) & 1);
             int ok = 1;
@@ -697,10 +718,21 @@ bool plan_gemv(int64_t ne00, int64_t ne01, int64_t ne11, const DeviceInfo& info,
         G = RP * std::max<int64_t>(1, (16384 + rp_bytes / 2) / rp_bytes);
         while (G > 8 && (ne01 + G - 1) / G < 2 * sms) G = std::max<int64_t>(8, G / 2);
         G = std::min<int64_t>(G, ne01);
-        stage = ((G * urow) + 127) / 128 * 128;
-        S = 0;
-        if (two_per_sm) S = (std::min<int64_t>(limit, 110 * 1024) - head - act_bytes) / stage;
-        if (S < 3) S = (limit - head - act_bytes) / stage;
+        const auto stages_for = [&](int64_t g) {
+            stage = ((g * urow) + 127) / 128 * 128;
+            int64_t n = 0;
+            if (two_per_sm) n = (std::min<int64_t>(limit, 110 * 1024) - head - act_bytes) / stage;
+            if (n < 3) n = (limit - head - act_bytes) / stage;
+            return n;
+        };
+        S = stages_for(G);
+        // Very long rows (a Q8_0 row of K = 14336 is 15 KB) or many tokens' activations
+        // leave room for fewer than two stages of RP rows: stage fewer rows (the row
+        // groups past G stay idle) rather than give the GEMV up.
+        while (S < 2 && G > 1) {
+            G = std::max<int64_t>(1, G / 2);
+            S = stages_for(G);
+        }
         if (S < 2) return false;
         S = std::min<int64_t>(S, MAX_STAGES);
     }
