@@ -796,13 +796,19 @@ def measure_next(dev, stream):
                                                              dst=ds[i], workspace=ws, flags=PDL)
                                     for c in range(copies) for i, (k, n) in enumerate(shapes)])
     ms_b = _replay_ms(stream, g_b, 50, copies)
+    # the same calls without the epilogue, in the same graph structure
+    g_p = _capture(stream, lambda: [q4q.q4q_mul_mat(wsets[c][i], k, n, gx[i], dst=ds[i], workspace=ws, flags=PDL)
+                                    for c in range(copies) for i, (k, n) in enumerate(shapes)])
+    ms_p = _replay_ms(stream, g_p, 50, copies)
     out["gpt2_bias_gelu"] = {
         "workload": "gpt2_decode_step with bias on 48 projections and GELU on the 12 c_mlp_fc",
-        "kernel": "gemv_q4_0_kernel (bias / GELU in the output write)",
+        "kernel": "gemv_q4_0_epi_kernel (bias / GELU in the output write)",
         "ms_per_step": round(ms_b, 5), "weight_gb_s": round(wbg / (ms_b * 1e-3) / 1e9, 1),
         "us_per_matrix": round(ms_b * 1e3 / len(shapes), 3),
-        "note": "49 PDL-chained q4q_mul_mat_bias_act calls per step; compare secondary_decode (no epilogue)"}
-    del wsets, wq, gx, bs, ds, g_b
+        "plain_us_per_matrix": round(ms_p * 1e3 / len(shapes), 3),
+        "note": "49 PDL-chained q4q_mul_mat_bias_act calls per step, graph of %d steps over weight copies; "
+                "plain = the same calls as q4q_mul_mat (no bias, no GELU) in the same graphs" % copies}
+    del wsets, wq, gx, bs, ds, g_b, g_p
     torch.cuda.empty_cache()
     return out
 
