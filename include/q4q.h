@@ -93,9 +93,12 @@ Q4Q_API q4q_status q4q_quantize_q4_0(const float* src, void* dst, int64_t ncols,
 Q4Q_API q4q_status q4q_quantize_q8_0(const float* src, void* dst, int64_t ncols, int64_t nrows,
                              q4q_stream_t stream);
 
-/* Bytes of device workspace q4q_mul_mat needs for this problem (0 when the
- * chosen kernel needs none).  The answer depends only on the shapes and on
- * the current device; it never exceeds ne11 * (2 * ne00 + 4 * ne00 / 32) + 4096. */
+/* Bytes of device workspace q4q_mul_mat wants for this problem (0 when the
+ * chosen kernel needs none).  The answer depends only on the shapes and on the
+ * current device.  For the tensor-core path it includes room for the fp32
+ * partial sums of split-K (used when the output tiles alone leave SMs idle: few
+ * tokens or few rows), at most ne11 * ne01 * 4 * ne00 / 512 bytes on top of
+ * ne11 * (2 * ne00 + 4 * ne00 / 32) + 4096. */
 Q4Q_API q4q_status q4q_mul_mat_workspace_size(int64_t ne00, int64_t ne01, int64_t ne11, size_t* bytes);
 
 /* ggml_mul_mat(src0 Q4_0 [ne00, ne01], src1 F32 [ne10, ne11]) -> dst F32 [ne01, ne11]
@@ -106,8 +109,10 @@ Q4Q_API q4q_status q4q_mul_mat_workspace_size(int64_t ne00, int64_t ne01, int64_
  * (results differ from a serial sum by rounding only).
  * src0: device, 2-byte aligned; src1 / dst: device, 4-byte aligned.
  * ne11 < 8 streams the weights once through a fused GEMV (no workspace);
- * ne11 >= 8 runs the tensor-core GEMM, which needs
- * q4q_mul_mat_workspace_size(...) bytes of 256-byte-aligned workspace.
+ * ne11 >= 8 runs the tensor-core GEMM on 256-byte-aligned workspace: with
+ * q4q_mul_mat_workspace_size(...) bytes it splits K as planned; with less (down to
+ * ne11 * (2 * ne00 + 4 * ne00 / 32) rounded, its split-free minimum) it uses fewer
+ * splits, each split's partial sums being added in a fixed order.
  * Limits: 0 < ne00 < 2^20 (ne00 % 32 == 0), 0 <= ne01 < 2^31, 0 <= ne11 < 2^20. */
 Q4Q_API q4q_status q4q_mul_mat(const void* src0, int64_t ne00, int64_t ne01,
                        const float* src1, int64_t ne10, int64_t ne11,
@@ -263,10 +268,10 @@ Q4Q_API q4q_status q4q_debug_block_isums_q8_0(const void* src0_q8_0, const void*
  * that the tensor-core and generic paths need comes from one static device array
  * of Q4Q_NOALLOC_SCRATCH_BYTES that the library owns on every GPU that loads it,
  * until the process exits.
- *  - Limit: problems whose q4q_mul_mat_workspace_size exceeds
- *    Q4Q_NOALLOC_SCRATCH_BYTES are rejected with Q4Q_ERR_WORKSPACE before any
- *    launch (e.g. ne11 = 512 tokens fits up to ne00 = 7680; ne11 = 2048 does not
- *    fit at ne00 = 4096).
+ *  - Limit: problems that need more than Q4Q_NOALLOC_SCRATCH_BYTES of scratch
+ *    even without split-K partial sums are rejected with Q4Q_ERR_WORKSPACE before
+ *    any launch (e.g. ne11 = 512 tokens fits up to ne00 = 7680; ne11 = 2048 does
+ *    not fit at ne00 = 4096); others use as many K splits as the array holds.
  *  - Set-up: the first call on a device, made while that device is current,
  *    looks up the array's device address (cudaGetSymbolAddress) and caches it;
  *    make that first call before any stream capture.

@@ -50,11 +50,9 @@ q4q_status check_mul_mat_shapes(int64_t ne00, int64_t ne01, int64_t ne10, int64_
     return Q4Q_OK;
 }
 
-}  // namespace q4q
+namespace {
 
-using namespace q4q;
-
-extern "C" q4q_status q4q_mul_mat_workspace_size(int64_t ne00, int64_t ne01, int64_t ne11, size_t* bytes) {
+q4q_status workspace_bytes_of(int64_t ne00, int64_t ne01, int64_t ne11, bool with_splits, size_t* bytes) {
     if (!bytes) return Q4Q_ERR_NULL;
     q4q_status st = check_mul_mat_shapes(ne00, ne01, ne00, ne11);
     if (st != Q4Q_OK) return st;
@@ -62,10 +60,26 @@ extern "C" q4q_status q4q_mul_mat_workspace_size(int64_t ne00, int64_t ne01, int
     if (ne11 >= 8) {
         DeviceInfo info;
         if ((st = current_device_info(&info)) != Q4Q_OK) return st;
-        if (mma_supported(ne00, ne01, ne11, info)) need = std::max(need, mma_workspace_bytes(ne00, ne11));
+        if (mma_supported(ne00, ne01, ne11, info))
+            need = std::max(need, with_splits ? mma_workspace_bytes_split(ne00, ne01, ne11, info)
+                                              : mma_workspace_bytes(ne00, ne11));
     }
     *bytes = need;
     return Q4Q_OK;
+}
+
+}  // namespace
+
+q4q_status mul_mat_min_workspace_bytes(int64_t ne00, int64_t ne01, int64_t ne11, size_t* bytes) {
+    return workspace_bytes_of(ne00, ne01, ne11, false, bytes);
+}
+
+}  // namespace q4q
+
+using namespace q4q;
+
+extern "C" q4q_status q4q_mul_mat_workspace_size(int64_t ne00, int64_t ne01, int64_t ne11, size_t* bytes) {
+    return workspace_bytes_of(ne00, ne01, ne11, true, bytes);
 }
 
 extern "C" q4q_status q4q_mul_mat(const void* src0, int64_t ne00, int64_t ne01,

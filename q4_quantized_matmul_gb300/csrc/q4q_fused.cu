@@ -122,7 +122,7 @@ extern "C" q4q_status q4q_mul_mat_q8_0_workspace_size(int64_t ne00, int64_t ne01
     if (ne11 >= 8) {
         DeviceInfo info;
         if ((st = current_device_info(&info)) != Q4Q_OK) return st;
-        if (mma_supported(ne00, ne01, ne11, info)) need = std::max(need, mma_workspace_bytes(ne00, ne11));
+        if (mma_supported(ne00, ne01, ne11, info)) need = std::max(need, mma_workspace_bytes_split(ne00, ne01, ne11, info));
     }
     *bytes = need;
     return Q4Q_OK;

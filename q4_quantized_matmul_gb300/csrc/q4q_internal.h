@@ -30,7 +30,10 @@ unsigned int mma_take_device_status();
 
 // tensor-core path (q4q_mma.cu)
 bool mma_supported(int64_t ne00, int64_t ne01, int64_t ne11, const DeviceInfo& info);
+// the least workspace the tensor-core path runs in (no split-K), and the size that
+// also holds the partial sums of the split-K it would pick for the shape
 size_t mma_workspace_bytes(int64_t ne00, int64_t ne11);
+size_t mma_workspace_bytes_split(int64_t ne00, int64_t ne01, int64_t ne11, const DeviceInfo& info);
 // q8_weights: src0 holds Q8_0 blocks instead of Q4_0 ones
 q4q_status mma_mul_mat(const void* src0, int64_t ne00, int64_t ne01, const float* src1, int64_t ne11,
                        float* dst, void* workspace, size_t workspace_bytes, cudaStream_t stream,
@@ -89,6 +92,9 @@ unsigned int rows_take_device_status();
 
 // Shape rules shared by every matmul entry point (q4q_api.cu).
 q4q_status check_mul_mat_shapes(int64_t ne00, int64_t ne01, int64_t ne10, int64_t ne11);
+// The least workspace q4q_mul_mat runs in for this shape (the tensor-core path then
+// uses fewer K splits than q4q_mul_mat_workspace_size makes room for).
+q4q_status mul_mat_min_workspace_bytes(int64_t ne00, int64_t ne01, int64_t ne11, size_t* bytes);
 
 // quantizers (q4q_quant.cu), also used by the GEMM / generic paths
 q4q_status launch_quantize(bool q4, const float* src, void* dst, int64_t ncols, int64_t nrows,

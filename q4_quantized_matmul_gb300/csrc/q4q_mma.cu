@@ -221,7 +221,8 @@ __host__ __device__ constexpr int perm8(int p) { return (p & 1) ? 4 + (p >> 1) :
 
 struct MmaParams {
     int M, N, K, nb, Npad;
-    float* dst;           // [N][M]
+    int splits;           // split-K: blockIdx.z takes raw stages [z * n / splits, (z + 1) * n / splits)
+    float* dst;           // [N][M]; with splits > 1 the partial sums go to dst + z * N * M
     const float* dx;      // [nb][Npad]
     int32_t* isums;       // debug: [N][M][nb]
 };
@@ -317,7 +318,12 @@ mma_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * NT;
     const int m0 = blockIdx.y * BM;
-    const int n_raw = p.K / KRAW, n_ab = p.K / KAB, n_slab = p.K / 32;
+    // this CTA's share of the K loop (split-K: a contiguous range of raw stages)
+    const int n_raw_all = p.K / KRAW;
+    const int r_begin = (int)(((int64_t)blockIdx.z * n_raw_all) / p.splits);
+    const int r_end = (int)(((int64_t)(blockIdx.z + 1) * n_raw_all) / p.splits);
+    const int n_raw = r_end - r_begin, n_ab = n_raw * (KRAW / KAB), n_slab = n_raw * (KRAW / 32);
+    const int ab_begin = r_begin * (KRAW / KAB);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < RAW_STAGES; ++s) {
@@ -353,7 +359,7 @@ mma_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                 const int st = r % RAW_STAGES;
                 if (r >= RAW_STAGES && !wait_or_abort(raw_empty + 8 * st, ((r / RAW_STAGES) + 1) & 1, abort_flag)) break;
                 mbar_arrive_expect_tx(raw_full + 8 * st, RAW_BYTES);
-                tma_load_2d(sbase + C::OFF_RAW + st * RAW_BYTES, &tmap_w, r * (C::RAW_ROW / raw_elem_bytes(WT)), m0,
+                tma_load_2d(sbase + C::OFF_RAW + st * RAW_BYTES, &tmap_w, (r_begin + r) * (C::RAW_ROW / raw_elem_bytes(WT)), m0,
                             raw_full + 8 * st);
             }
             if (*abort_flag)   // let the loads already issued land before the CTA exits
@@ -369,10 +375,10 @@ mma_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                 if (i >= AB_STAGES && !wait_or_abort(ab_empty + 8 * s, ((i / AB_STAGES) + 1) & 1, abort_flag)) break;
                 const uint32_t bar = ab_full + 8 * s;
                 mbar_arrive_expect_tx(bar, C::B_BYTES + C::DX_BYTES);
-                tma_load_2d(sbase + C::OFF_B + s * C::B_STRIDE, &tmap_b, i * KAB, n0, bar);
+                tma_load_2d(sbase + C::OFF_B + s * C::B_STRIDE, &tmap_b, (ab_begin + i) * KAB, n0, bar);
                 const uint32_t dxd = sbase + C::OFF_DX + s * C::DX_BYTES;
-                bulk_g2s(dxd, p.dx + (size_t)(2 * i) * p.Npad + n0, NT * 4, bar);
-                bulk_g2s(dxd + NT * 4, p.dx + (size_t)(2 * i + 1) * p.Npad + n0, NT * 4, bar);
+                bulk_g2s(dxd, p.dx + (size_t)(2 * (ab_begin + i)) * p.Npad + n0, NT * 4, bar);
+                bulk_g2s(dxd + NT * 4, p.dx + (size_t)(2 * (ab_begin + i) + 1) * p.Npad + n0, NT * 4, bar);
             }
             if (*abort_flag)
                 for (int i2 = max(0, i - AB_STAGES); i2 < i; ++i2)
@@ -541,7 +547,8 @@ mma_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                     for (int c = 0; c < 8; ++c) {
                         const int n = n0 + col0 + c0 + c;
                         if (n < p.N && m < p.M)
-                            p.isums[((size_t)n * p.M + m) * p.nb + g] = (int32_t)__uint_as_float(r[c]);
+                            p.isums[((size_t)n * p.M + m) * p.nb + r_begin * (KRAW / 32) + g] =
+                                (int32_t)__uint_as_float(r[c]);
                     }
                 }
                 tc_fence_before();
@@ -613,13 +620,14 @@ mma_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                 if (lane == 0) mbar_arrive(ab_empty + 8 * s);
             }
             if (!aborted && !*abort_flag && m < p.M) {
+                float* out = p.dst + (size_t)blockIdx.z * p.N * p.M;
 #pragma unroll
                 for (int c = 0; c < C::CPW / 2; ++c) {
                     float x0, x1;
                     unpack2(acc[c], x0, x1);
                     const int n = n0 + col0 + 2 * c;
-                    if (n < p.N) p.dst[(size_t)n * p.M + m] = x0;
-                    if (n + 1 < p.N) p.dst[(size_t)(n + 1) * p.M + m] = x1;
+                    if (n < p.N) out[(size_t)n * p.M + m] = x0;
+                    if (n + 1 < p.N) out[(size_t)(n + 1) * p.M + m] = x1;
                 }
             }
         }
@@ -713,6 +721,16 @@ q8_to_mma_kernel(const uint8_t* __restrict__ yq, __half* __restrict__ bmat, floa
     }
 }
 
+// dst[i] = sum over the splits of part[s][i], in split order (deterministic).
+__global__ void __launch_bounds__(256)
+split_reduce_kernel(const float* __restrict__ part, float* __restrict__ dst, int splits, int64_t nm) {
+    for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < nm; i += (int64_t)gridDim.x * 256) {
+        float acc = __ldcs(part + i);
+        for (int z = 1; z < splits; ++z) acc = __fadd_rn(acc, __ldcs(part + (int64_t)z * nm + i));
+        dst[i] = acc;
+    }
+}
+
 // ------------------------------------------------------------------ host ----
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -752,14 +770,14 @@ q4q_status launch_mma_t(const CUtensorMap& tw, const CUtensorMap& tb, const MmaP
             return Q4Q_ERR_CUDA;
         configured[device].store(1);
     }
-    dim3 grid((unsigned)((p.N + NT - 1) / NT), (unsigned)((p.M + BM - 1) / BM));
+    dim3 grid((unsigned)((p.N + NT - 1) / NT), (unsigned)((p.M + BM - 1) / BM), (unsigned)p.splits);
     kern<<<grid, C::THREADS, C::SMEM, stream>>>(tw, tb, p);
     return launch_status();
 }
 
 template <bool DEBUG, int WT>
 q4q_status run_mma(const void* src0, int64_t ne00, int64_t ne01, int64_t ne11, const __half* bmat, const float* dx,
-                   float* dst, int32_t* isums, cudaStream_t stream, const DeviceInfo& info) {
+                   float* dst, int32_t* isums, int splits, cudaStream_t stream, const DeviceInfo& info) {
     if (!get_encode()) return Q4Q_ERR_CUDA;
     const int NT = pick_nt(ne11);
     const int64_t row_bytes = ne00 / QK * (WT == WQ8_0 ? Q8_0_BYTES : Q4_0_BYTES);
@@ -792,6 +810,7 @@ q4q_status run_mma(const void* src0, int64_t ne00, int64_t ne01, int64_t ne11, c
     p.K = (int)ne00;
     p.nb = (int)(ne00 / QK);
     p.Npad = (int)npad_of(ne11);
+    p.splits = splits;
     p.dst = dst;
     p.dx = dx;
     p.isums = isums;
@@ -823,10 +842,36 @@ size_t mma_workspace_bytes(int64_t ne00, int64_t ne11) {
     return b_bytes_of(ne00, ne11) + (size_t)(ne00 / QK) * (size_t)npad_of(ne11) * 4;
 }
 
+// Split-K: when the output tiles alone leave SMs idle (few tokens, few rows), the K
+// loop of every tile is split over blockIdx.z, each split writing fp32 partial sums
+// that split_reduce_kernel adds in split order.  Each split keeps at least two raw
+// stages (512 K).
+int mma_desired_splits(int64_t ne00, int64_t ne01, int64_t ne11, const DeviceInfo& info) {
+    const int NT = pick_nt(ne11);
+    const int64_t tiles = ((ne11 + NT - 1) / NT) * ((ne01 + BM - 1) / BM);
+    const int64_t target = (int64_t)info.sm_count * (NT <= 32 ? 2 : 1);
+    if (tiles <= 0 || tiles >= target) return 1;
+    const int64_t most = (ne00 / KRAW) / 2;
+    return (int)std::max<int64_t>(1, std::min<int64_t>((target + tiles - 1) / tiles, most));
+}
+
+size_t split_partial_bytes(int64_t ne01, int64_t ne11, int splits) {
+    return splits > 1 ? ((size_t)splits * (size_t)ne01 * (size_t)ne11 * 4 + 255) / 256 * 256 : 0;
+}
+
+size_t mma_workspace_bytes_split(int64_t ne00, int64_t ne01, int64_t ne11, const DeviceInfo& info) {
+    return mma_workspace_bytes(ne00, ne11) + split_partial_bytes(ne01, ne11, mma_desired_splits(ne00, ne01, ne11, info));
+}
+
 q4q_status mma_mul_mat(const void* src0, int64_t ne00, int64_t ne01, const float* src1, int64_t ne11, float* dst,
                        void* workspace, size_t workspace_bytes, cudaStream_t stream, const DeviceInfo& info,
                        bool q8_weights) {
-    if (workspace_bytes < mma_workspace_bytes(ne00, ne11)) return Q4Q_ERR_WORKSPACE;
+    const size_t base = mma_workspace_bytes(ne00, ne11);
+    if (workspace_bytes < base) return Q4Q_ERR_WORKSPACE;
+    // as many K splits as wanted and as the workspace holds partial sums for
+    int splits = mma_desired_splits(ne00, ne01, ne11, info);
+    while (splits > 1 && base + split_partial_bytes(ne01, ne11, splits) > workspace_bytes) --splits;
+    float* part = splits > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + base) : nullptr;
     __half* bmat = static_cast<__half*>(workspace);
     float* dx = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + b_bytes_of(ne00, ne11));
     const int64_t items = ne11 * (ne00 / QK) * 4;
@@ -834,8 +879,14 @@ q4q_status mma_mul_mat(const void* src0, int64_t ne00, int64_t ne01, const float
     act_to_mma_kernel<<<grid, 256, 0, stream>>>(src1, bmat, dx, (int)ne00, (int)ne11, (int)npad_of(ne11));
     q4q_status st = launch_status();
     if (st != Q4Q_OK) return st;
-    return q8_weights ? run_mma<false, WQ8_0>(src0, ne00, ne01, ne11, bmat, dx, dst, nullptr, stream, info)
-                      : run_mma<false, WQ4_0>(src0, ne00, ne01, ne11, bmat, dx, dst, nullptr, stream, info);
+    float* out = splits > 1 ? part : dst;
+    st = q8_weights ? run_mma<false, WQ8_0>(src0, ne00, ne01, ne11, bmat, dx, out, nullptr, splits, stream, info)
+                    : run_mma<false, WQ4_0>(src0, ne00, ne01, ne11, bmat, dx, out, nullptr, splits, stream, info);
+    if (st != Q4Q_OK || splits == 1) return st;
+    const int64_t nm = ne01 * ne11;
+    const int rgrid = (int)std::max<int64_t>(1, std::min<int64_t>((nm + 255) / 256, (int64_t)info.sm_count * 8));
+    split_reduce_kernel<<<rgrid, 256, 0, stream>>>(part, dst, splits, nm);
+    return launch_status();
 }
 
 size_t mma_debug_workspace_bytes(int64_t ne00, int64_t ne11) { return mma_workspace_bytes(ne00, ne11); }
@@ -856,8 +907,8 @@ q4q_status mma_debug_isums(const void* src0, const void* src1_q8_0, int64_t ne00
                                                (int)ne11, (int)npad_of(ne11));
     q4q_status st = launch_status();
     if (st != Q4Q_OK) return st;
-    return q8_weights ? run_mma<true, WQ8_0>(src0, ne00, ne01, ne11, bmat, dx, nullptr, out, stream, info)
-                      : run_mma<true, WQ4_0>(src0, ne00, ne01, ne11, bmat, dx, nullptr, out, stream, info);
+    return q8_weights ? run_mma<true, WQ8_0>(src0, ne00, ne01, ne11, bmat, dx, nullptr, out, 1, stream, info)
+                      : run_mma<true, WQ4_0>(src0, ne00, ne01, ne11, bmat, dx, nullptr, out, 1, stream, info);
 }
 
 }  // namespace q4q

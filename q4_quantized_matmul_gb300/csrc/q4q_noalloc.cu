@@ -48,7 +48,7 @@ extern "C" q4q_status q4q_mul_mat_noalloc(const void* src0, int64_t ne00, int64_
                                           const float* src1, int64_t ne10, int64_t ne11,
                                           float* dst, q4q_stream_t stream) {
     size_t need = 0;
-    q4q_status st = q4q_mul_mat_workspace_size(ne00, ne01, ne11, &need);
+    q4q_status st = q4q::mul_mat_min_workspace_bytes(ne00, ne01, ne11, &need);
     if (st != Q4Q_OK) return st;
     if (ne10 != ne00) return Q4Q_ERR_SHAPE;
     if (ne01 == 0 || ne11 == 0) return Q4Q_OK;
