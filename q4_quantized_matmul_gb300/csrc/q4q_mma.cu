@@ -842,17 +842,22 @@ size_t mma_workspace_bytes(int64_t ne00, int64_t ne11) {
     return b_bytes_of(ne00, ne11) + (size_t)(ne00 / QK) * (size_t)npad_of(ne11) * 4;
 }
 
-// Split-K: when the output tiles alone leave SMs idle (few tokens, few rows), the K
-// loop of every tile is split over blockIdx.z, each split writing fp32 partial sums
-// that split_reduce_kernel adds in split order.  Each split keeps at least two raw
-// stages (512 K).
+// Split-K: when the output tiles alone leave most SMs idle (few tokens, few rows),
+// the K loop of every tile is split over blockIdx.z, each split writing fp32 partial
+// sums that split_reduce_kernel adds in split order.  Each split keeps at least two
+// raw stages (512 K).  Fewer than 4 splits do not pay for the partial sums' traffic
+// and the extra launch: timed on the Llama set, 2 or 3 splits made gate/up (112
+// tiles at 8-64 tokens) and q/o/down (128 tiles at 512 tokens) slower, while 5-10
+// splits made the 8- and 32-tile matrices 1.3-2.4x faster.
 int mma_desired_splits(int64_t ne00, int64_t ne01, int64_t ne11, const DeviceInfo& info) {
     const int NT = pick_nt(ne11);
     const int64_t tiles = ((ne11 + NT - 1) / NT) * ((ne01 + BM - 1) / BM);
     const int64_t target = (int64_t)info.sm_count * (NT <= 32 ? 2 : 1);
-    if (tiles <= 0 || tiles >= target) return 1;
+    if (tiles <= 0) return 1;
+    const int64_t want = (target + tiles - 1) / tiles;
     const int64_t most = (ne00 / KRAW) / 2;
-    return (int)std::max<int64_t>(1, std::min<int64_t>((target + tiles - 1) / tiles, most));
+    const int64_t s = std::min<int64_t>(want, most);
+    return s >= 4 ? (int)s : 1;
 }
 
 size_t split_partial_bytes(int64_t ne01, int64_t ne11, int splits) {
