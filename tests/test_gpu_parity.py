@@ -308,6 +308,42 @@ def test_mul_mat_tensor_core(q4q, ne00, ne01, ne11):
     assert q4q.q4q_device_status() == 0
 
 
+def _min_mma_workspace(ne00, ne11):
+    # the split-free minimum of the tensor-core path: fp16 operand + block scales
+    return (ne11 * ne00 * 2 + 255) // 256 * 256 + (ne00 // 32) * ((ne11 + 127) // 128 * 128) * 4
+
+
+@pytest.mark.parametrize("ne00,ne01,ne11,split", [(4096, 1024, 8, True), (4096, 300, 64, True),
+                                                  (14336, 256, 16, True), (1024, 64, 200, False)])
+@pytest.mark.parametrize("kind", ["q4_0", "q8_0"])
+def test_mul_mat_split_k(q4q, ne00, ne01, ne11, split, kind):
+    """Split-K (few output tiles): with the workspace q4q_mul_mat_workspace_size asks for,
+    the K loop is split and the partial sums added in order; with the split-free minimum
+    it runs unsplit.  Both are within tolerance of the oracle."""
+    rng = np.random.default_rng([ne00, ne01, ne11, 11])
+    w = _special_weights(rng, ne01, ne00)
+    x = rng.standard_normal((ne11, ne00)).astype(np.float32)
+    x[ne11 // 3] = 0.0
+    if kind == "q4_0":
+        wq = oracle.quantize_q4_0(w)
+        full = q4q.q4q_mul_mat_workspace_size(ne00, ne01, ne11)
+        call = q4q.q4q_mul_mat
+        ref, scale = oracle.mul_mat(wq, ne00, ne01, x, nthreads=8)
+    else:
+        wq = oracle.quantize_q8_0(w)
+        full = q4q.q4q_mul_mat_q8_0_workspace_size(ne00, ne01, ne11)
+        call = q4q.q4q_mul_mat_q8_0
+        ref, scale = oracle.mul_mat_w8(wq, ne00, ne01, x, nthreads=8)
+    least = _min_mma_workspace(ne00, ne11)
+    assert (full > least) == split
+    wq_d, x_d = dev(wq), dev(x)
+    for nbytes in (full, least):
+        ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        got = call(wq_d, ne00, ne01, x_d, workspace=ws).cpu().numpy()
+        assert_close(got, ref, scale)
+    assert q4q.q4q_device_status() == 0
+
+
 def test_mul_mat_pdl_chain(q4q):
     # y1 = W1 x, y2 = W2 y1, y3 = W3 y2 with programmatic dependent launch: every
     # call must see its predecessor's output (same kernels, so results are identical)
