@@ -58,7 +58,7 @@ typedef enum {
     Q4Q_ERR_SHAPE = 2,      /* ne00 <= 0, ne00 % 32 != 0, ne10 != ne00, size < 0,
                                or a size beyond the documented limits              */
     Q4Q_ERR_ALIGN = 3,      /* a pointer is not aligned as the call requires       */
-    Q4Q_ERR_WORKSPACE = 4,  /* workspace smaller than q4q_mul_mat_workspace_size   */
+    Q4Q_ERR_WORKSPACE = 4,  /* workspace smaller than the call needs (see each call) */
     Q4Q_ERR_CUDA = 5,       /* a CUDA runtime call or kernel launch failed          */
     Q4Q_ERR_TIMEOUT = 6,    /* a bounded device wait ran out (see q4q_device_status) */
     Q4Q_ERR_ARG = 7         /* any other invalid argument (e.g. unknown path)       */
