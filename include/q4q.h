@@ -299,6 +299,14 @@ Q4Q_API q4q_status q4q_debug_block_isums(const void* src0, const void* src1_q8_0
                                  int32_t* out, void* workspace, size_t workspace_bytes,
                                  q4q_stream_t stream);
 
+/* Debug: the failure path of the library's bounded waits, on its own.  Launches
+ * one CTA whose thread waits, for at most limit_ns nanoseconds, on an mbarrier
+ * phase that nothing completes (the wait every kernel uses for its copies and
+ * hand-offs), then records Q4Q_ERR_TIMEOUT in the device status word and returns;
+ * q4q_device_status reports it.  No GPU fault or hang is involved, and the context
+ * stays usable.  limit_ns: 1 .. 1e9, else Q4Q_ERR_ARG. */
+Q4Q_API q4q_status q4q_debug_wait_timeout(uint64_t limit_ns, q4q_stream_t stream);
+
 /* Synchronizes the device, returns (in *status) the first device-side error
  * recorded since the last call (Q4Q_OK if none) and clears it. */
 Q4Q_API q4q_status q4q_device_status(q4q_status* status);

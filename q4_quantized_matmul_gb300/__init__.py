@@ -25,7 +25,7 @@ __all__ = [
     "Q4Q_ACT_NONE", "Q4Q_ACT_GELU", "q4q_mul_mat_bias_act", "q4q_mul_mat_swiglu_workspace_size",
     "q4q_mul_mat_swiglu", "q4q_get_rows_q4_0", "q4q_get_rows_q8_0", "q4q_mul_mat_q8_0_workspace_size",
     "q4q_mul_mat_q8_0", "q4q_debug_block_isums_q8_0", "Q4Q_GROUP_MAX", "q4q_mul_mat_group_workspace_size",
-    "q4q_mul_mat_group",
+    "q4q_mul_mat_group", "q4q_debug_wait_timeout",
 ]
 
 QK = 32
@@ -380,3 +380,9 @@ def q4q_mul_mat_group(src0s, ne01s, ne00: int, src1: torch.Tensor, dsts=None,
     _check("q4q_mul_mat_group", _lib.load().q4q_mul_mat_group(n, ptrs, rows, ne00, _dev(x, "src1"), ne10, ne11, outs,
                                                              ws_ptr, ws_bytes, int(flags), _stream(stream)))
     return dsts
+
+
+def q4q_debug_wait_timeout(limit_ns: int, stream=None) -> None:
+    """Run the library's bounded-wait failure path on its own: one wait that nothing
+    completes, given up after limit_ns; q4q_device_status() then reports Q4Q_ERR_TIMEOUT (6)."""
+    _check("q4q_debug_wait_timeout", _lib.load().q4q_debug_wait_timeout(int(limit_ns), _stream(stream)))

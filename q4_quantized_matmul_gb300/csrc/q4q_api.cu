@@ -138,6 +138,11 @@ extern "C" q4q_status q4q_debug_block_isums(const void* src0, const void* src1_q
     return mma_debug_isums(src0, src1_q8_0, ne00, ne01, ne11, out, workspace, workspace_bytes, stream, info);
 }
 
+extern "C" q4q_status q4q_debug_wait_timeout(uint64_t limit_ns, q4q_stream_t stream) {
+    if (limit_ns == 0 || limit_ns > WAIT_LIMIT_NS) return Q4Q_ERR_ARG;
+    return launch_wait_timeout(limit_ns, (cudaStream_t)stream);
+}
+
 extern "C" q4q_status q4q_device_status(q4q_status* status) {
     if (!status) return Q4Q_ERR_NULL;
     if (cudaDeviceSynchronize() != cudaSuccess) return Q4Q_ERR_CUDA;

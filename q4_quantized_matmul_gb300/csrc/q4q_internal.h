@@ -87,6 +87,9 @@ q4q_status gemv_mul_mat_group(int n, const void* const* src0, const int64_t* ne0
                               int64_t ne11, float* const* dst, cudaStream_t stream, const DeviceInfo& info,
                               bool pdl);
 
+// the bounded-wait failure path on its own (q4q_gemv.cu)
+q4q_status launch_wait_timeout(uint64_t limit_ns, cudaStream_t stream);
+
 // row gather (q4q_rows.cu)
 unsigned int rows_take_device_status();
 

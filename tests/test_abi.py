@@ -179,3 +179,8 @@ def test_argument_errors_of_the_group_entry(lib):
     assert lib.q4q_mul_mat_group(2, ptrs, zero, 64, None, 64, 1, ptrs, None, 0, 0, None) == 0
     assert lib.q4q_mul_mat_group_workspace_size(2, rows, 64, 3, None) == 1
     assert lib.q4q_mul_mat_group_workspace_size(9, rows, 64, 3, ctypes.byref(n)) == 7
+
+
+def test_wait_timeout_argument_errors(lib):
+    assert lib.q4q_debug_wait_timeout(0, None) == 7
+    assert lib.q4q_debug_wait_timeout(2 * 10 ** 9, None) == 7

@@ -414,6 +414,23 @@ def test_no_device_errors_recorded(q4q):
     assert q4q.q4q_device_status() == 0
 
 
+def test_bounded_wait_reports_timeout_and_context_stays_usable(q4q):
+    # a wait that nothing completes gives up after 2 ms and records Q4Q_ERR_TIMEOUT;
+    # the status is read (and cleared) on the host, and the next call works
+    assert q4q.q4q_device_status() == 0
+    q4q.q4q_debug_wait_timeout(2_000_000)
+    assert q4q.q4q_device_status() == 6
+    assert q4q.q4q_device_status() == 0
+    rng = np.random.default_rng(12)
+    w = (rng.standard_normal((300, 1024)) * 0.02).astype(np.float32)
+    x = rng.standard_normal((1, 1024)).astype(np.float32)
+    wq = oracle.quantize_q4_0(w)
+    got = q4q.q4q_mul_mat(dev(wq), 1024, 300, dev(x)).cpu().numpy()
+    ref, scale = oracle.mul_mat(wq, 1024, 300, x)
+    assert_close(got, ref, scale)
+    assert q4q.q4q_device_status() == 0
+
+
 # ---------------------------------------------------- full-size workloads ----
 
 def _sample_rows(ne01, n, seed):
