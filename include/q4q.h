@@ -299,6 +299,25 @@ Q4Q_API q4q_status q4q_debug_block_isums(const void* src0, const void* src1_q8_0
                                  int32_t* out, void* workspace, size_t workspace_bytes,
                                  q4q_stream_t stream);
 
+/* Debug, host only (no GPU needed): the GEMV launch plan for 1..7 tokens on a
+ * device with sm_count SMs and smem_optin bytes of opt-in shared memory per CTA,
+ * for weight blocks of weight_block_bytes (18: Q4_0, 34: Q8_0) and mats matrices
+ * streamed side by side (1, or 2 for the SwiGLU kernel).  On Q4Q_OK, out[0 ..
+ * Q4Q_DEBUG_GEMV_PLAN_FIELDS-1] receives: rows per unit, ring stages, bytes per
+ * stage, dynamic shared memory, grid (without clusters), cluster size, lanes per
+ * row, register-resident block pairs per lane, units, and the shared-memory
+ * offsets of the activations, of the ring and of the second matrix's rows in a
+ * stage, the row bytes, and the offsets of the activation scales and code sums.
+ * Q4Q_ERR_SHAPE when the GEMV takes no such problem (the generic kernel runs it). */
+#define Q4Q_DEBUG_GEMV_PLAN_FIELDS 15
+Q4Q_API q4q_status q4q_debug_gemv_plan(int64_t ne00, int64_t ne01, int64_t ne11, int weight_block_bytes, int mats,
+                               int sm_count, int smem_optin, int64_t* out);
+
+/* Debug, host only: how many ways the tensor-core GEMM splits K for this problem
+ * on a device with sm_count SMs, given enough workspace (1 = no split).  Requires
+ * ne00 % 256 == 0, ne11 >= 8 and ne01 > 0, else Q4Q_ERR_ARG. */
+Q4Q_API q4q_status q4q_debug_mma_splits(int64_t ne00, int64_t ne01, int64_t ne11, int sm_count, int* splits);
+
 /* Debug: the failure path of the library's bounded waits, on its own.  Launches
  * one CTA whose thread waits, for at most limit_ns nanoseconds, on an mbarrier
  * phase that nothing completes (the wait every kernel uses for its copies and

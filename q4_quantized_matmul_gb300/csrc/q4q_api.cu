@@ -138,6 +138,24 @@ extern "C" q4q_status q4q_debug_block_isums(const void* src0, const void* src1_q
     return mma_debug_isums(src0, src1_q8_0, ne00, ne01, ne11, out, workspace, workspace_bytes, stream, info);
 }
 
+extern "C" q4q_status q4q_debug_gemv_plan(int64_t ne00, int64_t ne01, int64_t ne11, int weight_block_bytes,
+                                          int mats, int sm_count, int smem_optin, int64_t* out) {
+    if (!out) return Q4Q_ERR_NULL;
+    if (weight_block_bytes != Q4Q_BLOCK_Q4_0_BYTES && weight_block_bytes != Q4Q_BLOCK_Q8_0_BYTES) return Q4Q_ERR_ARG;
+    if (mats != 1 && mats != 2) return Q4Q_ERR_ARG;
+    if (sm_count <= 0 || smem_optin <= 0) return Q4Q_ERR_ARG;
+    return debug_gemv_plan(ne00, ne01, ne11, weight_block_bytes, mats, sm_count, smem_optin, out);
+}
+
+extern "C" q4q_status q4q_debug_mma_splits(int64_t ne00, int64_t ne01, int64_t ne11, int sm_count, int* splits) {
+    if (!splits) return Q4Q_ERR_NULL;
+    q4q_status st = check_mul_mat_shapes(ne00, ne01, ne00, ne11);
+    if (st != Q4Q_OK) return st;
+    if (sm_count <= 0 || ne00 % 256 != 0 || ne11 < 8 || ne01 == 0) return Q4Q_ERR_ARG;
+    *splits = debug_mma_splits(ne00, ne01, ne11, sm_count);
+    return Q4Q_OK;
+}
+
 extern "C" q4q_status q4q_debug_wait_timeout(uint64_t limit_ns, q4q_stream_t stream) {
     if (limit_ns == 0 || limit_ns > WAIT_LIMIT_NS) return Q4Q_ERR_ARG;
     return launch_wait_timeout(limit_ns, (cudaStream_t)stream);
@@ -151,7 +169,7 @@ extern "C" q4q_status q4q_device_status(q4q_status* status) {
     const unsigned int words[] = {gemv_take_device_status(), mma_take_device_status(),
                                   gemv_swiglu_take_device_status(), gemv_w8_take_device_status(),
                                   gemv_group_take_device_status(), gemv_epi_take_device_status(),
-                                  rows_take_device_status()};
+                                  rows_take_device_status(), debug_take_device_status()};
     unsigned int first = 0;
     for (unsigned int w : words)
         if (!first) first = w;

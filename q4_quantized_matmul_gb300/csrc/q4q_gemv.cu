@@ -96,27 +96,9 @@ debug_isums_gemv_kernel(const uint8_t* __restrict__ w, const uint8_t* __restrict
     }
 }
 
-// One thread waits on phase 0 of an mbarrier that no thread or copy ever
-// completes, with the bounded wait every kernel of the library uses, and records
-// Q4Q_ERR_TIMEOUT when the limit runs out: the failure path of the real kernels,
-// driven without planting a fault in them.
-__global__ void __launch_bounds__(32) wait_timeout_kernel(uint64_t limit_ns) {
-    __shared__ __align__(8) uint64_t bar;
-    if (threadIdx.x == 0) {
-        mbar_init(smem_u32(&bar), 1);
-        fence_mbar_init();
-        if (!mbar_wait_bounded(smem_u32(&bar), 0, limit_ns)) record_error(&g_gemv_status, DEV_TIMEOUT);
-    }
-}
-
 }  // namespace
 
 unsigned int gemv_take_device_status() { return take_gemv_status_word(); }
-
-q4q_status launch_wait_timeout(uint64_t limit_ns, cudaStream_t stream) {
-    wait_timeout_kernel<<<1, 32, 0, stream>>>(limit_ns);
-    return launch_status();
-}
 
 bool gemv_supported(const void* src0, int64_t ne00, int64_t ne01, const float* src1, int64_t ne11,
                     const DeviceInfo& info) {

@@ -87,8 +87,16 @@ q4q_status gemv_mul_mat_group(int n, const void* const* src0, const int64_t* ne0
                               int64_t ne11, float* const* dst, cudaStream_t stream, const DeviceInfo& info,
                               bool pdl);
 
-// the bounded-wait failure path on its own (q4q_gemv.cu)
+// the GEMM's split-K count for a shape (q4q_mma.cu)
+int mma_desired_splits(int64_t ne00, int64_t ne01, int64_t ne11, const DeviceInfo& info);
+
+// test entry points (q4q_debug.cu): host-only views of the launch planning, and
+// the bounded-wait failure path on its own (with its own device status word)
+q4q_status debug_gemv_plan(int64_t ne00, int64_t ne01, int64_t ne11, int block_bytes, int mats, int sm_count,
+                           int smem_optin, int64_t* out);
+int debug_mma_splits(int64_t ne00, int64_t ne01, int64_t ne11, int sm_count);
 q4q_status launch_wait_timeout(uint64_t limit_ns, cudaStream_t stream);
+unsigned int debug_take_device_status();
 
 // row gather (q4q_rows.cu)
 unsigned int rows_take_device_status();
