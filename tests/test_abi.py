@@ -184,3 +184,41 @@ def test_argument_errors_of_the_group_entry(lib):
 def test_wait_timeout_argument_errors(lib):
     assert lib.q4q_debug_wait_timeout(0, None) == 7
     assert lib.q4q_debug_wait_timeout(2 * 10 ** 9, None) == 7
+
+
+def test_c_program_links_and_calls_the_library(lib):
+    """A plain C99 caller: includes q4q.h, links libq4q.so and makes the calls that
+    need no GPU (version, status strings, argument errors, host-only planning)."""
+    from q4_quantized_matmul_gb300 import _lib
+    src = r"""
+#include <stdio.h>
+#include <string.h>
+#include "q4q.h"
+int main(void) {
+    int64_t plan[Q4Q_DEBUG_GEMV_PLAN_FIELDS];
+    int splits = 0;
+    size_t ws = 0;
+    if ((q4q_version() >> 16) != 1) return 1;
+    if (strcmp(q4q_status_string(Q4Q_ERR_SHAPE), "invalid shape") != 0) return 2;
+    if (q4q_mul_mat((const void*)0x1000, 33, 4, (const float*)0x1000, 33, 1, (float*)0x1000, NULL, 0, NULL)
+        != Q4Q_ERR_SHAPE) return 3;
+    if (q4q_mul_mat_workspace_size(64, 4, 3, &ws) != Q4Q_OK || ws != 3 * 2 * 34) return 4;
+    if (q4q_debug_gemv_plan(4096, 128256, 1, Q4Q_BLOCK_Q4_0_BYTES, 1, 152, 232448, plan) != Q4Q_OK) return 5;
+    if (plan[0] != 8 || plan[4] != 304) return 6;
+    if (q4q_debug_mma_splits(4096, 1024, 8, 152, &splits) != Q4Q_OK || splits != 8) return 7;
+    if (q4q_get_rows_q4_0((const void*)0x1000, 48, 10, NULL, 3, (float*)0x1000, NULL) != Q4Q_ERR_SHAPE) return 8;
+    printf("ok\n");
+    return 0;
+}
+"""
+    exe = "/tmp/q4q_c_caller_%d" % os.getpid()
+    build_dir = os.path.dirname(_lib.LIB_PATH)
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), "-x", "c", "-",
+                        "-L", build_dir, "-lq4q", "-Wl,-rpath," + build_dir, "-o", exe],
+                       input=src, text=True, capture_output=True)
+    assert r.returncode == 0, r.stderr
+    try:
+        out = subprocess.run([exe], capture_output=True, text=True)
+    finally:
+        os.unlink(exe)
+    assert out.returncode == 0 and out.stdout == "ok\n", (out.returncode, out.stdout, out.stderr)
