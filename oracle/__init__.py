@@ -20,6 +20,12 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "q4q_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "_build", "liboracle.so")
+# The mutation tests (tests/test_oracle_mutations.py) run the pins against copies
+# of q4q_oracle.c with one planted mistake each: Q4Q_ORACLE_SRC names such a copy,
+# which is then built into its own library beside it.
+if os.environ.get("Q4Q_ORACLE_SRC"):
+    _SRC = os.path.abspath(os.environ["Q4Q_ORACLE_SRC"])
+    _LIB_PATH = os.path.join(os.path.dirname(_SRC), "_build", "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
@@ -37,7 +43,7 @@ def build(force: bool = False) -> str:
         return _LIB_PATH
     tmp = _LIB_PATH + ".tmp.%d" % os.getpid()
     cmd = ["gcc", "-std=c99", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
-           "-fPIC", "-shared", "-Wall", "-o", tmp, _SRC, "-lm"]
+           "-fPIC", "-shared", "-Wall", "-I" + _HERE, "-o", tmp, _SRC, "-lm"]
     subprocess.run(cmd, check=True, cwd=_HERE)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH

@@ -70,6 +70,58 @@ def test_hand_worked_block():
     assert float(np.dot(w[0].astype(np.float64), x[0])) == float(g["dst_unquantized"])
 
 
+
+def test_two_block_tolerance_scale():
+    # The tolerance scale S = sum_b |fp32(d_w d_x) * isum_b| on a row whose two
+    # block sums have opposite signs (the hand block followed by its negation,
+    # tests/golden/two_block_scale.txt): S is the sum of the absolute block terms,
+    # not the absolute value of their sum, and dst keeps its sign.
+    g = _golden("two_block_scale.txt")
+    a = ((np.arange(32) - 16) * 0.25).astype(np.float32)
+    w = np.concatenate([a, -a]).reshape(1, 64)
+    blocks = oracle.quantize_q4_0(w)[0]
+    assert bytes(blocks[18:]) == bytes(int(t, 16) for t in g["block_b_bytes"].split())
+    q = np.array([int(t) for t in g["block_b_q"].split()], dtype=np.float32)
+    np.testing.assert_array_equal(oracle.dequantize_q4_0(blocks[18:], 32)[0], q * 0.5)
+    x = np.ones((1, 64), np.float32)
+    q8 = oracle.quantize_q8_0(x)
+    np.testing.assert_array_equal(oracle.block_isums(blocks, q8, 64, 1, 1)[0, 0],
+                                  [int(g["isum_a"]), int(g["isum_b"])])
+    dst, scale = oracle.mul_mat(blocks, 64, 1, x)
+    assert dst[0, 0] == np.float32(float(g["dst"]))
+    assert scale[0, 0] == float(g["scale"])
+    # the same through the already-quantized entry point, and with the blocks swapped
+    dst2, scale2 = oracle.mul_mat_q8(blocks, 64, 1, q8, 1)
+    assert dst2[0, 0] == dst[0, 0] and scale2[0, 0] == scale[0, 0]
+    swapped = np.concatenate([blocks[18:], blocks[:18]])
+    dst3, scale3 = oracle.mul_mat(swapped, 64, 1, x)
+    assert dst3[0, 0] == dst[0, 0] and scale3[0, 0] == scale[0, 0]
+
+
+def test_tolerance_scale_closed_forms():
+    # Where every block term has the same sign, S = |dst| up to dst's fp32 rounding.
+    rng = np.random.default_rng(17)
+    w = np.abs(rng.standard_normal((6, 256))).astype(np.float32)
+    x = np.abs(rng.standard_normal((3, 256))).astype(np.float32)
+    dst, scale = oracle.mul_mat(oracle.quantize_q4_0(w), 256, 6, x)
+    assert np.all(np.abs(np.abs(dst) - scale) <= 8 * 2.0 ** -24 * scale)
+    # A row whose second block repeats the first while the activations of the second
+    # block are the negated first ones: Q8_0 quantization is symmetric (round half
+    # away from zero, scale from |x|), so isum_b = -isum_a and the two terms cancel
+    # exactly: dst = 0 while S is twice one block's term.
+    wa = (rng.standard_normal((4, 32)) * 0.02).astype(np.float32)
+    xa = rng.standard_normal((3, 32)).astype(np.float32)
+    rows = oracle.quantize_q4_0(np.concatenate([wa, wa], axis=1))
+    xx = np.concatenate([xa, -xa], axis=1)
+    isums = oracle.block_isums(rows, oracle.quantize_q8_0(xx), 64, 4, 3)
+    np.testing.assert_array_equal(isums[..., 1], -isums[..., 0])
+    d, s = oracle.mul_mat(rows, 64, 4, xx)
+    single_d, single_s = oracle.mul_mat(oracle.quantize_q4_0(wa), 32, 4, xa)
+    assert np.all(d == 0.0)
+    np.testing.assert_array_equal(s, 2 * single_s)
+    # one block: S is |d * isum| in fp64, dst the same product rounded once to fp32
+    assert np.all(np.abs(single_s - np.abs(single_d)) <= 2.0 ** -24 * single_s)
+
 # -------------------------------------------------------------------- fp16 --
 
 def _fp32_patterns(rng):
@@ -233,6 +285,19 @@ def test_half_away_from_zero_rounding():
     deq = oracle.dequantize_q4_0(b, 32)[0] / d
     np.testing.assert_array_equal(deq[1:7], [3, -3, 2, -2, 1, -1])
 
+
+
+def test_q8_0_half_away_from_zero_rounding():
+    # Q8_0 with amax = 127 s (s a power of two) has d32 = s exactly, so elements at
+    # (k + 1/2) s are exact ties: they round away from zero (roundf), not to even.
+    s = np.float32(2.0 ** -5)
+    vals = np.zeros(32, np.float32)
+    vals[0] = 127 * s
+    ties = np.array([2.5, -2.5, 1.5, -1.5, 0.5, -0.5, 126.5, -126.5], np.float32)
+    vals[1:9] = ties * s
+    q = oracle.quantize_q8_0(vals.reshape(1, 32))[0]
+    assert int.from_bytes(bytes(q[:2]), "little") == 0x2800          # fp16 2^-5
+    np.testing.assert_array_equal(q[3:11].view(np.int8), [3, -3, 2, -2, 1, -1, 127, -127])
 
 # ---------------------------------------------------------- brute force --
 

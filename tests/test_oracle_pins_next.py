@@ -15,6 +15,7 @@ with plain Python loops.  Sources:
   * Q8_0 weights: the Q8_0 type of §2's type table in the contraction of §3.
 """
 import math
+import os
 
 import numpy as np
 import pytest
@@ -212,3 +213,36 @@ def test_w8_isum_brute_force_tiny():
     yb = np.zeros(34, np.uint8)
     yb[2:] = np.int8(127).view(np.uint8)
     assert oracle.block_isums_w8(xa, yb, 32, 1, 1)[0, 0, 0] == -32 * 127 * 127
+
+
+def _golden(name):
+    out = {}
+    with open(os.path.join(os.path.dirname(__file__), "golden", name), encoding="utf-8") as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                k, v = line.split("=", 1)
+                out[k.strip()] = v.strip()
+    return out
+
+
+def test_w8_two_block_tolerance_scale():
+    # The Q8_0-weight contraction's tolerance scale on a hand-worked row whose two
+    # block sums have opposite signs (tests/golden/two_block_scale.txt): S sums the
+    # absolute block terms, dst keeps the sign of their sum.
+    g = _golden("two_block_scale.txt")
+    w = np.zeros((1, 64), np.float32)
+    w[0, 0] = 127.0 / 128.0
+    w[0, 32] = -127.0 / 256.0
+    x = np.zeros((1, 64), np.float32)
+    x[0, 0] = x[0, 32] = 127.0 / 128.0
+    wq = oracle.quantize_q8_0(w)
+    assert int.from_bytes(bytes(wq[0, :2]), "little") == 0x2000          # 2^-7
+    assert int.from_bytes(bytes(wq[0, 34:36]), "little") == 0x1C00       # 2^-8
+    isums = oracle.block_isums_w8(wq, oracle.quantize_q8_0(x), 64, 1, 1)[0, 0]
+    np.testing.assert_array_equal(isums, [int(g["w8_isum_a"]), int(g["w8_isum_b"])])
+    dst, scale = oracle.mul_mat_w8(wq, 64, 1, x)
+    assert dst[0, 0] == np.float32(float(g["w8_dst"]))
+    assert scale[0, 0] == float(g["w8_scale"])
+    d2, s2 = oracle.mul_mat_w8_q8(wq, 64, 1, oracle.quantize_q8_0(x), 1)
+    assert d2[0, 0] == dst[0, 0] and s2[0, 0] == scale[0, 0]
