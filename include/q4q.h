@@ -26,7 +26,9 @@
  *    and nothing is launched.  A failed launch returns Q4Q_ERR_CUDA.  Kernels
  *    that wait on asynchronous copies bound every wait (about one second); a
  *    wait that runs out records Q4Q_ERR_TIMEOUT in a device status word that
- *    q4q_device_status() returns (and clears), and the kernel returns early.
+ *    q4q_device_status() returns (and clears), and that call's kernel returns
+ *    early, leaving its output incomplete.  The abort is scoped to the call:
+ *    later calls run normally whether or not the word has been read.
  *  - Empty problems (ne01 == 0 or ne11 == 0, or nrows == 0) are valid and launch
  *    nothing.
  *  - Out of contract (not checked): non-finite inputs, and inputs whose block
@@ -95,10 +97,12 @@ Q4Q_API q4q_status q4q_quantize_q8_0(const float* src, void* dst, int64_t ncols,
 
 /* Bytes of device workspace q4q_mul_mat wants for this problem (0 when the
  * chosen kernel needs none).  The answer depends only on the shapes and on the
- * current device.  For the tensor-core path it includes room for the fp32
- * partial sums of split-K (used when the output tiles alone leave SMs idle: few
- * tokens or few rows), at most ne11 * ne01 * 4 * ne00 / 512 bytes on top of
- * ne11 * (2 * ne00 + 4 * ne00 / 32) + 4096. */
+ * current device.  The tensor-core path (ne11 >= 8) runs in
+ *   B = round_up(2 * ne00 * ne11, 256) + (ne00 / 32) * round_up(ne11, 128) * 4 + 256
+ * bytes (fp16 activation codes, block scales, a control word); the size returned
+ * adds room for the fp32 partial sums of split-K (used when the output tiles alone
+ * leave SMs idle: few tokens or few rows): round_up(s * ne01 * ne11 * 4, 256) for
+ * s <= ne00 / 512 splits.  The generic path needs (ne00 / 32) * ne11 * 34 bytes. */
 Q4Q_API q4q_status q4q_mul_mat_workspace_size(int64_t ne00, int64_t ne01, int64_t ne11, size_t* bytes);
 
 /* ggml_mul_mat(src0 Q4_0 [ne00, ne01], src1 F32 [ne10, ne11]) -> dst F32 [ne01, ne11]
@@ -111,8 +115,8 @@ Q4Q_API q4q_status q4q_mul_mat_workspace_size(int64_t ne00, int64_t ne01, int64_
  * ne11 < 8 streams the weights once through a fused GEMV (no workspace);
  * ne11 >= 8 runs the tensor-core GEMM on 256-byte-aligned workspace: with
  * q4q_mul_mat_workspace_size(...) bytes it splits K as planned; with less (down to
- * ne11 * (2 * ne00 + 4 * ne00 / 32) rounded, its split-free minimum) it uses fewer
- * splits, each split's partial sums being added in a fixed order.
+ * its split-free minimum B, see q4q_mul_mat_workspace_size) it uses fewer splits,
+ * each split's partial sums being added in a fixed order.
  * Limits: 0 < ne00 < 2^20 (ne00 % 32 == 0), 0 <= ne01 < 2^31, 0 <= ne11 < 2^20. */
 Q4Q_API q4q_status q4q_mul_mat(const void* src0, int64_t ne00, int64_t ne01,
                        const float* src1, int64_t ne10, int64_t ne11,
@@ -263,8 +267,11 @@ Q4Q_API q4q_status q4q_debug_block_isums_q8_0(const void* src0_q8_0, const void*
  * counterpart to this call; it exists for callers such as a plugin inside a host
  * application that owns every device allocation (an inference server with its
  * own memory pool, a runtime that forbids allocation after start-up) and so has
- * no workspace to pass.  It computes exactly what q4q_mul_mat computes, with the
- * same arguments minus the workspace, and allocates nothing: the scratch space
+ * no workspace to pass.  It computes what q4q_mul_mat computes, with the same
+ * arguments minus the workspace -- the same result within the library's output
+ * bound (1e-5 of sum_b |d_w d_x isum_b|; the tensor-core path may split K fewer
+ * ways than with a full workspace, which changes the fp32 summation order) --
+ * and allocates nothing: the scratch space
  * that the tensor-core and generic paths need comes from one static device array
  * of Q4Q_NOALLOC_SCRATCH_BYTES that the library owns on every GPU that loads it,
  * until the process exits.
@@ -274,7 +281,9 @@ Q4Q_API q4q_status q4q_debug_block_isums_q8_0(const void* src0_q8_0, const void*
  *    not fit at ne00 = 4096); others use as many K splits as the array holds.
  *  - Set-up: the first call on a device, made while that device is current,
  *    looks up the array's device address (cudaGetSymbolAddress) and caches it;
- *    make that first call before any stream capture.
+ *    make that first call before any stream capture.  A device reset
+ *    (cudaDeviceReset) discards the array and with it the cached address: after
+ *    one, the process must not call q4q_mul_mat_noalloc on that device again.
  *  - Sharing: every call on a device uses the same array, which keeps whatever
  *    the last call left in it (no call needs it to start at zero: each call
  *    rewrites every scratch byte it reads).  Calls that overlap on the GPU (on
@@ -326,8 +335,29 @@ Q4Q_API q4q_status q4q_debug_mma_splits(int64_t ne00, int64_t ne01, int64_t ne11
  * stays usable.  limit_ns: 1 .. 1e9, else Q4Q_ERR_ARG. */
 Q4Q_API q4q_status q4q_debug_wait_timeout(uint64_t limit_ns, q4q_stream_t stream);
 
+/* Debug: the failure path of the matmul kernels' own bounded waits.  Runs the
+ * kernel q4q_mul_mat would run for this problem -- path 0: the GEMV (ne11 1..7),
+ * path 1: the tensor-core GEMM (ne11 >= 8) -- with every wait bounded by limit_ns
+ * nanoseconds and one hand-off left out in its first CTA: that CTA's first stage
+ * of weights (GEMV) or of activations (GEMM) is never copied, so the waits on it
+ * run out.  The CTA that gives up records Q4Q_ERR_TIMEOUT in the device status
+ * word (read by q4q_device_status) and raises the call's abort; it and every CTA
+ * of the call that then finds the abort raised wait (bounded) for their own copies
+ * in flight, free their tensor memory and return.  No GPU fault or hang is
+ * involved and the context stays usable; dst is left incomplete.  Arguments as
+ * q4q_mul_mat (path 1: its workspace); the problem must take the chosen path
+ * (ne00 % 256 == 0, 16-byte aligned src0 and src1), else Q4Q_ERR_SHAPE.
+ * limit_ns: 1 .. 1e9, path: 0 or 1, else Q4Q_ERR_ARG. */
+Q4Q_API q4q_status q4q_debug_mul_mat_timeout(const void* src0, int64_t ne00, int64_t ne01, const float* src1,
+                                     int64_t ne11, float* dst, void* workspace, size_t workspace_bytes,
+                                     int path, uint64_t limit_ns, q4q_stream_t stream);
+
 /* Synchronizes the device, returns (in *status) the first device-side error
- * recorded since the last call (Q4Q_OK if none) and clears it. */
+ * recorded since the last call (Q4Q_OK if none) and clears it.  This is where a
+ * bounded wait that ran out (Q4Q_ERR_TIMEOUT) or an out-of-range row id of
+ * q4q_get_rows_* (Q4Q_ERR_ARG) is reported: the call whose kernel recorded it has
+ * already returned, and its output is incomplete.  A recorded error does not
+ * affect later calls. */
 Q4Q_API q4q_status q4q_device_status(q4q_status* status);
 
 /* Static string for a status code. */

@@ -11,6 +11,7 @@ The operation is ggml_mul_mat(Q4_0 weights, F32 activations) as described in
 from __future__ import annotations
 
 import ctypes
+import functools
 from typing import Optional
 
 import torch
@@ -45,6 +46,31 @@ class Q4QError(RuntimeError):
 def _check(fn: str, status: int):
     if status != 0:
         raise Q4QError(fn, status)
+
+
+def _first_cuda_device(values):
+    for v in values:
+        if isinstance(v, torch.Tensor) and v.is_cuda:
+            return v.device
+        if isinstance(v, (list, tuple)):
+            d = _first_cuda_device(v)
+            if d is not None:
+                return d
+    return None
+
+
+def _on_tensor_device(fn):
+    """Run a wrapper with the device of its first CUDA tensor argument current: the
+    library plans for, allocates on and launches on the current device (and the
+    default stream is that device's current stream)."""
+    @functools.wraps(fn)
+    def wrapper(*args, **kwargs):
+        dev = _first_cuda_device(list(args) + list(kwargs.values()))
+        if dev is None:
+            return fn(*args, **kwargs)
+        with torch.cuda.device(dev):
+            return fn(*args, **kwargs)
+    return wrapper
 
 
 def _stream(stream) -> Optional[int]:
@@ -82,6 +108,7 @@ def q4q_status_string(status: int) -> str:
     return _lib.load().q4q_status_string(int(status)).decode()
 
 
+@_on_tensor_device
 def _quantize(fn: str, src: torch.Tensor, dst: Optional[torch.Tensor], row_bytes, stream):
     if src.dtype != torch.float32 or src.dim() != 2:
         raise TypeError("src must be a 2-D float32 tensor")
@@ -109,6 +136,7 @@ def q4q_mul_mat_workspace_size(ne00: int, ne01: int, ne11: int) -> int:
     return int(n.value)
 
 
+@_on_tensor_device
 def q4q_mul_mat(src0: torch.Tensor, ne00: int, ne01: int, src1: torch.Tensor,
                 dst: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
                 stream=None, flags: int = 0) -> torch.Tensor:
@@ -150,6 +178,7 @@ Q4Q_MUL_MAT_PDL = 1
 Q4Q_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
+@_on_tensor_device
 def q4q_mul_mat_noalloc(src0: torch.Tensor, ne00: int, ne01: int, src1: torch.Tensor,
                         dst: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """q4q_mul_mat without a workspace, for callers that cannot allocate device
@@ -176,6 +205,7 @@ def q4q_debug_workspace_size(ne00: int, ne11: int, path: int) -> int:
     return int(n.value)
 
 
+@_on_tensor_device
 def q4q_debug_block_isums(src0: torch.Tensor, src1_q8_0: torch.Tensor, ne00: int, ne01: int, ne11: int,
                           path: int = 0, out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
                           stream=None) -> torch.Tensor:
@@ -233,6 +263,7 @@ def _workspace(need: int, workspace: Optional[torch.Tensor], device):
     return None, 0
 
 
+@_on_tensor_device
 def q4q_mul_mat_bias_act(src0: torch.Tensor, ne00: int, ne01: int, src1: torch.Tensor,
                          bias: Optional[torch.Tensor] = None, act: int = Q4Q_ACT_NONE,
                          dst: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
@@ -261,6 +292,7 @@ def q4q_mul_mat_swiglu_workspace_size(ne00: int, ne01: int, ne11: int) -> int:
     return int(n.value)
 
 
+@_on_tensor_device
 def q4q_mul_mat_swiglu(gate: torch.Tensor, up: torch.Tensor, ne00: int, ne01: int, src1: torch.Tensor,
                        dst: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
                        stream=None, flags: int = 0) -> torch.Tensor:
@@ -279,6 +311,7 @@ def q4q_mul_mat_swiglu(gate: torch.Tensor, up: torch.Tensor, ne00: int, ne01: in
     return dst
 
 
+@_on_tensor_device
 def _get_rows(fn: str, row_bytes, src0: torch.Tensor, ne00: int, ne01: int, ids: Optional[torch.Tensor],
               n_ids: Optional[int], dst: Optional[torch.Tensor], stream) -> torch.Tensor:
     if ids is not None:
@@ -316,6 +349,7 @@ def q4q_mul_mat_q8_0_workspace_size(ne00: int, ne01: int, ne11: int) -> int:
     return int(n.value)
 
 
+@_on_tensor_device
 def q4q_mul_mat_q8_0(src0: torch.Tensor, ne00: int, ne01: int, src1: torch.Tensor,
                      dst: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
                      stream=None, flags: int = 0) -> torch.Tensor:
@@ -333,6 +367,7 @@ def q4q_mul_mat_q8_0(src0: torch.Tensor, ne00: int, ne01: int, src1: torch.Tenso
     return dst
 
 
+@_on_tensor_device
 def q4q_debug_block_isums_q8_0(src0_q8_0: torch.Tensor, src1_q8_0: torch.Tensor, ne00: int, ne01: int, ne11: int,
                                path: int = 0, out: Optional[torch.Tensor] = None,
                                workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
@@ -361,6 +396,7 @@ def q4q_mul_mat_group_workspace_size(ne01s, ne00: int, ne11: int) -> int:
     return int(out.value)
 
 
+@_on_tensor_device
 def q4q_mul_mat_group(src0s, ne01s, ne00: int, src1: torch.Tensor, dsts=None,
                       workspace: Optional[torch.Tensor] = None, stream=None, flags: int = 0):
     """[ggml_mul_mat(src0s[m] (Q4_0 [ne00, ne01s[m]]), src1) for m] in one call: F32 [ne11, ne01s[m]] each."""
@@ -386,3 +422,22 @@ def q4q_debug_wait_timeout(limit_ns: int, stream=None) -> None:
     """Run the library's bounded-wait failure path on its own: one wait that nothing
     completes, given up after limit_ns; q4q_device_status() then reports Q4Q_ERR_TIMEOUT (6)."""
     _check("q4q_debug_wait_timeout", _lib.load().q4q_debug_wait_timeout(int(limit_ns), _stream(stream)))
+
+
+@_on_tensor_device
+def q4q_debug_mul_mat_timeout(src0: torch.Tensor, ne00: int, ne01: int, src1: torch.Tensor, path: int,
+                              limit_ns: int, dst: Optional[torch.Tensor] = None,
+                              workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Run the matmul kernel of `path` (0 = GEMV, 1 = tensor-core GEMM) with one hand-off
+    left out in its first CTA and every wait bounded by limit_ns: the waits run out,
+    q4q_device_status() then reports Q4Q_ERR_TIMEOUT (6), and dst is incomplete."""
+    x = _acts_2d(src1)
+    ne11, ne10 = x.shape
+    if dst is None:
+        dst = torch.empty((ne11, ne01), dtype=torch.float32, device=x.device)
+    need = q4q_mul_mat_workspace_size(ne00, ne01, ne11) if path == 1 else 0
+    ws_ptr, ws_bytes = _workspace(need, workspace, x.device)
+    _check("q4q_debug_mul_mat_timeout", _lib.load().q4q_debug_mul_mat_timeout(
+        _dev(src0, "src0", ne01 * q4_0_row_bytes(ne00)), ne00, ne01, _dev(x, "src1"), ne11,
+        _dev(dst, "dst", 4 * ne01 * ne11), ws_ptr, ws_bytes, int(path), int(limit_ns), _stream(stream)))
+    return dst

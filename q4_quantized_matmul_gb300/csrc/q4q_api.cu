@@ -161,6 +161,31 @@ extern "C" q4q_status q4q_debug_wait_timeout(uint64_t limit_ns, q4q_stream_t str
     return launch_wait_timeout(limit_ns, (cudaStream_t)stream);
 }
 
+extern "C" q4q_status q4q_debug_mul_mat_timeout(const void* src0, int64_t ne00, int64_t ne01, const float* src1,
+                                                int64_t ne11, float* dst, void* workspace, size_t workspace_bytes,
+                                                int path, uint64_t limit_ns, q4q_stream_t stream_) {
+    if (path != 0 && path != 1) return Q4Q_ERR_ARG;
+    if (limit_ns == 0 || limit_ns > WAIT_LIMIT_NS) return Q4Q_ERR_ARG;
+    q4q_status st = check_mul_mat_shapes(ne00, ne01, ne00, ne11);
+    if (st != Q4Q_OK) return st;
+    if (ne01 == 0 || ne11 == 0) return Q4Q_ERR_SHAPE;
+    if (!src0 || !src1 || !dst) return Q4Q_ERR_NULL;
+    DeviceInfo info;
+    if ((st = current_device_info(&info)) != Q4Q_OK) return st;
+    cudaStream_t stream = (cudaStream_t)stream_;
+    const KernelDebug dbg{limit_ns, 1};
+    if (path == 0) {
+        if (ne11 >= 8 || !gemv_supported(src0, ne00, ne01, src1, ne11, info)) return Q4Q_ERR_SHAPE;
+        return gemv_mul_mat(src0, ne00, ne01, src1, ne11, dst, stream, info, false, &dbg);
+    }
+    if (ne11 < 8 || !mma_supported(ne00, ne01, ne11, info) || !aligned(src0, 16) || !aligned(src1, 16))
+        return Q4Q_ERR_SHAPE;
+    if (workspace_bytes < mma_workspace_bytes(ne00, ne11)) return Q4Q_ERR_WORKSPACE;
+    if (!workspace) return Q4Q_ERR_NULL;
+    if (!aligned(workspace, 256)) return Q4Q_ERR_ALIGN;
+    return mma_mul_mat(src0, ne00, ne01, src1, ne11, dst, workspace, workspace_bytes, stream, info, false, &dbg);
+}
+
 extern "C" q4q_status q4q_device_status(q4q_status* status) {
     if (!status) return Q4Q_ERR_NULL;
     if (cudaDeviceSynchronize() != cudaSuccess) return Q4Q_ERR_CUDA;

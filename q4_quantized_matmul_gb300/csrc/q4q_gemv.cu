@@ -107,9 +107,13 @@ bool gemv_supported(const void* src0, int64_t ne00, int64_t ne01, const float* s
 }
 
 q4q_status gemv_mul_mat(const void* src0, int64_t ne00, int64_t ne01, const float* src1, int64_t ne11,
-                        float* dst, cudaStream_t stream, const DeviceInfo& info, bool pdl) {
+                        float* dst, cudaStream_t stream, const DeviceInfo& info, bool pdl, const KernelDebug* dbg) {
     GemvPlan plan;
     if (!plan_gemv(ne00, ne01, ne11, info, &plan)) return Q4Q_ERR_SHAPE;
+    if (dbg) {
+        plan.p.limit_ns = dbg->limit_ns;
+        plan.p.fault = dbg->fault;
+    }
     const GemvArgs a{static_cast<const uint8_t*>(src0), nullptr, src1, dst, nullptr, Q4Q_ACT_NONE, GemvGroup{}};
     return launch_gemv<WQ4_0, M_SINGLE>(plan, ne11, a, stream, info.device, pdl);
 }

@@ -77,6 +77,8 @@ struct GemvParams {
     int act;           // Q4Q_ACT_* applied to every output (after the bias)
     const float* bias; // [ne01] added to every output row, or null
     GemvGroup grp;     // group mode only
+    uint64_t limit_ns; // bound of every wait (WAIT_LIMIT_NS unless a test asks for less)
+    int fault;         // test only: 1 = CTA 0 leaves out its first unit's copies
 };
 
 // The rows a unit covers: its matrix's weights, output and row count, and its
@@ -424,13 +426,16 @@ __device__ __forceinline__ void gemv_body(const uint8_t* __restrict__ w, const u
                 const int s = k % p.S;
                 if (k >= p.S) {
                     const uint32_t bar = empty0 + 8 * s, par = ((k / p.S) + 1) & 1;
-                    const bool ok = mbar_wait_until(bar, par, abort_flag, WAIT_LIMIT_NS);
+                    const bool ok = mbar_wait_until(bar, par, abort_flag, p.limit_ns);
                     if (!ok) {
                         if (!*abort_flag) record_error(&g_gemv_status, DEV_TIMEOUT);
                         *abort_flag = 1;
                         break;
                     }
                 }
+                // test only: CTA 0 leaves out its first unit (no expected bytes, no copy), so
+                // that stage never completes and the consumers' bounded waits run out
+                if (p.fault && k == 0 && blockIdx.x == 0) continue;
                 const UnitRows ur = unit_rows<MODE>(p, w, dst, u);
                 const int r0 = ur.r0;
                 const int nr = min(p.G, ur.rows - r0);
@@ -442,11 +447,11 @@ __device__ __forceinline__ void gemv_body(const uint8_t* __restrict__ w, const u
                     bulk_g2s(smem_u32(stages + (size_t)s * p.stage_bytes + p.half_off),
                              w2 + (int64_t)r0 * p.row_bytes, bytes, full0 + 8 * s);
             }
-            if (*abort_flag) {
-                // let the copies still in flight land before the CTA exits
-                for (int k2 = max(0, k - p.S); k2 < k; ++k2)
-                    mbar_wait_bounded(full0 + 8 * (k2 % p.S), (uint32_t)((k2 / p.S) & 1), WAIT_LIMIT_NS);
-            }
+            // let every copy issued land before the CTA can exit: consumers that gave up
+            // no longer wait for them (the unit a test leaves out never lands)
+            for (int k2 = max(0, k - p.S); k2 < k; ++k2)
+                if (!(p.fault && k2 == 0 && blockIdx.x == 0))
+                    mbar_wait_bounded(full0 + 8 * (k2 % p.S), (uint32_t)((k2 / p.S) & 1), p.limit_ns);
         }
         return;
     }
@@ -532,7 +537,7 @@ __device__ __forceinline__ void gemv_body(const uint8_t* __restrict__ w, const u
             const uint32_t bar = full0 + 8 * s, par = (uint32_t)((k / p.S) & 1);
             int ok = 1;
             if (lane == 0) {
-                const bool got = mbar_wait_until(bar, par, abort_flag, WAIT_LIMIT_NS);
+                const bool got = mbar_wait_until(bar, par, abort_flag, p.limit_ns);
                 if (!got) {
                     if (!*abort_flag) record_error(&g_gemv_status, DEV_TIMEOUT);
                     *abort_flag = 1;
@@ -748,6 +753,8 @@ bool plan_gemv(int64_t ne00, int64_t ne01, int64_t ne11, const DeviceInfo& info,
     p.act = Q4Q_ACT_NONE;
     p.bias = nullptr;
     p.grp = GemvGroup{};
+    p.limit_ns = WAIT_LIMIT_NS;
+    p.fault = 0;
     plan->smem = (size_t)(head + act_bytes + S * stage);
     plan->lpr = lpr;
     const int per_sm = (!small && plan->smem <= 113 * 1024 && two_per_sm) ? 2 : 1;

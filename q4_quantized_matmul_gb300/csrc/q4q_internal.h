@@ -24,6 +24,14 @@ q4q_status launch_status();
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Test-only knobs of one matmul launch (q4q_debug_mul_mat_timeout); the normal
+// path passes none, which means every wait is bounded by WAIT_LIMIT_NS and no
+// hand-off is left out.
+struct KernelDebug {
+    uint64_t limit_ns;   // bound of every wait of the launch
+    int fault;           // 1: the first CTA leaves out one hand-off (its first stage)
+};
+
 // device status words of the translation units that wait on async copies
 unsigned int gemv_take_device_status();
 unsigned int mma_take_device_status();
@@ -37,7 +45,7 @@ size_t mma_workspace_bytes_split(int64_t ne00, int64_t ne01, int64_t ne11, const
 // q8_weights: src0 holds Q8_0 blocks instead of Q4_0 ones
 q4q_status mma_mul_mat(const void* src0, int64_t ne00, int64_t ne01, const float* src1, int64_t ne11,
                        float* dst, void* workspace, size_t workspace_bytes, cudaStream_t stream,
-                       const DeviceInfo& info, bool q8_weights = false);
+                       const DeviceInfo& info, bool q8_weights = false, const KernelDebug* dbg = nullptr);
 q4q_status mma_debug_isums(const void* src0, const void* src1_q8_0, int64_t ne00, int64_t ne01,
                            int64_t ne11, int32_t* out, void* workspace, size_t workspace_bytes,
                            cudaStream_t stream, const DeviceInfo& info, bool q8_weights = false);
@@ -46,7 +54,8 @@ q4q_status mma_debug_isums(const void* src0, const void* src1_q8_0, int64_t ne00
 bool gemv_supported(const void* src0, int64_t ne00, int64_t ne01, const float* src1, int64_t ne11,
                     const DeviceInfo& info);
 q4q_status gemv_mul_mat(const void* src0, int64_t ne00, int64_t ne01, const float* src1, int64_t ne11,
-                        float* dst, cudaStream_t stream, const DeviceInfo& info, bool pdl);
+                        float* dst, cudaStream_t stream, const DeviceInfo& info, bool pdl,
+                        const KernelDebug* dbg = nullptr);
 
 // the same GEMV with the bias / activation epilogue (q4q_gemv_epi.cu)
 unsigned int gemv_epi_take_device_status();

@@ -24,8 +24,12 @@
 // K order inside every 8-element group is permuted the same way on both operands
 // ([0,4,1,5,2,6,3,7]) so that a 32-bit word of nibbles turns into fp16 with a
 // handful of bit operations; the dot product does not depend on that order.
-// Every mbarrier wait is bounded; a wait that runs out records Q4Q_ERR_TIMEOUT and
-// the CTA winds down (waits for its own copies, frees its TMEM) and returns.
+// Every mbarrier wait is bounded; a wait that runs out records Q4Q_ERR_TIMEOUT in the
+// library's status word, raises the call's abort word (in the workspace, zeroed by
+// the activation kernel that precedes every GEMM launch, so an old timeout never
+// reaches a later call), and the CTA winds down (waits for its own copies, frees its
+// TMEM) and returns.  Other CTAs of the same call that find the abort word raised
+// while they wait wind down the same way.
 #include <algorithm>
 #include <atomic>
 #include <cuda.h>
@@ -39,6 +43,9 @@ namespace q4q {
 namespace {
 
 __device__ unsigned int g_mma_status = 0;
+
+// Bytes at the end of the GEMM's workspace operands that hold the call's abort word.
+constexpr size_t CTRL_BYTES = 256;
 
 constexpr int BM = 128;                 // weight rows per CTA tile (MMA M)
 constexpr int KRAW = 256;               // K per raw-weight stage (8 blocks per row)
@@ -146,19 +153,29 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
     return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// bounded wait that also gives up as soon as another role has aborted
-__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+// What a bounded wait looks at besides its barrier: the CTA's abort flag (shared
+// memory), the call's abort word (global memory) and the time limit.
+struct Waiter {
+    volatile int* flag;
+    volatile unsigned int* word;
+    uint64_t limit_ns;
+};
+
+// bounded wait that also gives up as soon as another role of the CTA, or another CTA
+// of the same call, has aborted
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, const Waiter& w) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
         if (mbar_try_wait_sleep(bar, parity, SLEEP_HINT_NS)) return true;
-        if (*abort_flag) return false;
-        if (*reinterpret_cast<volatile unsigned int*>(&g_mma_status) != 0) {   // another CTA gave up
-            *abort_flag = 1;
+        if (*w.flag) return false;
+        if (*w.word != 0) {   // another CTA of this call gave up
+            *w.flag = 1;
             return false;
         }
-        if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
-            *abort_flag = 1;
+        if (global_timer_ns() - t0 > w.limit_ns) {
+            *w.flag = 1;
+            atomicExch(const_cast<unsigned int*>(w.word), 1u);
             record_error(&g_mma_status, DEV_TIMEOUT);
             return false;
         }
@@ -168,9 +185,8 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
 // Every lane polls the barrier itself (each gets its own acquire of the completed
 // phase, which cannot advance before this warp arrives on the matching "empty"
 // barrier); a single vote makes the verdict warp-uniform.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int lane) {
-    (void)lane;
-    const bool ok = mbar_try_wait(bar, parity) || wait_or_abort(bar, parity, abort_flag);
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Waiter& w) {
+    const bool ok = mbar_try_wait(bar, parity) || wait_or_abort(bar, parity, w);
     return __all_sync(0xffffffffu, ok);
 }
 
@@ -225,7 +241,11 @@ struct MmaParams {
     float* dst;           // [N][M]; with splits > 1 the partial sums go to dst + z * N * M
     const float* dx;      // [nb][Npad]
     int32_t* isums;       // debug: [N][M][nb]
+    unsigned int* abort_word;   // this call's abort word (workspace; zero at launch)
+    uint64_t limit_ns;    // bound of every wait
+    int fault;            // test only: 1 = CTA (0, 0, 0) leaves out its first activation stage
 };
+
 
 __device__ __forceinline__ uint64_t pack2(float x, float y) {
     uint64_t r;
@@ -312,6 +332,7 @@ mma_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
     const uint32_t drain = slab_full + 16 * NBUF;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 16);
+    const Waiter wt{abort_flag, p.abort_word, p.limit_ns};
     float* dw_s = reinterpret_cast<float*>(smem + C::OFF_DW);
     const float* dx_s = reinterpret_cast<const float*>(smem + C::OFF_DX);
 
@@ -357,14 +378,15 @@ mma_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
             int r = 0;
             for (; r < n_raw; ++r) {
                 const int st = r % RAW_STAGES;
-                if (r >= RAW_STAGES && !wait_or_abort(raw_empty + 8 * st, ((r / RAW_STAGES) + 1) & 1, abort_flag)) break;
+                if (r >= RAW_STAGES && !wait_or_abort(raw_empty + 8 * st, ((r / RAW_STAGES) + 1) & 1, wt)) break;
                 mbar_arrive_expect_tx(raw_full + 8 * st, RAW_BYTES);
                 tma_load_2d(sbase + C::OFF_RAW + st * RAW_BYTES, &tmap_w, (r_begin + r) * (C::RAW_ROW / raw_elem_bytes(WT)), m0,
                             raw_full + 8 * st);
             }
-            if (*abort_flag)   // let the loads already issued land before the CTA exits
-                for (int r2 = max(0, r - RAW_STAGES); r2 < r; ++r2)
-                    mbar_wait_bounded(raw_full + 8 * (r2 % RAW_STAGES), (r2 / RAW_STAGES) & 1, WAIT_LIMIT_NS);
+            // let every load issued land before the CTA can exit: consumers that gave up
+            // (this CTA's or another's abort) no longer wait for them
+            for (int r2 = max(0, r - RAW_STAGES); r2 < r; ++r2)
+                mbar_wait_bounded(raw_full + 8 * (r2 % RAW_STAGES), (r2 / RAW_STAGES) & 1, p.limit_ns);
         }
     } else if (warp == 2) {
         // ---------------- activation tile + activation scale producer
@@ -372,7 +394,10 @@ mma_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
             int i = 0;
             for (; i < n_ab; ++i) {
                 const int s = i % AB_STAGES;
-                if (i >= AB_STAGES && !wait_or_abort(ab_empty + 8 * s, ((i / AB_STAGES) + 1) & 1, abort_flag)) break;
+                if (i >= AB_STAGES && !wait_or_abort(ab_empty + 8 * s, ((i / AB_STAGES) + 1) & 1, wt)) break;
+                // test only: the first CTA leaves out its first stage (no expected bytes, no
+                // copies), so that stage never completes and every role's bounded wait runs out
+                if (p.fault && i == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) continue;
                 const uint32_t bar = ab_full + 8 * s;
                 mbar_arrive_expect_tx(bar, C::B_BYTES + C::DX_BYTES);
                 tma_load_2d(sbase + C::OFF_B + s * C::B_STRIDE, &tmap_b, (ab_begin + i) * KAB, n0, bar);
@@ -380,9 +405,10 @@ mma_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                 bulk_g2s(dxd, p.dx + (size_t)(2 * (ab_begin + i)) * p.Npad + n0, NT * 4, bar);
                 bulk_g2s(dxd + NT * 4, p.dx + (size_t)(2 * (ab_begin + i) + 1) * p.Npad + n0, NT * 4, bar);
             }
-            if (*abort_flag)
-                for (int i2 = max(0, i - AB_STAGES); i2 < i; ++i2)
-                    mbar_wait_bounded(ab_full + 8 * (i2 % AB_STAGES), (i2 / AB_STAGES) & 1, WAIT_LIMIT_NS);
+            const bool faulted = p.fault && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
+            for (int i2 = max(0, i - AB_STAGES); i2 < i; ++i2)
+                if (!(faulted && i2 == 0))   // the stage left out never completes
+                    mbar_wait_bounded(ab_full + 8 * (i2 % AB_STAGES), (i2 / AB_STAGES) & 1, p.limit_ns);
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer
@@ -403,8 +429,8 @@ mma_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                     const bool ra = mbar_try_wait(ab_full + 8 * s, par_a);
                     const bool re = i < NPAIR || mbar_try_wait(slab_empty + 8 * pr, par_e);
                     if (!(ra && re) &&
-                        (!wait_or_abort(ab_full + 8 * s, par_a, abort_flag) ||
-                         (i >= NPAIR && !wait_or_abort(slab_empty + 8 * pr, par_e, abort_flag)))) {
+                        (!wait_or_abort(ab_full + 8 * s, par_a, wt) ||
+                         (i >= NPAIR && !wait_or_abort(slab_empty + 8 * pr, par_e, wt)))) {
                         ok = false;
                         break;
                     }
@@ -425,13 +451,13 @@ mma_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
             }
             for (int i = 0; i < n_ab && ok && !PAIRWISE; ++i) {
                 const int s = i % AB_STAGES;
-                if (!wait_or_abort(ab_full + 8 * s, (i / AB_STAGES) & 1, abort_flag)) { ok = false; break; }
+                if (!wait_or_abort(ab_full + 8 * s, (i / AB_STAGES) & 1, wt)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t a_base = sbase + C::OFF_A + s * A_BYTES;
                 const uint32_t b_base = sbase + C::OFF_B + s * C::B_STRIDE;
                 for (int j = 0; j < 2; ++j, ++g) {
                     const int buf = g % NBUF;
-                    if (g >= NBUF && !wait_or_abort(slab_empty + 8 * buf, ((g / NBUF) + 1) & 1, abort_flag)) {
+                    if (g >= NBUF && !wait_or_abort(slab_empty + 8 * buf, ((g / NBUF) + 1) & 1, wt)) {
                         ok = false;
                         break;
                     }
@@ -449,7 +475,7 @@ mma_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
             if (!ok) {
                 // no MMA may still be reading shared memory or writing TMEM at exit
                 mma_commit(drain);
-                mbar_wait_bounded(drain, 0, WAIT_LIMIT_NS);
+                mbar_wait_bounded(drain, 0, p.limit_ns);
             }
         }
     } else if (warp >= 4 && warp < 8) {
@@ -460,13 +486,13 @@ mma_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
         bool ok = true;
         for (int r = 0; r < n_raw && ok; ++r) {
             const int st = r % RAW_STAGES;
-            if (!warp_wait(raw_full + 8 * st, (r / RAW_STAGES) & 1, abort_flag, lane)) { ok = false; break; }
+            if (!warp_wait(raw_full + 8 * st, (r / RAW_STAGES) & 1, wt)) { ok = false; break; }
             const uint4* rowp = reinterpret_cast<const uint4*>(smem + C::OFF_RAW + st * RAW_BYTES + t * C::RAW_ROW);
 #pragma unroll
             for (int a = 0; a < KRAW / KAB; ++a) {
                 const int i = r * (KRAW / KAB) + a;
                 const int s = i % AB_STAGES;
-                if (i >= AB_STAGES && !warp_wait(ab_empty + 8 * s, ((i / AB_STAGES) + 1) & 1, abort_flag, lane)) {
+                if (i >= AB_STAGES && !warp_wait(ab_empty + 8 * s, ((i / AB_STAGES) + 1) & 1, wt)) {
                     ok = false;
                     break;
                 }
@@ -536,7 +562,7 @@ mma_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
             for (int g = 0; g < n_slab; ++g) {
                 const int buf = g % NBUF;
                 const int i = g >> 1, s = i % AB_STAGES, j = g & 1;
-                if (!warp_wait(slab_full + 8 * buf, (g / NBUF) & 1, abort_flag, lane)) break;
+                if (!warp_wait(slab_full + 8 * buf, (g / NBUF) & 1, wt)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int c0 = 0; c0 < C::CPW; c0 += 8) {
@@ -584,7 +610,7 @@ mma_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                     const bool ra = mbar_try_wait(bar_a, par_a);
                     const bool rb = mbar_try_wait(bar_b, par_b);
                     if (!__all_sync(0xffffffffu, ra && rb) &&
-                        !(warp_wait(bar_a, par_a, abort_flag, lane) && warp_wait(bar_b, par_b, abort_flag, lane))) {
+                        !(warp_wait(bar_a, par_a, wt) && warp_wait(bar_b, par_b, wt))) {
                         aborted = true;
                         break;
                     }
@@ -645,8 +671,9 @@ mma_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
 // d_x[b][n] (zero for the padding rows n >= N).
 __global__ void __launch_bounds__(256)
 act_to_mma_kernel(const float* __restrict__ x, __half* __restrict__ bmat, float* __restrict__ dx, int K, int N,
-                  int Npad) {
+                  int Npad, unsigned int* __restrict__ abort_word) {
     const int nb = K / QK;
+    if (blockIdx.x == 0 && threadIdx.x == 0) *abort_word = 0u;   // the GEMM launched next starts un-aborted
     const int64_t total = (int64_t)N * nb * 4;
     for (int64_t m0 = (int64_t)blockIdx.x * 256; m0 < total; m0 += (int64_t)gridDim.x * 256) {
         const int64_t m = m0 + threadIdx.x;
@@ -695,8 +722,9 @@ act_to_mma_kernel(const float* __restrict__ x, __half* __restrict__ bmat, float*
 // Public Q8_0 blocks -> the same operands (debug path).
 __global__ void __launch_bounds__(256)
 q8_to_mma_kernel(const uint8_t* __restrict__ yq, __half* __restrict__ bmat, float* __restrict__ dx, int K, int N,
-                 int Npad) {
+                 int Npad, unsigned int* __restrict__ abort_word) {
     const int nb = K / QK;
+    if (blockIdx.x == 0 && threadIdx.x == 0) *abort_word = 0u;
     const int64_t total = (int64_t)N * nb * 4;
     for (int64_t m = (int64_t)blockIdx.x * 256 + threadIdx.x; m < total; m += (int64_t)gridDim.x * 256) {
         const int64_t blk = m >> 2;
@@ -758,6 +786,11 @@ int64_t npad_of(int64_t N) { return (N + NPAD - 1) / NPAD * NPAD; }
 
 size_t b_bytes_of(int64_t K, int64_t N) { return ((size_t)N * K * 2 + 255) / 256 * 256; }
 
+// Workspace of one GEMM call: the fp16 activation operand, the activation scales
+// ([nb][Npad] fp32, a multiple of 512 bytes), then the call's control block (its
+// abort word).  Split-K partial sums, when used, follow.
+size_t ctrl_offset_of(int64_t K, int64_t N) { return b_bytes_of(K, N) + (size_t)(K / QK) * (size_t)npad_of(N) * 4; }
+
 template <int NT, bool DEBUG, int WT>
 q4q_status launch_mma_t(const CUtensorMap& tw, const CUtensorMap& tb, const MmaParams& p, cudaStream_t stream,
                         int device) {
@@ -777,7 +810,8 @@ q4q_status launch_mma_t(const CUtensorMap& tw, const CUtensorMap& tb, const MmaP
 
 template <bool DEBUG, int WT>
 q4q_status run_mma(const void* src0, int64_t ne00, int64_t ne01, int64_t ne11, const __half* bmat, const float* dx,
-                   float* dst, int32_t* isums, int splits, cudaStream_t stream, const DeviceInfo& info) {
+                   unsigned int* abort_word, float* dst, int32_t* isums, int splits, cudaStream_t stream,
+                   const DeviceInfo& info, const KernelDebug* dbg = nullptr) {
     if (!get_encode()) return Q4Q_ERR_CUDA;
     const int NT = pick_nt(ne11);
     const int64_t row_bytes = ne00 / QK * (WT == WQ8_0 ? Q8_0_BYTES : Q4_0_BYTES);
@@ -814,6 +848,9 @@ q4q_status run_mma(const void* src0, int64_t ne00, int64_t ne01, int64_t ne11, c
     p.dst = dst;
     p.dx = dx;
     p.isums = isums;
+    p.abort_word = abort_word;
+    p.limit_ns = dbg ? dbg->limit_ns : WAIT_LIMIT_NS;
+    p.fault = dbg ? dbg->fault : 0;
     switch (NT) {
         case 16: return launch_mma_t<16, DEBUG, WT>(tw, tb, p, stream, info.device);
         case 32: return launch_mma_t<32, DEBUG, WT>(tw, tb, p, stream, info.device);
@@ -838,9 +875,7 @@ bool mma_supported(int64_t ne00, int64_t ne01, int64_t ne11, const DeviceInfo& i
     return std::max(Cfg<128, WQ4_0>::SMEM, Cfg<128, WQ8_0>::SMEM) <= info.max_smem_optin && get_encode();
 }
 
-size_t mma_workspace_bytes(int64_t ne00, int64_t ne11) {
-    return b_bytes_of(ne00, ne11) + (size_t)(ne00 / QK) * (size_t)npad_of(ne11) * 4;
-}
+size_t mma_workspace_bytes(int64_t ne00, int64_t ne11) { return ctrl_offset_of(ne00, ne11) + CTRL_BYTES; }
 
 // Split-K: when the output tiles alone leave most SMs idle (few tokens, few rows),
 // the K loop of every tile is split over blockIdx.z, each split writing fp32 partial
@@ -870,23 +905,27 @@ size_t mma_workspace_bytes_split(int64_t ne00, int64_t ne01, int64_t ne11, const
 
 q4q_status mma_mul_mat(const void* src0, int64_t ne00, int64_t ne01, const float* src1, int64_t ne11, float* dst,
                        void* workspace, size_t workspace_bytes, cudaStream_t stream, const DeviceInfo& info,
-                       bool q8_weights) {
+                       bool q8_weights, const KernelDebug* dbg) {
     const size_t base = mma_workspace_bytes(ne00, ne11);
     if (workspace_bytes < base) return Q4Q_ERR_WORKSPACE;
     // as many K splits as wanted and as the workspace holds partial sums for
     int splits = mma_desired_splits(ne00, ne01, ne11, info);
     while (splits > 1 && base + split_partial_bytes(ne01, ne11, splits) > workspace_bytes) --splits;
+    if (splits < 4) splits = 1;   // 2 or 3 splits measured slower than none (see mma_desired_splits)
     float* part = splits > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + base) : nullptr;
     __half* bmat = static_cast<__half*>(workspace);
     float* dx = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + b_bytes_of(ne00, ne11));
+    unsigned int* abort_word =
+        reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(workspace) + ctrl_offset_of(ne00, ne11));
     const int64_t items = ne11 * (ne00 / QK) * 4;
     const int grid = (int)std::min<int64_t>((items + 255) / 256, (int64_t)info.sm_count * 8);
-    act_to_mma_kernel<<<grid, 256, 0, stream>>>(src1, bmat, dx, (int)ne00, (int)ne11, (int)npad_of(ne11));
+    act_to_mma_kernel<<<grid, 256, 0, stream>>>(src1, bmat, dx, (int)ne00, (int)ne11, (int)npad_of(ne11), abort_word);
     q4q_status st = launch_status();
     if (st != Q4Q_OK) return st;
     float* out = splits > 1 ? part : dst;
-    st = q8_weights ? run_mma<false, WQ8_0>(src0, ne00, ne01, ne11, bmat, dx, out, nullptr, splits, stream, info)
-                    : run_mma<false, WQ4_0>(src0, ne00, ne01, ne11, bmat, dx, out, nullptr, splits, stream, info);
+    st = q8_weights
+             ? run_mma<false, WQ8_0>(src0, ne00, ne01, ne11, bmat, dx, abort_word, out, nullptr, splits, stream, info, dbg)
+             : run_mma<false, WQ4_0>(src0, ne00, ne01, ne11, bmat, dx, abort_word, out, nullptr, splits, stream, info, dbg);
     if (st != Q4Q_OK || splits == 1) return st;
     const int64_t nm = ne01 * ne11;
     const int rgrid = (int)std::max<int64_t>(1, std::min<int64_t>((nm + 255) / 256, (int64_t)info.sm_count * 8));
@@ -906,14 +945,16 @@ q4q_status mma_debug_isums(const void* src0, const void* src1_q8_0, int64_t ne00
     if (!aligned(workspace, 256)) return Q4Q_ERR_ALIGN;
     __half* bmat = static_cast<__half*>(workspace);
     float* dx = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + b_bytes_of(ne00, ne11));
+    unsigned int* abort_word =
+        reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(workspace) + ctrl_offset_of(ne00, ne11));
     const int64_t items = ne11 * (ne00 / QK) * 4;
     const int grid = (int)std::min<int64_t>((items + 255) / 256, (int64_t)info.sm_count * 8);
     q8_to_mma_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint8_t*>(src1_q8_0), bmat, dx, (int)ne00,
-                                               (int)ne11, (int)npad_of(ne11));
+                                               (int)ne11, (int)npad_of(ne11), abort_word);
     q4q_status st = launch_status();
     if (st != Q4Q_OK) return st;
-    return q8_weights ? run_mma<true, WQ8_0>(src0, ne00, ne01, ne11, bmat, dx, nullptr, out, 1, stream, info)
-                      : run_mma<true, WQ4_0>(src0, ne00, ne01, ne11, bmat, dx, nullptr, out, 1, stream, info);
+    return q8_weights ? run_mma<true, WQ8_0>(src0, ne00, ne01, ne11, bmat, dx, abort_word, nullptr, out, 1, stream, info)
+                      : run_mma<true, WQ4_0>(src0, ne00, ne01, ne11, bmat, dx, abort_word, nullptr, out, 1, stream, info);
 }
 
 }  // namespace q4q

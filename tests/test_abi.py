@@ -186,6 +186,18 @@ def test_wait_timeout_argument_errors(lib):
     assert lib.q4q_debug_wait_timeout(2 * 10 ** 9, None) == 7
 
 
+def test_kernel_timeout_entry_argument_errors(lib):
+    P = ctypes.c_void_p
+    fake = P(0x1000)
+    f = lib.q4q_debug_mul_mat_timeout
+    assert f(fake, 256, 4, fake, 1, fake, None, 0, 2, 10 ** 6, None) == 7          # unknown path
+    assert f(fake, 256, 4, fake, 1, fake, None, 0, 0, 0, None) == 7                # limit 0
+    assert f(fake, 256, 4, fake, 1, fake, None, 0, 0, 2 * 10 ** 9, None) == 7      # limit above 1 s
+    assert f(fake, 48, 4, fake, 1, fake, None, 0, 0, 10 ** 6, None) == 2           # ne00 % 32
+    assert f(fake, 256, 0, fake, 1, fake, None, 0, 0, 10 ** 6, None) == 2          # nothing to run
+    assert f(None, 256, 4, fake, 1, fake, None, 0, 0, 10 ** 6, None) == 1
+
+
 def test_c_program_links_and_calls_the_library(lib):
     """A plain C99 caller: includes q4q.h, links libq4q.so and makes the calls that
     need no GPU (version, status strings, argument errors, host-only planning)."""

@@ -169,9 +169,16 @@ def test_mul_mat_bias_act_pdl_chain(q4q):
         outs[flags] = (h.cpu().numpy(), y.cpu().numpy())
     np.testing.assert_array_equal(outs[0][0], outs[q4q.Q4Q_MUL_MAT_PDL][0])
     np.testing.assert_array_equal(outs[0][1], outs[q4q.Q4Q_MUL_MAT_PDL][1])
-    ref_h, _, _ = oracle.mul_mat_epilogue(wfc.cpu().numpy(), 768, 3072, x.cpu().numpy(), bias=bfc.cpu().numpy(),
-                                          act=oracle.ACT_GELU)
-    np.testing.assert_allclose(outs[0][0], ref_h, rtol=1e-4, atol=1e-5)
+    # each step against the oracle on the same input the GPU step read, at the
+    # epilogue's own bar (the matmul's 1e-5 S, one fp32 rounding of the bias add,
+    # GELU's slope and its own error)
+    h_gpu, y_gpu = outs[0]
+    ref_h, pre_h, s_h = oracle.mul_mat_epilogue(wfc.cpu().numpy(), 768, 3072, x.cpu().numpy(), bias=bfc.cpu().numpy(),
+                                                act=oracle.ACT_GELU)
+    e_h = TOL * s_h + 2.0 ** -23 * np.abs(pre_h)
+    _check(h_gpu, ref_h, 1.13 * e_h + 1e-5 * np.abs(ref_h) + 1e-30, "pdl fc")
+    ref_y, pre_y, s_y = oracle.mul_mat_epilogue(wpj.cpu().numpy(), 3072, 768, h_gpu, bias=bpj.cpu().numpy())
+    _check(y_gpu, ref_y, TOL * s_y + 2.0 ** -23 * np.abs(pre_y), "pdl proj")
 
 
 # ------------------------------------------------------------------ SwiGLU --

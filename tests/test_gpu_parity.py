@@ -309,8 +309,8 @@ def test_mul_mat_tensor_core(q4q, ne00, ne01, ne11):
 
 
 def _min_mma_workspace(ne00, ne11):
-    # the split-free minimum of the tensor-core path: fp16 operand + block scales
-    return (ne11 * ne00 * 2 + 255) // 256 * 256 + (ne00 // 32) * ((ne11 + 127) // 128 * 128) * 4
+    # the split-free minimum of the tensor-core path: fp16 operand + block scales + control word
+    return (ne11 * ne00 * 2 + 255) // 256 * 256 + (ne00 // 32) * ((ne11 + 127) // 128 * 128) * 4 + 256
 
 
 @pytest.mark.parametrize("ne00,ne01,ne11,split", [(4096, 1024, 8, True), (4096, 300, 64, True),
@@ -359,11 +359,14 @@ def test_mul_mat_pdl_chain(q4q):
             y = q4q.q4q_mul_mat(ws[i], dims[i], dims[i + 1], y, flags=flags)
         outs[flags] = y.cpu().numpy()
     np.testing.assert_array_equal(outs[0], outs[q4q.Q4Q_MUL_MAT_PDL])
-    # and against the oracle, step by step
-    y = x.cpu().numpy()
+    # and every step against the oracle at the 1e-5 S bar, on the input the GPU step read
+    y = x
     for i in range(3):
-        y, _ = oracle.mul_mat(ws[i].cpu().numpy(), dims[i], dims[i + 1], y)
-    np.testing.assert_allclose(outs[0], y, rtol=1e-4, atol=1e-6)
+        got = q4q.q4q_mul_mat(ws[i], dims[i], dims[i + 1], y, flags=q4q.Q4Q_MUL_MAT_PDL)
+        ref, scale = oracle.mul_mat(ws[i].cpu().numpy(), dims[i], dims[i + 1], y.cpu().numpy())
+        assert_close(got.cpu().numpy(), ref, scale)
+        y = got
+    np.testing.assert_array_equal(y.cpu().numpy(), outs[0])
 
 
 def test_mul_mat_misaligned_weights_take_generic_path(q4q):
@@ -479,4 +482,123 @@ def test_full_size_batched_workloads(q4q, name, ne11):
         ref, scale = oracle.mul_mat(wq_rows, ne00, rows.size, x, nthreads=16)
         assert_close(got[:, rows], ref, scale)
         del wq_d
+    assert q4q.q4q_device_status() == 0
+
+
+# ------------------------------------------------------------ tiny block scales --
+
+def _tiny_scale_rows(rng, levels, nblocks):
+    """Blocks whose scale d32 = amax / levels sits around the smallest fp16 normal
+    (2^-14) and the smallest fp16 subnormal (2^-24, with 2^-25 rounding to zero),
+    blocks whose amax is itself an fp32 subnormal (d32 may underflow to zero; a
+    reciprocal that flushes subnormals gives infinity, so the exact division must
+    decide), and blocks just above the smallest fp32 normal.  Each block holds
+    +-amax, exact ties (k + 1/2) d32 where they are representable, and uniform
+    values."""
+    lo_hi = [(-16.0, -13.0), (-27.0, -23.0), (-149.0 + np.log2(levels), -126.0), (-126.0, -120.0)]
+    exact = [2.0 ** -14, 2.0 ** -24, 2.0 ** -25, 3 * 2.0 ** -26, 2.0 ** -14 * (1 - 2.0 ** -11)]
+    out = np.empty((nblocks, 32), np.float32)
+    for i in range(nblocks):
+        if i < len(exact) * 4:
+            d = exact[i % len(exact)]
+            amax = np.float32(d * levels)
+        else:
+            lo, hi = lo_hi[i % len(lo_hi)]
+            amax = np.float32(2.0 ** rng.uniform(lo, hi) * (levels if hi > -126.0 else 1.0))
+        d32 = np.float32(amax / np.float32(levels))
+        blk = (rng.uniform(-1.0, 1.0, 32) * np.float64(amax)).astype(np.float32)
+        blk[rng.integers(0, 32)] = amax if rng.random() < 0.5 else -amax
+        if d32 > 0:
+            k = rng.integers(-levels, levels, size=6) + 0.5
+            t = (k * np.float64(d32)).astype(np.float32)
+            ok = (np.abs(t) <= amax) & (t.astype(np.float64) == k * np.float64(d32))
+            blk[1:7][ok] = t[ok]
+        out[i] = blk
+    return out
+
+
+@pytest.mark.parametrize("kind", ["q4_0", "q8_0"])
+def test_quantize_tiny_scales_bit_exact(q4q, kind):
+    import ctypes
+    levels = 8 if kind == "q4_0" else 127
+    rng = np.random.default_rng(71 + levels)
+    w = _tiny_scale_rows(rng, levels, 4096).reshape(-1, 256)
+    assert np.any(w != 0) and np.any((np.abs(w) < 2.0 ** -126) & (w != 0))
+    fn = q4q.q4q_quantize_q4_0 if kind == "q4_0" else q4q.q4q_quantize_q8_0
+    ref = oracle.quantize_q4_0(w) if kind == "q4_0" else oracle.quantize_q8_0(w)
+    np.testing.assert_array_equal(fn(dev(w)).cpu().numpy(), ref)
+    # the same rows through the scalar kernel (misaligned buffers)
+    nrows, ncols = w.shape
+    src = torch.zeros(w.size + 1, dtype=torch.float32, device="cuda")
+    src[1:] = dev(w.reshape(-1))
+    bpr = ncols // 32 * (18 if kind == "q4_0" else 34)
+    dst = torch.zeros(nrows * bpr + 1, dtype=torch.uint8, device="cuda")
+    lib = q4q._lib.load()
+    cfn = lib.q4q_quantize_q4_0 if kind == "q4_0" else lib.q4q_quantize_q8_0
+    assert cfn(ctypes.c_void_p(src.data_ptr() + 4), ctypes.c_void_p(dst.data_ptr() + 1), ncols, nrows,
+               ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)) == 0
+    np.testing.assert_array_equal(dst[1:].cpu().numpy().reshape(nrows, bpr), ref)
+
+
+def test_mul_mat_tiny_activation_scales(q4q):
+    # The activation quantization fused into the GEMV (1..7 tokens) and into the
+    # tensor-core path's operand kernel (16 tokens) on tiny-scale blocks, against
+    # weights with one nonzero code per block so that every output isolates codes.
+    rng = np.random.default_rng(72)
+    ne00, ne01 = 4096, 64
+    x = _tiny_scale_rows(rng, 127, 16 * ne00 // 32).reshape(16, ne00)
+    wq_rows = np.zeros((ne01, ne00 // 32, 18), np.uint8)
+    wq_rows[:, :, 0:2] = np.frombuffer(np.float16(0.5).tobytes(), np.uint8)
+    wq_rows[:, :, 2:] = 0x88
+    sel = rng.integers(0, 32, size=(ne01, ne00 // 32))
+    for r in range(ne01):
+        for b in range(ne00 // 32):
+            j = sel[r, b]
+            wq_rows[r, b, 2 + j // 2] = (0x8F if j % 2 == 0 else 0xF8)    # nibble 15: value +7 d
+    wq = wq_rows.reshape(-1)
+    for ne11 in (1, 3, 7, 16):
+        got = q4q.q4q_mul_mat(dev(wq), ne00, ne01, dev(x[:ne11])).cpu().numpy()
+        ref, scale = oracle.mul_mat(wq, ne00, ne01, x[:ne11])
+        assert np.any(scale > 0) and np.any(scale == 0)
+        assert_close(got, ref, scale)
+    assert q4q.q4q_device_status() == 0
+
+
+# --------------------------------------------- the kernels' own bounded waits --
+
+@pytest.mark.parametrize("path,ne00,ne01,ne11", [(0, 4096, 1024, 1), (0, 1024, 300, 3), (0, 4096, 128256, 1),
+                                                 (1, 4096, 1024, 16), (1, 1024, 256, 130), (1, 4096, 2048, 64)])
+def test_kernel_timeout_path(q4q, path, ne00, ne01, ne11):
+    """A matmul kernel whose first CTA never receives its first stage (a hand-off left
+    out on purpose, with every wait bounded by 5 ms): the waits run out, the device
+    status reports Q4Q_ERR_TIMEOUT once, and the CTAs wind down (their copies landed,
+    tensor memory freed), so the same kernel then runs normally, twice in a row, and
+    matches the oracle.  No GPU fault or hang is involved."""
+    assert q4q.q4q_device_status() == 0
+    rng = np.random.default_rng([path, ne00, ne01, ne11])
+    w = (rng.standard_normal((ne01, ne00)) * 0.02).astype(np.float32)
+    x = rng.standard_normal((ne11, ne00)).astype(np.float32)
+    wq_d = q4q.q4q_quantize_q4_0(dev(w))
+    x_d = dev(x)
+    q4q.q4q_debug_mul_mat_timeout(wq_d, ne00, ne01, x_d, path, 5_000_000)
+    assert q4q.q4q_device_status() == 6
+    assert q4q.q4q_device_status() == 0
+    rows = _sample_rows(ne01, 2048, 7)
+    ref, scale = oracle.mul_mat(wq_d.view(ne01, -1)[torch.from_numpy(rows).cuda()].cpu().numpy(), ne00, rows.size, x,
+                                nthreads=8)
+    for _ in range(2):
+        got = q4q.q4q_mul_mat(wq_d, ne00, ne01, x_d).cpu().numpy()
+        assert_close(got[:, rows], ref, scale)
+    assert q4q.q4q_device_status() == 0
+
+
+def test_kernel_timeout_argument_errors(q4q):
+    wq = torch.zeros(64 * 8 * 18, dtype=torch.uint8, device="cuda")
+    x = torch.zeros((1, 256), device="cuda")
+    with pytest.raises(q4q.Q4QError):            # path 1 needs ne11 >= 8
+        q4q.q4q_debug_mul_mat_timeout(wq, 256, 64, x, 1, 1_000_000)
+    with pytest.raises(q4q.Q4QError):            # limit above one second
+        q4q.q4q_debug_mul_mat_timeout(wq, 256, 64, x, 0, 2_000_000_000)
+    with pytest.raises(q4q.Q4QError):            # unknown path
+        q4q.q4q_debug_mul_mat_timeout(wq, 256, 64, x, 2, 1_000_000)
     assert q4q.q4q_device_status() == 0

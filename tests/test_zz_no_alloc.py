@@ -47,8 +47,10 @@ def _call_noalloc_abi(lib, wq, ne00, ne01, x, out):
 
 def test_noalloc_matches_workspace_entry_point_twice_in_a_row(q4q):
     lib = q4q._lib.load()
-    # tensor-core path (ne11 >= 8) twice with different shapes, then the GEMV path
-    cases = [(4096, 1000, 64, 1), (768, 130, 17, 2), (1024, 300, 3, 3)]
+    # the tensor-core path (ne11 >= 8) twice with different shapes, the generic path
+    # (ne00 % 256 != 0: Q8_0 activations in the scratch array) twice, then the GEMV,
+    # which needs no scratch; each against the workspace entry point and the oracle
+    cases = [(4096, 1000, 64, 1), (768, 130, 17, 2), (800, 200, 12, 4), (96, 33, 9, 5), (1024, 300, 3, 3)]
     for ne00, ne01, ne11, seed in cases:
         w, x = _problem(ne00, ne01, ne11, seed)
         wq = q4q.q4q_quantize_q4_0(torch.from_numpy(w).cuda())
@@ -59,8 +61,10 @@ def test_noalloc_matches_workspace_entry_point_twice_in_a_row(q4q):
         torch.cuda.synchronize()
         ref_dev = ref_dev.cpu().numpy()
         got = got.cpu().numpy()
-        _, scale = oracle.mul_mat(wq.cpu().numpy(), ne00, ne01, x, nthreads=8)
+        want, scale = oracle.mul_mat(wq.cpu().numpy(), ne00, ne01, x, nthreads=8)
         assert np.all(np.abs(got.astype(np.float64) - ref_dev) <= TOL * scale)
+        assert np.all(np.abs(got.astype(np.float64) - want) <= TOL * scale)
+        assert np.all(got[scale == 0] == 0)
     assert q4q.q4q_device_status() == 0
 
 
