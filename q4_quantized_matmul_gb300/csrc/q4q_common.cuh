@@ -84,7 +84,7 @@ __device__ __forceinline__ float recip_approx(float d) {
 constexpr float NEAR_LIMIT = 0.49995f;            // 0.5 - NEAR_BAND
 //
 // RAW: the codes are only right in their low byte (the caller packs bytes and
-// handles d == 0 itself); for Q8_0, where no clamp is needed.
+// handles d == 0 itself); for Q8_0, whose common path needs no clamp.
 template <int N, bool RAW = false>
 __device__ __forceinline__ void quant8n(const float (&v)[N][8], const float (&d)[N], float lo, float hi,
                                         int (&q)[N][8]) {
@@ -115,14 +115,18 @@ __device__ __forceinline__ void quant8n(const float (&v)[N][8], const float (&d)
             for (int e = 0; e < 8; ++e) {
                 const float t = v[n][e] * inv[n];
                 const float r = __fsub_rn(__fadd_rn(t, MAGIC), MAGIC);
-                if (d[n] != 0.0f && !(fabsf(__fsub_rn(t, r)) <= NEAR_LIMIT)) q[n][e] = (int)roundf(__fdiv_rn(v[n][e], d[n]));
+                if (d[n] != 0.0f && !(fabsf(__fsub_rn(t, r)) <= NEAR_LIMIT))
+                    q[n][e] = (int)fminf(fmaxf(roundf(__fdiv_rn(v[n][e], d[n])), lo), hi);
             }
         }
     }
-    // Codes stay inside [lo, hi] by construction except one: |x / d| <= 127.0001
-    // never rounds past 127 (Q8_0), and x / d >= -8 never below -8 (Q4_0), but
-    // x = +amax gives +8 in Q4_0, which the format stops at 7.
-    (void)lo;
+    // Codes stay inside [lo, hi] by construction on the common path: where d is an
+    // fp32 normal, |x / d| <= 127.0001 never rounds past 127 (Q8_0) and x / d >= -8
+    // never below -8 (Q4_0); x = +amax gives +8 in Q4_0, which the format stops at 7
+    // (below).  Where d is an fp32 subnormal it carries too few bits for that bound
+    // (amax = 11 * 2^-149 gives d = fl(amax / 8) = 2^-149 and quotients up to 11),
+    // but then the flushed reciprocal is infinite, every element takes the exact
+    // division above, and that path clamps to [lo, hi] itself.
     if constexpr (RAW) return;
     const int ihi = (int)hi;
 #pragma unroll
