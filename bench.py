@@ -370,6 +370,9 @@ def run_ours(args, rank, world, local_rank):
               if (rank == 0 and args.secondary_decode not in ("", "none") and args.secondary_decode != args.workload)
               else None)
     nxt = measure_next(dev, stream) if (rank == 0 and args.next_rows) else None
+    if nxt is not None and ne11 == 1 and args.workload != "gpt2_decode_step":
+        # the main decode set as one chain launch, A/B against its PDL-chained calls
+        nxt["chain_" + args.workload] = measure_decode(dev, stream, args.workload, steps=200)
 
     # ---- CPU baseline: the oracle on this host's cores, bounded sample
     cpu = cpu_baseline(args.workload, ne11, budget_s=args.cpu_seconds) if (rank == 0 and args.cpu_seconds > 0) else None
@@ -499,7 +502,38 @@ def measure_decode(dev, stream, name, steps=300):
            "us_per_matrix": round(ms * 1e3 / len(shapes), 3),
            "graph_steps": 1,
            "note": "dependent-chain launch (PDL), one kernel per matrix; small matrices are launch-latency bound"}
-    del wsets, wq, xs, ds
+    # The same step as one q4q_mul_mat_chain launch over the same weights and inputs
+    # (each link still waits for the previous one to complete everywhere before it
+    # reads its activations), timed the same way right after: the A/B of the
+    # persistent chain against the PDL chain of separate launches.
+    wsc = torch.empty(q4q.q4q_mul_mat_chain_workspace_size(len(shapes)), dtype=torch.uint8, device=dev)
+    links = [[(wsets[c][i], ne00, ne01, xs[i].reshape(-1), ds[i].reshape(-1)) for i, (ne00, ne01) in
+              enumerate(shapes)] for c in range(copies)]
+    with torch.cuda.stream(stream):
+        for c in range(copies):
+            q4q.q4q_mul_mat_chain(links[c], workspace=wsc)
+    torch.cuda.synchronize()
+    cgraphs = []
+    for c in range(copies):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            q4q.q4q_mul_mat_chain(links[c], workspace=wsc)
+        cgraphs.append(g)
+    with torch.cuda.stream(stream):
+        for k in range(10):
+            cgraphs[k % copies].replay()
+        e0.record(stream)
+        for k in range(steps):
+            cgraphs[k % copies].replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    cms = e0.elapsed_time(e1) / steps
+    cgbs = wbytes / (cms * 1e-3) / 1e9
+    out["chain"] = {"value": round(cgbs, 1), "unit": "GB/s", "ms_per_step": round(cms, 5),
+                    "frac_of_hbm": round(cgbs / peak, 4), "us_per_matrix": round(cms * 1e3 / len(shapes), 3),
+                    "speedup_vs_pdl_launches": round(ms / cms, 3),
+                    "note": "one cooperative q4q_mul_mat_chain launch per step (memset of its counters + kernel)"}
+    del wsets, wq, xs, ds, cgraphs, links
     torch.cuda.empty_cache()
     return out
 

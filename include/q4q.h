@@ -260,6 +260,45 @@ Q4Q_API q4q_status q4q_debug_block_isums_q8_0(const void* src0_q8_0, const void*
                                       int64_t ne01, int64_t ne11, int path, int32_t* out,
                                       void* workspace, size_t workspace_bytes, q4q_stream_t stream);
 
+/* Most links one q4q_mul_mat_chain call takes. */
+#define Q4Q_CHAIN_MAX 64
+
+/* One projection of a chain (one token): dst = ggml_mul_mat(src0 Q4_0 [ne00, ne01],
+ * src1 F32 [ne00, 1]) -> F32 [ne01], computed as q4q_mul_mat computes it. */
+typedef struct {
+    const void* src0;     /* Q4_0 weights, ne01 rows of ne00/32 blocks; device, 16-byte aligned */
+    int64_t ne00, ne01;   /* 0 < ne00 < 2^20 with ne00 % 256 == 0; 0 < ne01 < 2^31 */
+    const float* src1;    /* fp32 [ne00]; device, 16-byte aligned; may be an earlier link's dst */
+    float* dst;           /* fp32 [ne01]; device, 4-byte aligned */
+} q4q_chain_link;
+
+/* Bytes of device workspace q4q_mul_mat_chain needs for n links (a completion
+ * count per link and an abort word); n: 1 .. Q4Q_CHAIN_MAX, else Q4Q_ERR_ARG. */
+Q4Q_API q4q_status q4q_mul_mat_chain_workspace_size(int n, size_t* bytes);
+
+/* A chain of dependent one-token projections in one launch: for i = 0 .. n-1, in
+ * order, links[i].dst = ggml_mul_mat(links[i].src0, links[i].src1), each exactly as
+ * q4q_mul_mat computes it.  This is the shape of a decode step: the "ggml GPT-2 117M
+ * inference walkthrough" runs every layer's QKV projection (§3.2), its output
+ * projection and MLP (§3.5) and finally the lm_head (§3.6) one after another, each
+ * a ggml_mul_mat ("llama.cpp 深度解读" §3) whose input an earlier step produced.
+ * Link i reads its src1 only after every earlier link has written all of its dst,
+ * so src1 of link i may be (or overlap) the dst of any earlier link; it must not
+ * overlap its own dst, and no dst may overlap any link's src0 (the weights of
+ * later links are read ahead).  One persistent grid is launched cooperatively (all
+ * of its CTAs resident at once): its CTAs stream every link's weights back to back
+ * and meet at device-side completion counts between links, instead of one launch
+ * per matrix.
+ * links: HOST array of n entries (read during the call); n: 1 .. Q4Q_CHAIN_MAX;
+ * ne11: must be 1 (one token), else Q4Q_ERR_SHAPE; flags: 0, else Q4Q_ERR_ARG;
+ * workspace: device, 4-byte aligned, q4q_mul_mat_chain_workspace_size(n) bytes,
+ * zeroed by the call on `stream` (calls that overlap on the GPU must not share it).
+ * Every wait between links and on the weight stages is bounded (about one second):
+ * one that runs out records Q4Q_ERR_TIMEOUT (q4q_device_status), raises the call's
+ * abort and the remaining links are not computed. */
+Q4Q_API q4q_status q4q_mul_mat_chain(const q4q_chain_link* links, int n, int64_t ne11, void* workspace,
+                             size_t workspace_bytes, unsigned int flags, q4q_stream_t stream);
+
 /* Size of the library-owned scratch array used by q4q_mul_mat_noalloc (per GPU). */
 #define Q4Q_NOALLOC_SCRATCH_BYTES (8u << 20)
 
@@ -340,14 +379,17 @@ Q4Q_API q4q_status q4q_debug_wait_timeout(uint64_t limit_ns, q4q_stream_t stream
  * path 1: the tensor-core GEMM (ne11 >= 8) -- with every wait bounded by limit_ns
  * nanoseconds and one hand-off left out in its first CTA: that CTA's first stage
  * of weights (GEMV) or of activations (GEMM) is never copied, so the waits on it
- * run out.  The CTA that gives up records Q4Q_ERR_TIMEOUT in the device status
+ * run out.  Path 2 (ne11 = 1): q4q_mul_mat_chain over two links of this matrix on
+ * the same input, whose first CTA never reports the first link finished, so the
+ * other CTAs' waits before the second link run out (workspace: that of a
+ * two-link chain).  The CTA that gives up records Q4Q_ERR_TIMEOUT in the device status
  * word (read by q4q_device_status) and raises the call's abort; it and every CTA
  * of the call that then finds the abort raised wait (bounded) for their own copies
  * in flight, free their tensor memory and return.  No GPU fault or hang is
  * involved and the context stays usable; dst is left incomplete.  Arguments as
  * q4q_mul_mat (path 1: its workspace); the problem must take the chosen path
  * (ne00 % 256 == 0, 16-byte aligned src0 and src1), else Q4Q_ERR_SHAPE.
- * limit_ns: 1 .. 1e9, path: 0 or 1, else Q4Q_ERR_ARG. */
+ * limit_ns: 1 .. 1e9, path: 0, 1 or 2, else Q4Q_ERR_ARG. */
 Q4Q_API q4q_status q4q_debug_mul_mat_timeout(const void* src0, int64_t ne00, int64_t ne01, const float* src1,
                                      int64_t ne11, float* dst, void* workspace, size_t workspace_bytes,
                                      int path, uint64_t limit_ns, q4q_stream_t stream);

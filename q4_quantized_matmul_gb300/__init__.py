@@ -435,9 +435,49 @@ def q4q_debug_mul_mat_timeout(src0: torch.Tensor, ne00: int, ne01: int, src1: to
     ne11, ne10 = x.shape
     if dst is None:
         dst = torch.empty((ne11, ne01), dtype=torch.float32, device=x.device)
-    need = q4q_mul_mat_workspace_size(ne00, ne01, ne11) if path == 1 else 0
+    need = {0: 0, 1: q4q_mul_mat_workspace_size(ne00, ne01, ne11) if path == 1 else 0,
+            2: q4q_mul_mat_chain_workspace_size(2)}.get(path, 0)
     ws_ptr, ws_bytes = _workspace(need, workspace, x.device)
     _check("q4q_debug_mul_mat_timeout", _lib.load().q4q_debug_mul_mat_timeout(
         _dev(src0, "src0", ne01 * q4_0_row_bytes(ne00)), ne00, ne01, _dev(x, "src1"), ne11,
         _dev(dst, "dst", 4 * ne01 * ne11), ws_ptr, ws_bytes, int(path), int(limit_ns), _stream(stream)))
     return dst
+
+
+# --------------------------------------------------- chains of projections --
+
+Q4Q_CHAIN_MAX = 64
+
+
+class ChainLink(ctypes.Structure):
+    """q4q_chain_link of include/q4q.h."""
+    _fields_ = [("src0", ctypes.c_void_p), ("ne00", ctypes.c_int64), ("ne01", ctypes.c_int64),
+                ("src1", ctypes.c_void_p), ("dst", ctypes.c_void_p)]
+
+
+def q4q_mul_mat_chain_workspace_size(n: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check("q4q_mul_mat_chain_workspace_size", _lib.load().q4q_mul_mat_chain_workspace_size(int(n), ctypes.byref(out)))
+    return int(out.value)
+
+
+def chain_links(links):
+    """ctypes array of q4q_chain_link from (src0, ne00, ne01, src1, dst) tuples of CUDA tensors."""
+    arr = (ChainLink * len(links))()
+    for i, (w, ne00, ne01, x, y) in enumerate(links):
+        arr[i] = ChainLink(_dev(w, "src0", ne01 * q4_0_row_bytes(ne00)).value, ne00, ne01,
+                           _dev(x, "src1", 4 * ne00).value, _dev(y, "dst", 4 * ne01).value)
+    return arr
+
+
+@_on_tensor_device
+def q4q_mul_mat_chain(links, workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Run a chain of one-token projections in one launch: for each (src0, ne00, ne01,
+    src1, dst) in order, dst = ggml_mul_mat(src0, src1); a link's src1 may be an
+    earlier link's dst.  src0: uint8 Q4_0 blocks, src1: float32 [ne00], dst: float32 [ne01]."""
+    n = len(links)
+    arr = chain_links(links)
+    if workspace is None:
+        workspace = torch.empty(q4q_mul_mat_chain_workspace_size(n), dtype=torch.uint8, device=links[0][0].device)
+    _check("q4q_mul_mat_chain", _lib.load().q4q_mul_mat_chain(arr, n, 1, _dev(workspace, "workspace"),
+                                                             workspace.numel(), 0, _stream(stream)))

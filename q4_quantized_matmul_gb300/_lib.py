@@ -49,6 +49,8 @@ _SIGNATURES = {
     "q4q_debug_gemv_plan": (STATUS, [I64, I64, I64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                      ctypes.POINTER(I64)]),
     "q4q_debug_mma_splits": (STATUS, [I64, I64, I64, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]),
+    "q4q_mul_mat_chain_workspace_size": (STATUS, [ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]),
+    "q4q_mul_mat_chain": (STATUS, [P, ctypes.c_int, I64, P, ctypes.c_size_t, ctypes.c_uint, P]),
     "q4q_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "q4q_version": (ctypes.c_int, []),
 }

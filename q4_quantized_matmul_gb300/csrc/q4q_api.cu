@@ -164,7 +164,7 @@ extern "C" q4q_status q4q_debug_wait_timeout(uint64_t limit_ns, q4q_stream_t str
 extern "C" q4q_status q4q_debug_mul_mat_timeout(const void* src0, int64_t ne00, int64_t ne01, const float* src1,
                                                 int64_t ne11, float* dst, void* workspace, size_t workspace_bytes,
                                                 int path, uint64_t limit_ns, q4q_stream_t stream_) {
-    if (path != 0 && path != 1) return Q4Q_ERR_ARG;
+    if (path < 0 || path > 2) return Q4Q_ERR_ARG;
     if (limit_ns == 0 || limit_ns > WAIT_LIMIT_NS) return Q4Q_ERR_ARG;
     q4q_status st = check_mul_mat_shapes(ne00, ne01, ne00, ne11);
     if (st != Q4Q_OK) return st;
@@ -177,6 +177,16 @@ extern "C" q4q_status q4q_debug_mul_mat_timeout(const void* src0, int64_t ne00, 
     if (path == 0) {
         if (ne11 >= 8 || !gemv_supported(src0, ne00, ne01, src1, ne11, info)) return Q4Q_ERR_SHAPE;
         return gemv_mul_mat(src0, ne00, ne01, src1, ne11, dst, stream, info, false, &dbg);
+    }
+    if (path == 2) {
+        // a two-link chain of this matrix on the same input (link 1 rewrites dst)
+        if (ne11 != 1) return Q4Q_ERR_SHAPE;
+        const q4q_chain_link links[2] = {{src0, ne00, ne01, src1, dst}, {src0, ne00, ne01, src1, dst}};
+        if ((st = chain_check(links, 2)) != Q4Q_OK) return st;
+        if (workspace_bytes < chain_workspace_bytes(2)) return Q4Q_ERR_WORKSPACE;
+        if (!workspace) return Q4Q_ERR_NULL;
+        if (!aligned(workspace, 4)) return Q4Q_ERR_ALIGN;
+        return chain_launch(links, 2, workspace, stream, info, &dbg);
     }
     if (ne11 < 8 || !mma_supported(ne00, ne01, ne11, info) || !aligned(src0, 16) || !aligned(src1, 16))
         return Q4Q_ERR_SHAPE;
@@ -194,7 +204,8 @@ extern "C" q4q_status q4q_device_status(q4q_status* status) {
     const unsigned int words[] = {gemv_take_device_status(), mma_take_device_status(),
                                   gemv_swiglu_take_device_status(), gemv_w8_take_device_status(),
                                   gemv_group_take_device_status(), gemv_epi_take_device_status(),
-                                  rows_take_device_status(), debug_take_device_status()};
+                                  rows_take_device_status(), debug_take_device_status(),
+                                  chain_take_device_status()};
     unsigned int first = 0;
     for (unsigned int w : words)
         if (!first) first = w;

@@ -245,8 +245,10 @@ __device__ __forceinline__ void quantize_chunk(const float (&v)[NI][8], int nb, 
 // tid below `end`) to Q8_0 into shared memory.  Every load is issued before any
 // arithmetic, so their latencies overlap.  m0 is a multiple of 4, so the four
 // lanes of a block stay in one aligned group; all 32 lanes of every consumer
-// warp must call it.
-template <int T, int NI, int CL>
+// warp must call it.  COHERENT: the activations may have been written earlier by
+// the same kernel (another CTA), so they are read from L2 (ld.global.cg) rather
+// than through the read-only path.
+template <int T, int NI, int CL, bool COHERENT = false>
 __device__ __forceinline__ void quantize_acts(const float* __restrict__ x, int ne00, int nb, int np, int m0,
                                               int end, const ActDst<CL>& dst, int tid) {
     const int per_tok = nb * 4;
@@ -258,7 +260,7 @@ __device__ __forceinline__ void quantize_acts(const float* __restrict__ x, int n
             int rem;
             const int t = act_item<T>(m, per_tok, rem);
             const float4* src = reinterpret_cast<const float4*>(x + (int64_t)t * ne00 + (rem >> 2) * QK + (rem & 3) * 8);
-            const float4 lo = __ldg(src), hi = __ldg(src + 1);
+            const float4 lo = COHERENT ? __ldcg(src) : __ldg(src), hi = COHERENT ? __ldcg(src + 1) : __ldg(src + 1);
             v[u][0] = lo.x; v[u][1] = lo.y; v[u][2] = lo.z; v[u][3] = lo.w;
             v[u][4] = hi.x; v[u][5] = hi.y; v[u][6] = hi.z; v[u][7] = hi.w;
         } else {

@@ -110,6 +110,13 @@ unsigned int debug_take_device_status();
 // row gather (q4q_rows.cu)
 unsigned int rows_take_device_status();
 
+// chains of dependent one-token projections in one launch (q4q_chain.cu)
+unsigned int chain_take_device_status();
+size_t chain_workspace_bytes(int n);
+q4q_status chain_check(const q4q_chain_link* links, int n);
+q4q_status chain_launch(const q4q_chain_link* links, int n, void* workspace, cudaStream_t stream,
+                        const DeviceInfo& info, const KernelDebug* dbg);
+
 // Shape rules shared by every matmul entry point (q4q_api.cu).
 q4q_status check_mul_mat_shapes(int64_t ne00, int64_t ne01, int64_t ne10, int64_t ne11);
 // The least workspace q4q_mul_mat runs in for this shape (the tensor-core path then

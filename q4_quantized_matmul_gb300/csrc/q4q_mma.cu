@@ -288,6 +288,11 @@ struct Cfg {
     // by its epilogue, which frees each slab as soon as it has read it.
     static constexpr bool PAIRWISE = NT <= 64;
     static constexpr int CPW = NT * 4 / EPI_WARPS;       // columns per epilogue warp
+    // Columns per tcgen05.ld: the widest tile reads its 32 columns per slab in two
+    // 16-column loads, which keeps the epilogue within the 80 registers a thread of a
+    // 768-thread CTA has (one 32-column load made it spill; measured 9% slower on the
+    // 512-token lm_head).
+    static constexpr int CH = NT >= 128 ? 16 : (CPW < 32 ? CPW : 32);
     static constexpr int THREADS = (8 + EPI_WARPS) * 32;
     static constexpr int B_BYTES = NT * KAB * 2;
     static constexpr int B_STRIDE = (B_BYTES + 1023) / 1024 * 1024;
@@ -585,10 +590,10 @@ mma_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                 }
             }
         } else {
-            // One TMEM round trip per slab per warp (its CPW <= 32 columns); the
-            // NT/32 warps that share a lane quadrant overlap their load latencies.
-            constexpr int CK = C::CPW;
-            static_assert(CK == 16 || CK == 32, "one load per slab");
+            // Per slab each warp reads its CPW columns in loads of CH; the NT/32 warps that
+            // share a lane quadrant overlap their load latencies.
+            constexpr int CH = C::CH;
+            static_assert(C::CPW % CH == 0 && (CH == 16 || CH == 32), "whole loads per slab");
             uint64_t acc[C::CPW / 2];
 #pragma unroll
             for (int c = 0; c < C::CPW / 2; ++c) acc[c] = 0;
@@ -597,11 +602,6 @@ mma_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
             constexpr bool PAIRWISE = C::PAIRWISE;
             for (int i = 0; i < n_ab && !aborted; ++i) {
                 const int s = i % AB_STAGES, pr = i % NPAIR;
-                // One check per stage with both polls in flight together: the stage's
-                // activation scales, and its slabs.  Pairwise: the commit of its slab
-                // pair (issued after the stage's MMAs).  Otherwise: its second slab; the
-                // issuer commits it after the first, and a commit completes only once
-                // every earlier MMA of that thread has, so it implies the first.
                 {
                     const int g1 = 2 * i + 1;
                     const uint32_t bar_a = ab_full + 8 * s, par_a = (uint32_t)((i / AB_STAGES) & 1);
@@ -619,26 +619,29 @@ mma_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     const int buf = 2 * pr + j;
-                    uint32_t r[CK];
-                    tmem_ld_chunk<CK>(tq + (uint32_t)(buf * NT + col0), r);
                     const float dwm = dw_s[(s * 2 + j) * BM + row];
                     const uint64_t dw2 = pack2(dwm, dwm);
                     const float4* dxs = reinterpret_cast<const float4*>(dx_s + (s * 2 + j) * NT + col0);
-                    tmem_ld_wait();
-                    if (!PAIRWISE || j == 1) {
-                        // the slab (pairwise: both slabs) is in registers: hand it back
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(slab_empty + 8 * (PAIRWISE ? pr : buf));
-                    }
 #pragma unroll
-                    for (int c = 0; c < CK / 4; ++c) {
-                        const float4 d4 = dxs[c];
-                        acc[2 * c] = ffma2(fmul2(dw2, pack2(d4.x, d4.y)),
-                                           pack2(__uint_as_float(r[4 * c]), __uint_as_float(r[4 * c + 1])), acc[2 * c]);
-                        acc[2 * c + 1] = ffma2(fmul2(dw2, pack2(d4.z, d4.w)),
+                    for (int h = 0; h < C::CPW / CH; ++h) {
+                        uint32_t r[CH];
+                        tmem_ld_chunk<CH>(tq + (uint32_t)(buf * NT + col0 + h * CH), r);
+                        tmem_ld_wait();
+                        if (h == C::CPW / CH - 1 && (!PAIRWISE || j == 1)) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(slab_empty + 8 * (PAIRWISE ? pr : buf));
+                        }
+#pragma unroll
+                        for (int c = 0; c < CH / 4; ++c) {
+                            const float4 d4 = dxs[h * (CH / 4) + c];
+                            const int a = h * (CH / 2) + 2 * c;
+                            acc[a] = ffma2(fmul2(dw2, pack2(d4.x, d4.y)),
+                                           pack2(__uint_as_float(r[4 * c]), __uint_as_float(r[4 * c + 1])), acc[a]);
+                            acc[a + 1] = ffma2(fmul2(dw2, pack2(d4.z, d4.w)),
                                                pack2(__uint_as_float(r[4 * c + 2]), __uint_as_float(r[4 * c + 3])),
-                                               acc[2 * c + 1]);
+                                               acc[a + 1]);
+                        }
                     }
                 }
                 // the stage's scales have been read for both of its slabs

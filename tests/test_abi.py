@@ -190,7 +190,7 @@ def test_kernel_timeout_entry_argument_errors(lib):
     P = ctypes.c_void_p
     fake = P(0x1000)
     f = lib.q4q_debug_mul_mat_timeout
-    assert f(fake, 256, 4, fake, 1, fake, None, 0, 2, 10 ** 6, None) == 7          # unknown path
+    assert f(fake, 256, 4, fake, 1, fake, None, 0, 3, 10 ** 6, None) == 7          # unknown path
     assert f(fake, 256, 4, fake, 1, fake, None, 0, 0, 0, None) == 7                # limit 0
     assert f(fake, 256, 4, fake, 1, fake, None, 0, 0, 2 * 10 ** 9, None) == 7      # limit above 1 s
     assert f(fake, 48, 4, fake, 1, fake, None, 0, 0, 10 ** 6, None) == 2           # ne00 % 32
@@ -234,3 +234,34 @@ int main(void) {
     finally:
         os.unlink(exe)
     assert out.returncode == 0 and out.stdout == "ok\n", (out.returncode, out.stdout, out.stderr)
+
+
+def test_chain_argument_errors(lib):
+    import q4_quantized_matmul_gb300 as q4q
+    P = ctypes.c_void_p
+    fake = 0x1000
+    links = (q4q.ChainLink * 3)(*[q4q.ChainLink(fake, 256, 4, fake, fake) for _ in range(3)])
+    n = ctypes.c_size_t(0)
+    assert lib.q4q_mul_mat_chain_workspace_size(3, ctypes.byref(n)) == 0 and n.value == 256
+    assert lib.q4q_mul_mat_chain_workspace_size(0, ctypes.byref(n)) == 7
+    assert lib.q4q_mul_mat_chain_workspace_size(65, ctypes.byref(n)) == 7
+    assert lib.q4q_mul_mat_chain_workspace_size(3, None) == 1
+    ws = P(fake)
+    assert lib.q4q_mul_mat_chain(links, 0, 1, ws, 256, 0, None) == 7          # no links
+    assert lib.q4q_mul_mat_chain(links, 65, 1, ws, 256, 0, None) == 7         # above Q4Q_CHAIN_MAX
+    assert lib.q4q_mul_mat_chain(links, 3, 1, ws, 256, 1, None) == 7          # flags must be 0
+    assert lib.q4q_mul_mat_chain(None, 3, 1, ws, 256, 0, None) == 1
+    assert lib.q4q_mul_mat_chain(links, 3, 2, ws, 256, 0, None) == 2          # one token only
+    assert lib.q4q_mul_mat_chain(links, 3, 1, ws, 16, 0, None) == 4           # workspace too small
+    assert lib.q4q_mul_mat_chain(links, 3, 1, None, 256, 0, None) == 1
+    links[1].ne00 = 288                                                        # ne00 % 256 != 0
+    assert lib.q4q_mul_mat_chain(links, 3, 1, ws, 256, 0, None) == 2
+    links[1].ne00 = 256
+    links[2].ne01 = 0
+    assert lib.q4q_mul_mat_chain(links, 3, 1, ws, 256, 0, None) == 2
+    links[2].ne01 = 4
+    links[0].src1 = fake + 4                                                   # src1 not 16-byte aligned
+    assert lib.q4q_mul_mat_chain(links, 3, 1, ws, 256, 0, None) == 3
+    links[0].src1 = fake
+    links[2].dst = None
+    assert lib.q4q_mul_mat_chain(links, 3, 1, ws, 256, 0, None) == 1

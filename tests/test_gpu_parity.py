@@ -603,5 +603,5 @@ def test_kernel_timeout_argument_errors(q4q):
     with pytest.raises(q4q.Q4QError):            # limit above one second
         q4q.q4q_debug_mul_mat_timeout(wq, 256, 64, x, 0, 2_000_000_000)
     with pytest.raises(q4q.Q4QError):            # unknown path
-        q4q.q4q_debug_mul_mat_timeout(wq, 256, 64, x, 2, 1_000_000)
+        q4q.q4q_debug_mul_mat_timeout(wq, 256, 64, x, 3, 1_000_000)
     assert q4q.q4q_device_status() == 0
