@@ -177,22 +177,29 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     wl = _workload(args.workload)
     ne11 = args.ne11 or wl.ne11[0]
-    shapes = list(wl.shapes)
+    # --matrices i,j,...: only those matrices of the set (profiling one kernel at full size)
+    pick = [int(t) for t in args.matrices.split(",")] if args.matrices else list(range(len(wl.shapes)))
+    shapes = [wl.shapes[i] for i in pick]
     nmat = len(shapes)
 
     # ---- set-up (untimed): fp32 weights -> Q4_0 on the GPU, activations resident
+    # the Q4_0 output is allocated outside the events: they bracket the encoder alone
     t_q = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     wq, xs, dsts = [], [], []
-    quant_ms, quant_in_bytes = 0.0, 0
-    for i, (ne00, ne01) in enumerate(shapes):
+    quant_ms, quant_in_bytes, quant_out_bytes = 0.0, 0, 0
+    for i, (ne00, ne01) in zip(pick, shapes):
         w, x = workloads.problem(args.workload, i, ne11)
         wd = torch.from_numpy(w).to(dev)
+        qd = torch.empty(ne01 * q4q.q4_0_row_bytes(ne00), dtype=torch.uint8, device=dev)
+        torch.cuda.synchronize()
         t_q[0].record()
-        wq.append(q4q.q4q_quantize_q4_0(wd))
+        q4q.q4q_quantize_q4_0(wd, dst=qd)
         t_q[1].record()
         torch.cuda.synchronize()
+        wq.append(qd)
         quant_ms += t_q[0].elapsed_time(t_q[1])
         quant_in_bytes += w.nbytes
+        quant_out_bytes += qd.numel()
         del wd
         xs.append(torch.from_numpy(x).to(dev))
         dsts.append(torch.empty((ne11, ne01), dtype=torch.float32, device=dev))
@@ -438,7 +445,13 @@ def run_ours(args, rank, world, local_rank):
                 "how": "CUDA graph per step: pinned-host -> device copy of all activations, %d q4q_mul_mat "
                        "calls, device -> pinned-host copy of all outputs" % nmat},
         "weight_quantize": {"gb_per_s_fp32_in": round(quant_in_bytes / (quant_ms * 1e-3) / 1e9, 1),
-                            "ms": round(quant_ms, 3), "note": "q4q_quantize_q4_0 over the set, once, per matrix"},
+                            "gb_per_s_in_out": round((quant_in_bytes + quant_out_bytes) / (quant_ms * 1e-3) / 1e9, 1),
+                            "frac_of_hbm": round((quant_in_bytes + quant_out_bytes) / (quant_ms * 1e-3) / 1e9 / peak,
+                                                 4),
+                            "ms": round(quant_ms, 3),
+                            "note": "q4q_quantize_q4_0 over the set at set-up, once per matrix (first call of each "
+                                    "shape), destination allocated outside the events; steady state in "
+                                    "next_rows.quantize"},
         "cpu_baseline": cpu,
         "clocks": clocks,
         "batched": batched,
@@ -844,6 +857,42 @@ def measure_next(dev, stream):
                 "plain = the same calls as q4q_mul_mat (no bias, no GELU) in the same graphs" % copies}
     del wsets, wq, gx, bs, ds, g_b, g_p
     torch.cuda.empty_cache()
+    out["quantize"] = measure_quantizers(dev, stream)
+    return out
+
+
+def measure_quantizers(dev, stream, reps=5):
+    """The two block encoders in steady state, each on an input larger than L2, the
+    destination allocated beforehand: Q4_0 of the Llama-3-8B lm_head weights
+    (128256 x 4096 fp32, 2.1 GB in, 295 MB out) and Q8_0 of 8192 activation rows of
+    14336 (470 MB in, 125 MB out).  Algorithmic bytes = fp32 read + blocks written."""
+    import torch
+
+    import q4_quantized_matmul_gb300 as q4q
+    peak, kind = _measured_peaks()
+    out = {}
+    cases = [("q4_0_lm_head_weights", q4q.q4q_quantize_q4_0, (128256, 4096), q4q.q4_0_row_bytes),
+             ("q8_0_activations", q4q.q4q_quantize_q8_0, (8192, 14336), q4q.q8_0_row_bytes)]
+    for name, fn, (rows, cols), row_bytes in cases:
+        g = torch.Generator(device=dev).manual_seed(5)
+        src = torch.randn((rows, cols), device=dev, generator=g) * 0.02
+        dst = torch.empty(rows * row_bytes(cols), dtype=torch.uint8, device=dev)
+        with torch.cuda.stream(stream):
+            fn(src, dst=dst)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                fn(src, dst=dst)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        nbytes = src.numel() * 4 + dst.numel()
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[name] = {"shape": [rows, cols], "us": round(ms * 1e3, 1), "gb_s": round(gbs, 1),
+                     "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "peak_kind": kind,
+                                  "unit": "GB/s", "frac": round(gbs / peak, 4)}}
+        del src, dst
+        torch.cuda.empty_cache()
     return out
 
 
@@ -976,10 +1025,31 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline budget (0 = skip)")
     ap.add_argument("--batched-tokens", type=int, default=512,
                     help="also measure the tensor-core path on the Llama-3-8B set at this many tokens (0 = skip)")
+    ap.add_argument("--matrices", default="", help="comma-separated indices: only those matrices of the set")
     ap.add_argument("--next-rows", type=int, default=1,
                     help="also time SwiGLU, bias/GELU, get_rows and Q8_0 weights (0 = skip)")
+    ap.add_argument("--probe", default="", choices=["", "quantize", "batched", "decode-chain"],
+                    help="run only this one measurement on GPU 0 and print its JSON (for profiling runs): "
+                         "quantize = both block encoders; batched = the tensor-core path at --batched-tokens; "
+                         "decode-chain = the --workload step as PDL launches and as one chain launch")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.probe:
+        import torch
+
+        import __graft_entry__
+        __graft_entry__.build()
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        stream = torch.cuda.Stream(device=dev)
+        if args.probe == "quantize":
+            res = measure_quantizers(dev, stream)
+        elif args.probe == "batched":
+            res = measure_batched(dev, stream, args)
+        else:
+            res = measure_decode(dev, stream, args.workload, steps=args.steps)
+        print(json.dumps({"probe": args.probe, "result": res}), flush=True)
+        return
 
     world = _env_int("WORLD_SIZE", 1)
     rank = _env_int("RANK", 0)
