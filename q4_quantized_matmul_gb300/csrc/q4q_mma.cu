@@ -17,8 +17,9 @@
 //   warp 1      : TMEM allocator and the single MMA-issuing thread
 //   warp 2      : TMA producer of the activation tile (fp16, 128-byte swizzle,
 //                 box = 64 K x NT tokens) into a 4-deep ring
-//   warps 4-7   : dequantizers: raw Q4_0 / Q8_0 -> fp16 A tile (128 rows x 64 K) in the
-//                 canonical K-major 128-byte-swizzle layout, plus the fp32 block scales
+//   warps 4-7   : dequantizers: raw Q4_0 / Q8_0 -> fp16 A tile (128 rows x 64 K) written
+//                 straight into tensor memory (tcgen05.st, row = TMEM lane), where the MMA
+//                 reads it as its A operand, plus the fp32 block scales (shared memory)
 //   warps 8..   : epilogue, NT/32 warps per TMEM lane quadrant: per 32-K slab each warp
 //                 loads its 32 columns with one tcgen05.ld and applies acc += d_w d_x S
 // K order inside every 8-element group is permuted the same way on both operands
@@ -50,7 +51,7 @@ constexpr size_t CTRL_BYTES = 256;
 constexpr int BM = 128;                 // weight rows per CTA tile (MMA M)
 constexpr int KRAW = 256;               // K per raw-weight stage (8 blocks per row)
 constexpr int KAB = 64;                 // K per A/B stage (2 blocks, one 128-byte swizzle row)
-constexpr int A_BYTES = BM * KAB * 2;   // 16384
+constexpr int A_COLS = KAB / 2;          // TMEM columns of one stage's A tile (2 fp16 per column)
 constexpr int WQ4_0 = 0;                // weight block types
 constexpr int WQ8_0 = 1;
 
@@ -68,10 +69,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int 
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
         ::"r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -95,6 +92,29 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
         ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
 }
+
+// The same MMA with its A operand in tensor memory (M = 128 rows in the 128 lanes, K along
+// the columns, two fp16 per 32-bit column).
+__device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+// 16 consecutive 32-bit columns of this thread's TMEM lane (its warp's lane quadrant).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16};"
+        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+          "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -296,13 +316,18 @@ struct Cfg {
     static constexpr int THREADS = (8 + EPI_WARPS) * 32;
     static constexpr int B_BYTES = NT * KAB * 2;
     static constexpr int B_STRIDE = (B_BYTES + 1023) / 1024 * 1024;
-    static constexpr int NBUF = NT * 4 <= 512 ? 4 : 2;   // TMEM slab buffers
-    static constexpr int TMEM_COLS = NT * NBUF < 32 ? 32 : NT * NBUF;
+    // TMEM: NBUF accumulator slabs of NT columns, then the A tiles of the A/B stages
+    // (A_COLS columns each); the allocation is the power of two that holds both.
+    static constexpr int NBUF = NT >= 128 ? 3 : 4;
+    static constexpr int A_COL0 = NBUF * NT;
+    static constexpr int TMEM_USED = A_COL0 + AB_STAGES * A_COLS;
+    static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64 : TMEM_USED <= 128 ? 128
+                                   : TMEM_USED <= 256 ? 256 : 512;
+    static_assert(TMEM_USED <= 512, "tensor memory holds 512 columns");
     static constexpr int DX_BYTES = 2 * NT * 4;           // activation scales of one A/B stage
     // shared memory map (offsets from a 1024-aligned base)
     static constexpr int OFF_RAW = 0;
-    static constexpr int OFF_A = OFF_RAW + RAW_STAGES * RAW_BYTES;                  // 1024-aligned
-    static constexpr int OFF_B = OFF_A + AB_STAGES * A_BYTES;
+    static constexpr int OFF_B = OFF_RAW + RAW_STAGES * RAW_BYTES;                  // 1024-aligned
     static constexpr int OFF_DW = OFF_B + AB_STAGES * B_STRIDE;
     static constexpr int OFF_DX = OFF_DW + AB_STAGES * 2 * BM * 4;
     static constexpr int OFF_BAR = OFF_DX + AB_STAGES * DX_BYTES;
@@ -440,15 +465,15 @@ mma_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_base = sbase + C::OFF_A + s * A_BYTES;
+                    const uint32_t a_col = tmem + (uint32_t)(C::A_COL0 + s * A_COLS);
                     const uint32_t b_base = sbase + C::OFF_B + s * C::B_STRIDE;
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
 #pragma unroll
                         for (int kk = 0; kk < 2; ++kk) {
-                            const uint32_t koff = (uint32_t)(64 * j + 32 * kk);   // bytes along the swizzled row
-                            mma_f16(tmem + (uint32_t)((2 * pr + j) * NT), smem_desc_sw128(a_base + koff),
-                                    smem_desc_sw128(b_base + koff), IDESC, (uint32_t)kk);
+                            const uint32_t koff = (uint32_t)(64 * j + 32 * kk);   // bytes along B's swizzled row
+                            mma_f16_tmem_a(tmem + (uint32_t)((2 * pr + j) * NT), a_col + (uint32_t)(16 * j + 8 * kk),
+                                           smem_desc_sw128(b_base + koff), IDESC, (uint32_t)kk);
                         }
                     }
                     mma_commit(slab_full + 8 * pr);
@@ -458,7 +483,7 @@ mma_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                 const int s = i % AB_STAGES;
                 if (!wait_or_abort(ab_full + 8 * s, (i / AB_STAGES) & 1, wt)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t a_base = sbase + C::OFF_A + s * A_BYTES;
+                const uint32_t a_col = tmem + (uint32_t)(C::A_COL0 + s * A_COLS);
                 const uint32_t b_base = sbase + C::OFF_B + s * C::B_STRIDE;
                 for (int j = 0; j < 2; ++j, ++g) {
                     const int buf = g % NBUF;
@@ -469,9 +494,9 @@ mma_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < 2; ++kk) {
-                        const uint32_t koff = (uint32_t)(64 * j + 32 * kk);    // bytes along the swizzled row
-                        mma_f16(tmem + (uint32_t)(buf * NT), smem_desc_sw128(a_base + koff),
-                                smem_desc_sw128(b_base + koff), IDESC, (uint32_t)kk);
+                        const uint32_t koff = (uint32_t)(64 * j + 32 * kk);    // bytes along B's swizzled row
+                        mma_f16_tmem_a(tmem + (uint32_t)(buf * NT), a_col + (uint32_t)(16 * j + 8 * kk),
+                                       smem_desc_sw128(b_base + koff), IDESC, (uint32_t)kk);
                     }
                     mma_commit(slab_full + 8 * buf);
                 }
@@ -484,10 +509,10 @@ mma_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
             }
         }
     } else if (warp >= 4 && warp < 8) {
-        // ---------------- dequantizers: thread t <-> tile row t; each A/B stage needs
-        // one pair of the row's 8 raw blocks, read as three 16-byte loads
+        // ---------------- dequantizers: thread t <-> tile row t = TMEM lane t (warp 4 + q
+        // owns lane quadrant q); each A/B stage needs one pair of the row's 8 raw blocks
         const int t = threadIdx.x - 128;
-        const int rsw = t & 7;
+        const uint32_t a_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)C::A_COL0;
         bool ok = true;
         for (int r = 0; r < n_raw && ok; ++r) {
             const int st = r % RAW_STAGES;
@@ -501,7 +526,8 @@ mma_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                     ok = false;
                     break;
                 }
-                uint8_t* atile = smem + C::OFF_A + s * A_BYTES + (t >> 3) * 1024 + rsw * 128;
+                tc_fence_after();      // the MMAs that read this stage's A columns have completed
+                const uint32_t a_stage = a_lane + (uint32_t)(s * A_COLS);
                 if constexpr (WT == WQ4_0) {
                     // pair a = blocks 2a, 2a+1 = words 9a .. 9a+8 of the row, inside the three
                     // 16-byte chunks (9a)/4 .. (9a)/4 + 2 (16-byte loads keep the eight lanes
@@ -519,8 +545,15 @@ mma_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
 #pragma unroll
                     for (int k = 0; k < 4; ++k) q[4 + k] = wv[w0 + 5 + k];                              // block 2a+1
 #pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<uint4*>(atile + ((c ^ rsw) << 4)) = nibbles_to_f16x8(q[c]);
+                    for (int j = 0; j < 2; ++j) {
+                        uint32_t av[16];
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const uint4 h = nibbles_to_f16x8(q[4 * j + c]);
+                            av[4 * c + 0] = h.x; av[4 * c + 1] = h.y; av[4 * c + 2] = h.z; av[4 * c + 3] = h.w;
+                        }
+                        tmem_st16(a_stage + (uint32_t)(16 * j), av);
+                    }
                     dw_s[(s * 2 + 0) * BM + t] = fp16_to_f32(wv[w0]);
                     dw_s[(s * 2 + 1) * BM + t] = fp16_to_f32(wv[w0 + 4] >> 16);
                 } else {
@@ -540,12 +573,21 @@ mma_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
 #pragma unroll
                     for (int k = 0; k < 8; ++k) q[8 + k] = wv[w0 + 9 + k];                              // block 2a+1
 #pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<uint4*>(atile + ((c ^ rsw) << 4)) = codes_to_f16x8(q[2 * c], q[2 * c + 1]);
+                    for (int j = 0; j < 2; ++j) {
+                        uint32_t av[16];
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const uint4 h = codes_to_f16x8(q[8 * j + 2 * c], q[8 * j + 2 * c + 1]);
+                            av[4 * c + 0] = h.x; av[4 * c + 1] = h.y; av[4 * c + 2] = h.z; av[4 * c + 3] = h.w;
+                        }
+                        tmem_st16(a_stage + (uint32_t)(16 * j), av);
+                    }
                     dw_s[(s * 2 + 0) * BM + t] = fp16_to_f32(wv[w0]);
                     dw_s[(s * 2 + 1) * BM + t] = fp16_to_f32(wv[w0 + 8] >> 16);
                 }
-                fence_proxy_async_smem();
+                // the A columns are written before the stage is handed to the MMA issuer
+                tmem_st_wait();
+                tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(ab_full + 8 * s);
             }
@@ -618,7 +660,7 @@ mma_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                 tc_fence_after();
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
-                    const int buf = 2 * pr + j;
+                    const int buf = PAIRWISE ? 2 * pr + j : (2 * i + j) % NBUF;
                     const float dwm = dw_s[(s * 2 + j) * BM + row];
                     const uint64_t dw2 = pack2(dwm, dwm);
                     const float4* dxs = reinterpret_cast<const float4*>(dx_s + (s * 2 + j) * NT + col0);
