@@ -605,3 +605,31 @@ def test_kernel_timeout_argument_errors(q4q):
     with pytest.raises(q4q.Q4QError):            # unknown path
         q4q.q4q_debug_mul_mat_timeout(wq, 256, 64, x, 3, 1_000_000)
     assert q4q.q4q_device_status() == 0
+
+
+def test_mul_mat_tensor_core_weight_scale_extremes(q4q):
+    """The tensor-core path at 130 tokens (128-token tiles) on rows that mix blocks whose
+    stored weight scales are fp16 subnormals, ordinary, exactly 8188, exactly 8192 and far
+    above (weights up to ~1e5, block scales up to ~5e4): every output within 1e-5 S of
+    the oracle."""
+    rng = np.random.default_rng(91)
+    ne00, ne01, ne11 = 1024, 256, 130
+    z = rng.standard_normal((ne01, ne00 // 32, 32))
+    scales = np.array([3e-7, 2e-5, 1e-3, 0.02, 1.0, 300.0, 4e4, 1.2e5])
+    pick = rng.integers(0, scales.size, size=(ne01, ne00 // 32))
+    w = (z * scales[pick][..., None]).astype(np.float32)
+    # blocks whose stored scale is exactly 8188 (amax 65504) and exactly 8192 (amax 65536)
+    w[3, :, :] = 0.0
+    w[3, :, 0] = 65504.0
+    w[3, :, 1:] = rng.uniform(-65504.0, 65504.0, size=(ne00 // 32, 31)).astype(np.float32)
+    w[4, :, 0] = -65536.0
+    w = w.reshape(ne01, ne00)
+    x = rng.standard_normal((ne11, ne00)).astype(np.float32)
+    x[5] = 0.0
+    wq = oracle.quantize_q4_0(w)
+    d = oracle.f32_from_fp16(wq.reshape(-1, 18)[:, :2].copy().view(np.uint16).reshape(-1))
+    assert np.any(d > 8188) and np.any((d > 0) & (d < 2.0 ** -14)) and np.any(d == 8188) and np.any(d == 8192)
+    got = q4q.q4q_mul_mat(dev(wq), ne00, ne01, dev(x)).cpu().numpy()
+    ref, scale = oracle.mul_mat(wq, ne00, ne01, x, nthreads=8)
+    assert_close(got, ref, scale)
+    assert q4q.q4q_device_status() == 0
