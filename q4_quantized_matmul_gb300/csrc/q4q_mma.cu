@@ -302,7 +302,9 @@ struct Cfg {
     static constexpr int RAW_STAGES = (NT <= 32 || WT == WQ8_0) ? 2 : 3;
     static constexpr int RAW_ROW = raw_row_bytes(WT);
     static constexpr int RAW_BYTES = BM * RAW_ROW;
-    static constexpr int AB_STAGES = NT <= 32 ? 3 : 4;
+    // 128-token tiles: 3 stages with 3 slab buffers, so that slab buffers repeat with the
+    // stage ring (the loops are unrolled over it); narrower tiles: 4 stages, 2 slab pairs
+    static constexpr int AB_STAGES = NT >= 128 ? 3 : 4;
     // Narrow tiles are bound by the single MMA-issuing thread: it hands TMEM over in
     // slab pairs (one check and one commit per A/B stage).  The widest tile is bound
     // by its epilogue, which frees each slab as soon as it has read it.
@@ -442,66 +444,88 @@ mma_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer
+        // A single thread issues every MMA of the CTA, so its own instruction latency is
+        // on the critical path: the stage loop is unrolled over the ring, which makes every
+        // stage slot, slab buffer and barrier parity a compile-time constant, and the B
+        // descriptors of the stage slots are formed once.
         if (lane == 0) {
             constexpr uint32_t IDESC = idesc_f16(BM, NT);
-            int g = 0;
             bool ok = true;
             constexpr bool PAIRWISE = C::PAIRWISE && !DEBUG;
+            // B descriptor of stage slot st at K offset `koff` bytes along the swizzled row:
+            // the start-address field is the shared-memory byte address / 16 and stays far
+            // from overflowing, so the slot and offset add to the first slot's descriptor
+            const uint64_t bdesc0 = smem_desc_sw128(sbase + C::OFF_B);
+#define Q4Q_BDESC(st, koff) (bdesc0 + (uint64_t)(((st) * C::B_STRIDE + (koff)) >> 4))
             if constexpr (PAIRWISE) {
                 // One hand-off per A/B stage: its two K blocks go to the two slab buffers
-                // of one pair, with one empty check and one commit for the pair (the
-                // issuing thread is on the critical path when the token tile is narrow).
+                // of one pair, with one empty check and one commit for the pair.
                 constexpr int NPAIR = NBUF / 2;
-                for (int i = 0; i < n_ab && ok; ++i) {
-                    const int s = i % AB_STAGES, pr = i % NPAIR;
-                    // both polls in flight together; the bounded waits only when one is not done
-                    const uint32_t par_a = (uint32_t)((i / AB_STAGES) & 1), par_e = (uint32_t)(((i / NPAIR) + 1) & 1);
-                    const bool ra = mbar_try_wait(ab_full + 8 * s, par_a);
-                    const bool re = i < NPAIR || mbar_try_wait(slab_empty + 8 * pr, par_e);
-                    if (!(ra && re) &&
-                        (!wait_or_abort(ab_full + 8 * s, par_a, wt) ||
-                         (i >= NPAIR && !wait_or_abort(slab_empty + 8 * pr, par_e, wt)))) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t a_col = tmem + (uint32_t)(C::A_COL0 + s * A_COLS);
-                    const uint32_t b_base = sbase + C::OFF_B + s * C::B_STRIDE;
+                static_assert(AB_STAGES % (2 * NPAIR) == 0, "slab pairs repeat with the stage ring");
+                for (int i0 = 0; i0 < n_ab && ok; i0 += AB_STAGES) {
+                    const uint32_t par_a = (uint32_t)((i0 / AB_STAGES) & 1);
 #pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-#pragma unroll
-                        for (int kk = 0; kk < 2; ++kk) {
-                            const uint32_t koff = (uint32_t)(64 * j + 32 * kk);   // bytes along B's swizzled row
-                            mma_f16_tmem_a(tmem + (uint32_t)((2 * pr + j) * NT), a_col + (uint32_t)(16 * j + 8 * kk),
-                                           smem_desc_sw128(b_base + koff), IDESC, (uint32_t)kk);
+                    for (int st = 0; st < AB_STAGES; ++st) {
+                        const int i = i0 + st;
+                        if (i >= n_ab) break;
+                        const int pr = st % NPAIR;
+                        const uint32_t par_e = (uint32_t)(((st / NPAIR) + 1) & 1);
+                        const bool ra = mbar_try_wait(ab_full + 8 * st, par_a);
+                        const bool re = i < NPAIR || mbar_try_wait(slab_empty + 8 * pr, par_e);
+                        if (!(ra && re) &&
+                            (!wait_or_abort(ab_full + 8 * st, par_a, wt) ||
+                             (i >= NPAIR && !wait_or_abort(slab_empty + 8 * pr, par_e, wt)))) {
+                            ok = false;
+                            break;
                         }
-                    }
-                    mma_commit(slab_full + 8 * pr);
-                }
-            }
-            for (int i = 0; i < n_ab && ok && !PAIRWISE; ++i) {
-                const int s = i % AB_STAGES;
-                if (!wait_or_abort(ab_full + 8 * s, (i / AB_STAGES) & 1, wt)) { ok = false; break; }
-                tc_fence_after();
-                const uint32_t a_col = tmem + (uint32_t)(C::A_COL0 + s * A_COLS);
-                const uint32_t b_base = sbase + C::OFF_B + s * C::B_STRIDE;
-                for (int j = 0; j < 2; ++j, ++g) {
-                    const int buf = g % NBUF;
-                    if (g >= NBUF && !wait_or_abort(slab_empty + 8 * buf, ((g / NBUF) + 1) & 1, wt)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
+                        tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < 2; ++kk) {
-                        const uint32_t koff = (uint32_t)(64 * j + 32 * kk);    // bytes along B's swizzled row
-                        mma_f16_tmem_a(tmem + (uint32_t)(buf * NT), a_col + (uint32_t)(16 * j + 8 * kk),
-                                       smem_desc_sw128(b_base + koff), IDESC, (uint32_t)kk);
+                        for (int j = 0; j < 2; ++j) {
+#pragma unroll
+                            for (int kk = 0; kk < 2; ++kk)
+                                mma_f16_tmem_a(tmem + (uint32_t)((2 * pr + j) * NT),
+                                               tmem + (uint32_t)(C::A_COL0 + st * A_COLS + 16 * j + 8 * kk),
+                                               Q4Q_BDESC(st, 64 * j + 32 * kk), IDESC, (uint32_t)kk);
+                        }
+                        mma_commit(slab_full + 8 * pr);
                     }
-                    mma_commit(slab_full + 8 * buf);
                 }
-                if (ok) mma_commit(ab_empty + 8 * s);
+            } else {
+                // One slab per K block, each handed back by the epilogue on its own; the
+                // slab buffers cycle with the stage ring (2 * AB_STAGES slabs a round).
+                static_assert((2 * AB_STAGES) % NBUF == 0 && ((2 * AB_STAGES) / NBUF) % 2 == 0,
+                              "slab buffers and their parities repeat with the stage ring");
+                for (int i0 = 0; i0 < n_ab && ok; i0 += AB_STAGES) {
+                    const uint32_t par_a = (uint32_t)((i0 / AB_STAGES) & 1);
+#pragma unroll
+                    for (int st = 0; st < AB_STAGES; ++st) {
+                        const int i = i0 + st;
+                        if (i >= n_ab) break;
+                        if (!wait_or_abort(ab_full + 8 * st, par_a, wt)) { ok = false; break; }
+                        tc_fence_after();
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) {
+                                const int gg = 2 * st + j;                    // slab index within the round
+                            const int buf = gg % NBUF;
+                            const uint32_t par_e = (uint32_t)(((gg / NBUF) + 1) & 1);
+                            if ((i0 > 0 || gg >= NBUF) && !wait_or_abort(slab_empty + 8 * buf, par_e, wt)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+#pragma unroll
+                            for (int kk = 0; kk < 2; ++kk)
+                                mma_f16_tmem_a(tmem + (uint32_t)(buf * NT),
+                                               tmem + (uint32_t)(C::A_COL0 + st * A_COLS + 16 * j + 8 * kk),
+                                               Q4Q_BDESC(st, 64 * j + 32 * kk), IDESC, (uint32_t)kk);
+                            mma_commit(slab_full + 8 * buf);
+                        }
+                        if (!ok) break;
+                        mma_commit(ab_empty + 8 * st);
+                    }
+                }
             }
+#undef Q4Q_BDESC
             if (!ok) {
                 // no MMA may still be reading shared memory or writing TMEM at exit
                 mma_commit(drain);
@@ -642,53 +666,68 @@ mma_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
             bool aborted = false;
             constexpr int NPAIR = NBUF / 2;
             constexpr bool PAIRWISE = C::PAIRWISE;
-            for (int i = 0; i < n_ab && !aborted; ++i) {
-                const int s = i % AB_STAGES, pr = i % NPAIR;
-                {
-                    const int g1 = 2 * i + 1;
-                    const uint32_t bar_a = ab_full + 8 * s, par_a = (uint32_t)((i / AB_STAGES) & 1);
-                    const uint32_t bar_b = PAIRWISE ? slab_full + 8 * pr : slab_full + 8 * (g1 % NBUF);
-                    const uint32_t par_b = PAIRWISE ? (uint32_t)((i / NPAIR) & 1) : (uint32_t)((g1 / NBUF) & 1);
-                    const bool ra = mbar_try_wait(bar_a, par_a);
-                    const bool rb = mbar_try_wait(bar_b, par_b);
-                    if (!__all_sync(0xffffffffu, ra && rb) &&
-                        !(warp_wait(bar_a, par_a, wt) && warp_wait(bar_b, par_b, wt))) {
-                        aborted = true;
-                        break;
-                    }
-                }
-                tc_fence_after();
+            // per-thread bases; the stage loop is unrolled over the ring (as the issuer's),
+            // so every stage slot, slab buffer and parity below is a compile-time constant
+            const float* dw_row = dw_s + row;
+            const float* dx_col = dx_s + col0;
+            const uint32_t tq_col = tq + (uint32_t)col0;
+            for (int i0 = 0; i0 < n_ab && !aborted; i0 += AB_STAGES) {
+                const uint32_t par_a = (uint32_t)((i0 / AB_STAGES) & 1);
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const int buf = PAIRWISE ? 2 * pr + j : (2 * i + j) % NBUF;
-                    const float dwm = dw_s[(s * 2 + j) * BM + row];
-                    const uint64_t dw2 = pack2(dwm, dwm);
-                    const float4* dxs = reinterpret_cast<const float4*>(dx_s + (s * 2 + j) * NT + col0);
-#pragma unroll
-                    for (int h = 0; h < C::CPW / CH; ++h) {
-                        uint32_t r[CH];
-                        tmem_ld_chunk<CH>(tq + (uint32_t)(buf * NT + col0 + h * CH), r);
-                        tmem_ld_wait();
-                        if (h == C::CPW / CH - 1 && (!PAIRWISE || j == 1)) {
-                            tc_fence_before();
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(slab_empty + 8 * (PAIRWISE ? pr : buf));
-                        }
-#pragma unroll
-                        for (int c = 0; c < CH / 4; ++c) {
-                            const float4 d4 = dxs[h * (CH / 4) + c];
-                            const int a = h * (CH / 2) + 2 * c;
-                            acc[a] = ffma2(fmul2(dw2, pack2(d4.x, d4.y)),
-                                           pack2(__uint_as_float(r[4 * c]), __uint_as_float(r[4 * c + 1])), acc[a]);
-                            acc[a + 1] = ffma2(fmul2(dw2, pack2(d4.z, d4.w)),
-                                               pack2(__uint_as_float(r[4 * c + 2]), __uint_as_float(r[4 * c + 3])),
-                                               acc[a + 1]);
+                for (int st = 0; st < AB_STAGES; ++st) {
+                    const int i = i0 + st;
+                    if (i >= n_ab) break;
+                    const int pr = st % NPAIR;
+                    {
+                        // the stage's scales, and its slabs: pairwise, the commit of its slab
+                        // pair; otherwise its second slab (the issuer commits it after the
+                        // first, and a commit completes only once every earlier MMA of that
+                        // thread has, so it implies the first)
+                        const int g1 = 2 * st + 1;
+                        const uint32_t bar_a = ab_full + 8 * st;
+                        const uint32_t bar_b = PAIRWISE ? slab_full + 8 * pr : slab_full + 8 * (g1 % NBUF);
+                        const uint32_t par_b = PAIRWISE ? (uint32_t)((st / NPAIR) & 1) : (uint32_t)((g1 / NBUF) & 1);
+                        const bool ra = mbar_try_wait(bar_a, par_a);
+                        const bool rb = mbar_try_wait(bar_b, par_b);
+                        if (!__all_sync(0xffffffffu, ra && rb) &&
+                            !(warp_wait(bar_a, par_a, wt) && warp_wait(bar_b, par_b, wt))) {
+                            aborted = true;
+                            break;
                         }
                     }
+                    tc_fence_after();
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const int buf = PAIRWISE ? 2 * pr + j : (2 * st + j) % NBUF;
+                        const float dwm = dw_row[(st * 2 + j) * BM];
+                        const uint64_t dw2 = pack2(dwm, dwm);
+                        const float4* dxs = reinterpret_cast<const float4*>(dx_col + (st * 2 + j) * NT);
+#pragma unroll
+                        for (int h = 0; h < C::CPW / CH; ++h) {
+                            uint32_t r[CH];
+                            tmem_ld_chunk<CH>(tq_col + (uint32_t)(buf * NT + h * CH), r);
+                            tmem_ld_wait();
+                            if (h == C::CPW / CH - 1 && (!PAIRWISE || j == 1)) {
+                                tc_fence_before();
+                                __syncwarp();
+                                if (lane == 0) mbar_arrive(slab_empty + 8 * (PAIRWISE ? pr : buf));
+                            }
+#pragma unroll
+                            for (int c = 0; c < CH / 4; ++c) {
+                                const float4 d4 = dxs[h * (CH / 4) + c];
+                                const int a = h * (CH / 2) + 2 * c;
+                                acc[a] = ffma2(fmul2(dw2, pack2(d4.x, d4.y)),
+                                               pack2(__uint_as_float(r[4 * c]), __uint_as_float(r[4 * c + 1])), acc[a]);
+                                acc[a + 1] = ffma2(fmul2(dw2, pack2(d4.z, d4.w)),
+                                                   pack2(__uint_as_float(r[4 * c + 2]), __uint_as_float(r[4 * c + 3])),
+                                                   acc[a + 1]);
+                            }
+                        }
+                    }
+                    // the stage's scales have been read for both of its slabs
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(ab_empty + 8 * st);
                 }
-                // the stage's scales have been read for both of its slabs
-                __syncwarp();
-                if (lane == 0) mbar_arrive(ab_empty + 8 * s);
             }
             if (!aborted && !*abort_flag && m < p.M) {
                 float* out = p.dst + (size_t)blockIdx.z * p.N * p.M;
