@@ -216,9 +216,10 @@ def run_ours(args, rank, world, local_rank):
     workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
 
     stream = torch.cuda.Stream(device=dev)
-    # decode chains launch with programmatic dependent launch: each call may start
-    # streaming its (resident, read-only) weights while the previous call finishes
-    flags = q4q.Q4Q_MUL_MAT_PDL if ne11 < 8 else 0
+    # calls launch with programmatic dependent launch: each may be scheduled, and start
+    # streaming its (resident, read-only) weights, while the previous call finishes
+    # (honoured by the GEMV and the warp-MMA kernel, ignored by the tensor-core GEMM)
+    flags = q4q.Q4Q_MUL_MAT_PDL
 
     def step(c):
         for i, (ne00, ne01) in enumerate(shapes):
@@ -619,9 +620,74 @@ def measure_batched(dev, stream, args):
                                                       "note": "fp16 exact-integer operands on tcgen05 kind::f16; "
                                                               "peak = dense f16/bf16"},
            "per_launch": per}
-    del wq, xs, ds, ws
+    del xs, ds, ws
+    torch.cuda.empty_cache()
+    if args.sweep_tokens:
+        out["token_sweep"] = measure_token_sweep(dev, stream, shapes, wq,
+                                                 [int(t) for t in args.sweep_tokens.split(",") if t])
+    del wq
     torch.cuda.empty_cache()
     return out
+
+
+def measure_token_sweep(dev, stream, shapes, wq, tokens):
+    """One step over the Llama-3-8B-shaped projection set (the 8 q4q_mul_mat calls) at
+    each token count of `tokens`: weights resident in 4 rotating copies (more than 3 x
+    L2, so every step reads them from HBM), activations N(0, 1) (seed 5), every call
+    with the workspace q4q_mul_mat_workspace_size asks for and the PDL flag, one CUDA
+    graph per weight copy.  The roofline time of a step is the larger of its Q4_0
+    weight bytes over the measured HBM bandwidth and its 2*M*N*K ops over the measured
+    dense bf16 rate; frac = that time / the measured time."""
+    import torch
+
+    import q4_quantized_matmul_gb300 as q4q
+    hbm, hbm_kind = _measured_peaks()
+    bf16, bf16_kind = _measured_bf16()
+    copies = 4
+    wsets = [wq] + [[t.clone() for t in wq] for _ in range(copies - 1)]
+    wbytes = _weights_bytes(shapes)
+    gen = torch.Generator(device="cpu").manual_seed(5)
+    rows = []
+    for ne11 in tokens:
+        xs = {k: torch.randn((ne11, k), generator=gen).to(dev) for k in sorted(set(k for k, _ in shapes))}
+        ds = [torch.empty((ne11, n), dtype=torch.float32, device=dev) for _, n in shapes]
+        ws = torch.empty(max(q4q.q4q_mul_mat_workspace_size(k, n, ne11) for k, n in shapes), dtype=torch.uint8,
+                         device=dev)
+
+        def step(c):
+            for i, (ne00, ne01) in enumerate(shapes):
+                q4q.q4q_mul_mat(wsets[c][i], ne00, ne01, xs[ne00], dst=ds[i], workspace=ws,
+                                flags=q4q.Q4Q_MUL_MAT_PDL)
+
+        graphs = [_capture(stream, lambda c=c: step(c)) for c in range(copies)]
+        reps = 20
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            for k in range(3 * copies):
+                graphs[k % copies].replay()
+            e0.record(stream)
+            for k in range(reps):
+                graphs[k % copies].replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / reps
+        ops = sum(2.0 * k * n * ne11 for k, n in shapes)
+        t_bytes = wbytes / (hbm * 1e3)             # us
+        t_ops = ops / (bf16 * 1e6)                 # us
+        path = ("GEMV or warp-MMA kernel by shape" if 2 <= ne11 <= 5 else "warp-MMA kernel" if ne11 <= 32
+                else "tensor-core GEMM")
+        rows.append({"ne11": ne11, "us_per_step": round(us, 1), "weights_gb_s": round(wbytes / us / 1e3, 1),
+                     "int8_equiv_tops": round(ops / us / 1e6, 1), "path": path,
+                     "roofline_us": round(max(t_bytes, t_ops), 1),
+                     "roofline_bound": "hbm" if t_bytes >= t_ops else "tensor",
+                     "frac": round(max(t_bytes, t_ops) / us, 4)})
+        del graphs, xs, ds, ws
+        torch.cuda.empty_cache()
+    del wsets
+    torch.cuda.empty_cache()
+    return {"workload": "llama3_8b_batched shapes (8 projections, one layer + lm_head)", "rows": rows,
+            "peaks": {"hbm_gb_s": hbm, "hbm_kind": hbm_kind, "bf16_tflops": bf16, "bf16_kind": bf16_kind},
+            "note": "us per step of 8 q4q_mul_mat calls; 1 token is the main line"}
 
 
 def _replay_ms(stream, graph, reps, calls_per_replay):
@@ -1026,6 +1092,8 @@ def main():
     ap.add_argument("--batched-tokens", type=int, default=512,
                     help="also measure the tensor-core path on the Llama-3-8B set at this many tokens (0 = skip)")
     ap.add_argument("--matrices", default="", help="comma-separated indices: only those matrices of the set")
+    ap.add_argument("--sweep-tokens", default="2,4,7,8,16,32,64",
+                    help="token counts of the batched-shape sweep (empty = skip)")
     ap.add_argument("--next-rows", type=int, default=1,
                     help="also time SwiGLU, bias/GELU, get_rows and Q8_0 weights (0 = skip)")
     ap.add_argument("--probe", default="", choices=["", "quantize", "batched", "decode-chain"],

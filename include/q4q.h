@@ -95,14 +95,18 @@ Q4Q_API q4q_status q4q_quantize_q4_0(const float* src, void* dst, int64_t ncols,
 Q4Q_API q4q_status q4q_quantize_q8_0(const float* src, void* dst, int64_t ncols, int64_t nrows,
                              q4q_stream_t stream);
 
-/* Bytes of device workspace q4q_mul_mat wants for this problem (0 when the
- * chosen kernel needs none).  The answer depends only on the shapes and on the
- * current device.  The tensor-core path (ne11 >= 8) runs in
+/* Bytes of device workspace q4q_mul_mat wants for this problem.  The answer
+ * depends only on the shapes and on the current device.  The tensor-core path
+ * (ne11 > 32) runs in
  *   B = round_up(2 * ne00 * ne11, 256) + (ne00 / 32) * round_up(ne11, 128) * 4 + 256
- * bytes (fp16 activation codes, block scales, a control word); the size returned
- * adds room for the fp32 partial sums of split-K (used when the output tiles alone
- * leave SMs idle: few tokens or few rows): round_up(s * ne01 * ne11 * 4, 256) for
- * s <= ne00 / 512 splits.  The generic path needs (ne00 / 32) * ne11 * 34 bytes. */
+ * bytes (fp16 activation codes, block scales, a control word) and the warp-MMA
+ * kernel (2 <= ne11 <= 32) in round_up(2 * ne00 * ne11, 256) + (ne00 / 32) * 256 + 256
+ * <= B bytes; the size returned adds room for split-K (used when the output tiles
+ * alone leave SMs idle: few tokens or few rows): the tensor-core path's fp32 partial
+ * sums, round_up(s * ne01 * ne11 * 4, 256) for s <= ne00 / 512 splits, or the
+ * warp-MMA kernel's split counters and partial sums, round_up(16 * T, 256) +
+ * s * T * 128 * round_up(ne11, 8) * 4 with T = ceil(ne01 / 128) and s <= min(ne00 /
+ * 256, 64).  The generic path needs (ne00 / 32) * ne11 * 34 bytes, the GEMV none. */
 Q4Q_API q4q_status q4q_mul_mat_workspace_size(int64_t ne00, int64_t ne01, int64_t ne11, size_t* bytes);
 
 /* ggml_mul_mat(src0 Q4_0 [ne00, ne01], src1 F32 [ne10, ne11]) -> dst F32 [ne01, ne11]
@@ -112,11 +116,17 @@ Q4Q_API q4q_status q4q_mul_mat_workspace_size(int64_t ne00, int64_t ne01, int64_
  * The block sums are exact; the fp32 sum over blocks may be taken in any order
  * (results differ from a serial sum by rounding only).
  * src0: device, 2-byte aligned; src1 / dst: device, 4-byte aligned.
- * ne11 < 8 streams the weights once through a fused GEMV (no workspace);
- * ne11 >= 8 runs the tensor-core GEMM on 256-byte-aligned workspace: with
- * q4q_mul_mat_workspace_size(...) bytes it splits K as planned; with less (down to
- * its split-free minimum B, see q4q_mul_mat_workspace_size) it uses fewer splits,
- * each split's partial sums being added in a fixed order.
+ * Paths (ne00 % 256 == 0 and 16-byte aligned src0 / src1 for all but the generic):
+ *   ne11 = 1, and 2..5 on matrices small enough that it is faster: a fused GEMV
+ *     that streams the weights once (no workspace);
+ *   2 <= ne11 <= 32 otherwise: the warp-MMA kernel (an activation kernel, then
+ *     per-warp mma.sync on nibbles unpacked in registers), given at least its
+ *     split-free minimum of 256-byte aligned workspace (else the GEMV below 8
+ *     tokens, Q4Q_ERR_WORKSPACE from 8);
+ *   ne11 > 32: the tensor-core GEMM (tcgen05) on 256-byte aligned workspace.
+ * With q4q_mul_mat_workspace_size(...) bytes K is split as planned; with less (down
+ * to the split-free minimum) fewer splits are used, the splits' partial sums being
+ * added in a fixed order, so a given workspace size gives the same bits every time.
  * Limits: 0 < ne00 < 2^20 (ne00 % 32 == 0), 0 <= ne01 < 2^31, 0 <= ne11 < 2^20. */
 Q4Q_API q4q_status q4q_mul_mat(const void* src0, int64_t ne00, int64_t ne01,
                        const float* src1, int64_t ne10, int64_t ne11,
@@ -135,7 +145,8 @@ Q4Q_API q4q_status q4q_debug_workspace_size(int64_t ne00, int64_t ne11, int path
  * before it on `stream` is still running; it waits for that work to complete
  * before it reads src1 or writes dst.  Valid only when no work still in flight on
  * the stream writes src0 (true for resident model weights).  Used by chains of
- * decode-step projections; honoured by the ne11 < 8 path, ignored by the others. */
+ * projections; honoured by the GEMV and the warp-MMA kernel (whose activation kernel
+ * then waits for the work before it), ignored by the tensor-core GEMM. */
 Q4Q_API q4q_status q4q_mul_mat_ex(const void* src0, int64_t ne00, int64_t ne01,
                           const float* src1, int64_t ne10, int64_t ne11,
                           float* dst, void* workspace, size_t workspace_bytes,
@@ -376,10 +387,10 @@ Q4Q_API q4q_status q4q_debug_wait_timeout(uint64_t limit_ns, q4q_stream_t stream
 
 /* Debug: the failure path of the matmul kernels' own bounded waits.  Runs the
  * kernel q4q_mul_mat would run for this problem -- path 0: the GEMV (ne11 1..7),
- * path 1: the tensor-core GEMM (ne11 >= 8) -- with every wait bounded by limit_ns
- * nanoseconds and one hand-off left out in its first CTA: that CTA's first stage
- * of weights (GEMV) or of activations (GEMM) is never copied, so the waits on it
- * run out.  Path 2 (ne11 = 1): q4q_mul_mat_chain over two links of this matrix on
+ * path 1: the tensor-core GEMM (ne11 >= 8), path 3: the warp-MMA kernel (ne11
+ * 1..32) -- with every wait bounded by limit_ns nanoseconds and one hand-off left
+ * out in its first CTA: that CTA's first stage of weights (GEMV), of activations
+ * (GEMM) or of both (warp-MMA) is never copied, so the waits on it run out.  Path 2 (ne11 = 1): q4q_mul_mat_chain over two links of this matrix on
  * the same input, whose first CTA never reports the first link finished, so the
  * other CTAs' waits before the second link run out (workspace: that of a
  * two-link chain).  The CTA that gives up records Q4Q_ERR_TIMEOUT in the device status
@@ -387,12 +398,29 @@ Q4Q_API q4q_status q4q_debug_wait_timeout(uint64_t limit_ns, q4q_stream_t stream
  * of the call that then finds the abort raised wait (bounded) for their own copies
  * in flight, free their tensor memory and return.  No GPU fault or hang is
  * involved and the context stays usable; dst is left incomplete.  Arguments as
- * q4q_mul_mat (path 1: its workspace); the problem must take the chosen path
+ * q4q_mul_mat (paths 1 and 3: its workspace); the problem must take the chosen path
  * (ne00 % 256 == 0, 16-byte aligned src0 and src1), else Q4Q_ERR_SHAPE.
- * limit_ns: 1 .. 1e9, path: 0, 1 or 2, else Q4Q_ERR_ARG. */
+ * limit_ns: 1 .. 1e9, path: 0, 1, 2 or 3, else Q4Q_ERR_ARG. */
 Q4Q_API q4q_status q4q_debug_mul_mat_timeout(const void* src0, int64_t ne00, int64_t ne01, const float* src1,
                                      int64_t ne11, float* dst, void* workspace, size_t workspace_bytes,
                                      int path, uint64_t limit_ns, q4q_stream_t stream);
+
+/* Debug: run one named path of q4q_mul_mat on a problem it accepts, whatever
+ * q4q_mul_mat itself would pick -- path 0: the GEMV (ne11 1..7, no workspace), path
+ * 1: the tensor-core GEMM (ne11 >= 8), path 3: the warp-MMA kernel (ne11 1..32).
+ * Same operation, outputs and tolerance as q4q_mul_mat.  Requires ne00 % 256 == 0 and
+ * 16-byte aligned src0 and src1 (else Q4Q_ERR_ALIGN / Q4Q_ERR_SHAPE); paths 1 and 3 take
+ * 256-byte aligned workspace of at least their split-free minimum (the same B as the
+ * tensor-core path's, see q4q_mul_mat_workspace_size; path 3 needs at most that), and
+ * split K as far as the workspace given allows.  path: 0, 1 or 3, else Q4Q_ERR_ARG;
+ * ne01 == 0 or ne11 == 0: Q4Q_ERR_SHAPE. */
+Q4Q_API q4q_status q4q_debug_mul_mat_path(const void* src0, int64_t ne00, int64_t ne01, const float* src1,
+                                  int64_t ne11, float* dst, void* workspace, size_t workspace_bytes,
+                                  int path, q4q_stream_t stream);
+
+/* Bytes of workspace q4q_debug_mul_mat_path's `path` plans its split-K for (0 for path 0). */
+Q4Q_API q4q_status q4q_debug_mul_mat_path_workspace_size(int64_t ne00, int64_t ne01, int64_t ne11, int path,
+                                                 size_t* bytes);
 
 /* Synchronizes the device, returns (in *status) the first device-side error
  * recorded since the last call (Q4Q_OK if none) and clears it.  This is where a

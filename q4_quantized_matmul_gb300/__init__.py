@@ -424,19 +424,47 @@ def q4q_debug_wait_timeout(limit_ns: int, stream=None) -> None:
     _check("q4q_debug_wait_timeout", _lib.load().q4q_debug_wait_timeout(int(limit_ns), _stream(stream)))
 
 
+def q4q_debug_mul_mat_path_workspace_size(ne00: int, ne01: int, ne11: int, path: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check("q4q_debug_mul_mat_path_workspace_size",
+           _lib.load().q4q_debug_mul_mat_path_workspace_size(ne00, ne01, ne11, int(path), ctypes.byref(n)))
+    return n.value
+
+
 @_on_tensor_device
-def q4q_debug_mul_mat_timeout(src0: torch.Tensor, ne00: int, ne01: int, src1: torch.Tensor, path: int,
-                              limit_ns: int, dst: Optional[torch.Tensor] = None,
-                              workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """Run the matmul kernel of `path` (0 = GEMV, 1 = tensor-core GEMM) with one hand-off
-    left out in its first CTA and every wait bounded by limit_ns: the waits run out,
-    q4q_device_status() then reports Q4Q_ERR_TIMEOUT (6), and dst is incomplete."""
+def q4q_debug_mul_mat_path(src0: torch.Tensor, ne00: int, ne01: int, src1: torch.Tensor, path: int,
+                           dst: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                           stream=None) -> torch.Tensor:
+    """q4q_mul_mat on one named path (0 = GEMV, 1 = tensor-core GEMM, 3 = warp-MMA
+    kernel), whatever q4q_mul_mat would pick for the shape; workspace defaults to what
+    the path plans its split-K for."""
     x = _acts_2d(src1)
     ne11, ne10 = x.shape
     if dst is None:
         dst = torch.empty((ne11, ne01), dtype=torch.float32, device=x.device)
-    need = {0: 0, 1: q4q_mul_mat_workspace_size(ne00, ne01, ne11) if path == 1 else 0,
-            2: q4q_mul_mat_chain_workspace_size(2)}.get(path, 0)
+    need = q4q_debug_mul_mat_path_workspace_size(ne00, ne01, ne11, path) if workspace is None else 0
+    ws_ptr, ws_bytes = _workspace(need, workspace, x.device)
+    _check("q4q_debug_mul_mat_path", _lib.load().q4q_debug_mul_mat_path(
+        _dev(src0, "src0", ne01 * q4_0_row_bytes(ne00)), ne00, ne01, _dev(x, "src1"), ne11,
+        _dev(dst, "dst", 4 * ne01 * ne11), ws_ptr, ws_bytes, int(path), _stream(stream)))
+    return dst
+
+
+@_on_tensor_device
+def q4q_debug_mul_mat_timeout(src0: torch.Tensor, ne00: int, ne01: int, src1: torch.Tensor, path: int,
+                              limit_ns: int, dst: Optional[torch.Tensor] = None,
+                              workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Run the matmul kernel of `path` (0 = GEMV, 1 = tensor-core GEMM, 2 = two-link chain,
+    3 = warp-MMA kernel) with one hand-off left out in its first CTA and every wait
+    bounded by limit_ns: the waits run out, q4q_device_status() then reports
+    Q4Q_ERR_TIMEOUT (6), and dst is incomplete."""
+    x = _acts_2d(src1)
+    ne11, ne10 = x.shape
+    if dst is None:
+        dst = torch.empty((ne11, ne01), dtype=torch.float32, device=x.device)
+    need = {1: q4q_mul_mat_workspace_size(ne00, ne01, ne11) if path == 1 else 0,
+            2: q4q_mul_mat_chain_workspace_size(2) if path == 2 else 0,
+            3: q4q_mul_mat_workspace_size(ne00, ne01, ne11) if path == 3 else 0}.get(path, 0)
     ws_ptr, ws_bytes = _workspace(need, workspace, x.device)
     _check("q4q_debug_mul_mat_timeout", _lib.load().q4q_debug_mul_mat_timeout(
         _dev(src0, "src0", ne01 * q4_0_row_bytes(ne00)), ne00, ne01, _dev(x, "src1"), ne11,

@@ -46,6 +46,8 @@ _SIGNATURES = {
     "q4q_debug_wait_timeout": (STATUS, [ctypes.c_uint64, P]),
     "q4q_debug_mul_mat_timeout": (STATUS, [P, I64, I64, P, I64, P, P, ctypes.c_size_t, ctypes.c_int,
                                            ctypes.c_uint64, P]),
+    "q4q_debug_mul_mat_path": (STATUS, [P, I64, I64, P, I64, P, P, ctypes.c_size_t, ctypes.c_int, P]),
+    "q4q_debug_mul_mat_path_workspace_size": (STATUS, [I64, I64, I64, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]),
     "q4q_debug_gemv_plan": (STATUS, [I64, I64, I64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                      ctypes.POINTER(I64)]),
     "q4q_debug_mma_splits": (STATUS, [I64, I64, I64, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]),

@@ -2,6 +2,9 @@
 //
 // ggml_mul_mat(Q4_0 src0 [ne00, ne01], F32 src1 [ne10, ne11]) -> F32 [ne01, ne11]
 // ("llama.cpp 深度解读" §3 "量化矩阵乘法 — 核心算子").  Paths:
+//   ne11 < 8 where the GEMV is the faster one (see prefer_gemv) -> fused GEMV (q4q_gemv.cu)
+//   2 <= ne11 <= 32, ne00 % 256 == 0, 16-byte aligned src0/src1, and a workspace
+//   of at least q4q_mul_mat_workspace_size's minimum        -> warp-MMA kernel (q4q_rmma.cu)
 //   ne11 < 8, ne00 % 256 == 0, 16-byte aligned src0/src1  -> fused GEMV (q4q_gemv.cu)
 //   ne11 >= 8 and the tensor-core GEMM accepts the shape    -> q4q_mma.cu
 //   anything else                                           -> generic two-kernel path
@@ -52,15 +55,42 @@ q4q_status check_mul_mat_shapes(int64_t ne00, int64_t ne01, int64_t ne10, int64_
 
 namespace {
 
+// Token counts the warp-MMA kernel takes (timed against the GEMV below and the
+// tensor-core GEMM above on the Llama-3-8B projection set).
+constexpr int64_t RMMA_MIN_TOKENS = 2;
+constexpr int64_t RMMA_MAX_TOKENS = 32;
+
+// Below 8 tokens the GEMV, which needs no activation kernel and no split-K, beats the
+// warp-MMA kernel's fixed cost on small matrices (CUDA-graph timings of the Llama-3-8B
+// projections with PDL: 4096 x 1024 at 2 / 3 / 4 / 5 / 7 tokens took 6.3 / 8.3 / 8.4 /
+// 10.3 / 12.4 us on the GEMV and 10.3 us on the warp-MMA kernel; 4096 x 4096 8.4 /
+// 10.3 / 12.4 against 10.4-11.6; 4096 x 128256 at 2 tokens 69.7 against 63.8).
+bool prefer_gemv(int64_t ne00, int64_t ne01, int64_t ne11) {
+    const int64_t w = ne00 * ne01;
+    if (ne11 < 2) return true;
+    if (ne11 == 2) return w < (1ll << 27);
+    return ne11 <= 5 && w * ne11 < (1ll << 26);
+}
+
+bool use_rmma(const void* src0, int64_t ne00, int64_t ne01, const float* src1, int64_t ne11, const DeviceInfo& info) {
+    return ne11 >= RMMA_MIN_TOKENS && ne11 <= RMMA_MAX_TOKENS && rmma_supported(ne00, ne01, ne11, info) &&
+           aligned(src0, 16) && aligned(src1, 16);
+}
+
 q4q_status workspace_bytes_of(int64_t ne00, int64_t ne01, int64_t ne11, bool with_splits, size_t* bytes) {
     if (!bytes) return Q4Q_ERR_NULL;
     q4q_status st = check_mul_mat_shapes(ne00, ne01, ne00, ne11);
     if (st != Q4Q_OK) return st;
     size_t need = generic_workspace_bytes(ne00, ne11);
-    if (ne11 >= 8) {
+    // the device is looked at only for shapes a device-specific kernel could take
+    if (ne11 >= 8 || (ne11 >= RMMA_MIN_TOKENS && ne00 % 256 == 0)) {
         DeviceInfo info;
         if ((st = current_device_info(&info)) != Q4Q_OK) return st;
-        if (mma_supported(ne00, ne01, ne11, info))
+        if (ne11 <= RMMA_MAX_TOKENS && !(ne11 < 8 && prefer_gemv(ne00, ne01, ne11)) &&
+            rmma_supported(ne00, ne01, ne11, info))
+            need = std::max(need, with_splits ? rmma_workspace_bytes(ne00, ne01, ne11, info)
+                                              : rmma_min_workspace_bytes(ne00, ne01, ne11));
+        if (ne11 >= 8 && mma_supported(ne00, ne01, ne11, info))
             need = std::max(need, with_splits ? mma_workspace_bytes_split(ne00, ne01, ne11, info)
                                               : mma_workspace_bytes(ne00, ne11));
     }
@@ -102,8 +132,14 @@ extern "C" q4q_status q4q_mul_mat_ex(const void* src0, int64_t ne00, int64_t ne0
     DeviceInfo info;
     if ((st = current_device_info(&info)) != Q4Q_OK) return st;
     cudaStream_t stream = (cudaStream_t)stream_;
-    if (ne11 < 8 && gemv_supported(src0, ne00, ne01, src1, ne11, info))
-        return gemv_mul_mat(src0, ne00, ne01, src1, ne11, dst, stream, info, (flags & Q4Q_MUL_MAT_PDL) != 0);
+    const bool pdl = (flags & Q4Q_MUL_MAT_PDL) != 0;
+    const bool gemv_ok = ne11 < 8 && gemv_supported(src0, ne00, ne01, src1, ne11, info);
+    if (gemv_ok && prefer_gemv(ne00, ne01, ne11))
+        return gemv_mul_mat(src0, ne00, ne01, src1, ne11, dst, stream, info, pdl);
+    if (use_rmma(src0, ne00, ne01, src1, ne11, info) && workspace && aligned(workspace, 256) &&
+        workspace_bytes >= rmma_min_workspace_bytes(ne00, ne01, ne11))
+        return rmma_mul_mat(src0, ne00, ne01, src1, ne11, dst, workspace, workspace_bytes, stream, info, pdl);
+    if (gemv_ok) return gemv_mul_mat(src0, ne00, ne01, src1, ne11, dst, stream, info, pdl);
     if (ne11 >= 8 && mma_supported(ne00, ne01, ne11, info) && aligned(src0, 16) && aligned(src1, 16)) {
         if (workspace_bytes < mma_workspace_bytes(ne00, ne11)) return Q4Q_ERR_WORKSPACE;
         if (!workspace) return Q4Q_ERR_NULL;
@@ -164,7 +200,7 @@ extern "C" q4q_status q4q_debug_wait_timeout(uint64_t limit_ns, q4q_stream_t str
 extern "C" q4q_status q4q_debug_mul_mat_timeout(const void* src0, int64_t ne00, int64_t ne01, const float* src1,
                                                 int64_t ne11, float* dst, void* workspace, size_t workspace_bytes,
                                                 int path, uint64_t limit_ns, q4q_stream_t stream_) {
-    if (path < 0 || path > 2) return Q4Q_ERR_ARG;
+    if (path < 0 || path > 3) return Q4Q_ERR_ARG;
     if (limit_ns == 0 || limit_ns > WAIT_LIMIT_NS) return Q4Q_ERR_ARG;
     q4q_status st = check_mul_mat_shapes(ne00, ne01, ne00, ne11);
     if (st != Q4Q_OK) return st;
@@ -188,12 +224,64 @@ extern "C" q4q_status q4q_debug_mul_mat_timeout(const void* src0, int64_t ne00, 
         if (!aligned(workspace, 4)) return Q4Q_ERR_ALIGN;
         return chain_launch(links, 2, workspace, stream, info, &dbg);
     }
+    if (path == 3) {
+        if (!rmma_supported(ne00, ne01, ne11, info) || !aligned(src0, 16) || !aligned(src1, 16))
+            return Q4Q_ERR_SHAPE;
+        if (workspace_bytes < rmma_min_workspace_bytes(ne00, ne01, ne11)) return Q4Q_ERR_WORKSPACE;
+        if (!workspace) return Q4Q_ERR_NULL;
+        if (!aligned(workspace, 256)) return Q4Q_ERR_ALIGN;
+        return rmma_mul_mat(src0, ne00, ne01, src1, ne11, dst, workspace, workspace_bytes, stream, info, false,
+                            &dbg);
+    }
     if (ne11 < 8 || !mma_supported(ne00, ne01, ne11, info) || !aligned(src0, 16) || !aligned(src1, 16))
         return Q4Q_ERR_SHAPE;
     if (workspace_bytes < mma_workspace_bytes(ne00, ne11)) return Q4Q_ERR_WORKSPACE;
     if (!workspace) return Q4Q_ERR_NULL;
     if (!aligned(workspace, 256)) return Q4Q_ERR_ALIGN;
     return mma_mul_mat(src0, ne00, ne01, src1, ne11, dst, workspace, workspace_bytes, stream, info, false, &dbg);
+}
+
+extern "C" q4q_status q4q_debug_mul_mat_path(const void* src0, int64_t ne00, int64_t ne01, const float* src1,
+                                             int64_t ne11, float* dst, void* workspace, size_t workspace_bytes,
+                                             int path, q4q_stream_t stream_) {
+    if (path != 0 && path != 1 && path != 3) return Q4Q_ERR_ARG;
+    q4q_status st = check_mul_mat_shapes(ne00, ne01, ne00, ne11);
+    if (st != Q4Q_OK) return st;
+    if (ne01 == 0 || ne11 == 0) return Q4Q_ERR_SHAPE;
+    if (!src0 || !src1 || !dst) return Q4Q_ERR_NULL;
+    if (!aligned(src0, 16) || !aligned(src1, 16) || !aligned(dst, 4)) return Q4Q_ERR_ALIGN;
+    DeviceInfo info;
+    if ((st = current_device_info(&info)) != Q4Q_OK) return st;
+    cudaStream_t stream = (cudaStream_t)stream_;
+    if (path == 0) {
+        if (ne11 >= 8 || !gemv_supported(src0, ne00, ne01, src1, ne11, info)) return Q4Q_ERR_SHAPE;
+        return gemv_mul_mat(src0, ne00, ne01, src1, ne11, dst, stream, info, false);
+    }
+    const bool ok = path == 1 ? (ne11 >= 8 && mma_supported(ne00, ne01, ne11, info))
+                              : rmma_supported(ne00, ne01, ne11, info);
+    if (!ok) return Q4Q_ERR_SHAPE;
+    if (workspace_bytes < (path == 1 ? mma_workspace_bytes(ne00, ne11) : rmma_min_workspace_bytes(ne00, ne01, ne11)))
+        return Q4Q_ERR_WORKSPACE;
+    if (!workspace) return Q4Q_ERR_NULL;
+    if (!aligned(workspace, 256)) return Q4Q_ERR_ALIGN;
+    if (path == 1) return mma_mul_mat(src0, ne00, ne01, src1, ne11, dst, workspace, workspace_bytes, stream, info);
+    return rmma_mul_mat(src0, ne00, ne01, src1, ne11, dst, workspace, workspace_bytes, stream, info);
+}
+
+extern "C" q4q_status q4q_debug_mul_mat_path_workspace_size(int64_t ne00, int64_t ne01, int64_t ne11, int path,
+                                                            size_t* bytes) {
+    if (!bytes) return Q4Q_ERR_NULL;
+    if (path != 0 && path != 1 && path != 3) return Q4Q_ERR_ARG;
+    q4q_status st = check_mul_mat_shapes(ne00, ne01, ne00, ne11);
+    if (st != Q4Q_OK) return st;
+    if (path == 0) {
+        *bytes = 0;
+        return Q4Q_OK;
+    }
+    DeviceInfo info;
+    if ((st = current_device_info(&info)) != Q4Q_OK) return st;
+    *bytes = path == 1 ? mma_workspace_bytes_split(ne00, ne01, ne11, info) : rmma_workspace_bytes(ne00, ne01, ne11, info);
+    return Q4Q_OK;
 }
 
 extern "C" q4q_status q4q_device_status(q4q_status* status) {
@@ -205,7 +293,7 @@ extern "C" q4q_status q4q_device_status(q4q_status* status) {
                                   gemv_swiglu_take_device_status(), gemv_w8_take_device_status(),
                                   gemv_group_take_device_status(), gemv_epi_take_device_status(),
                                   rows_take_device_status(), debug_take_device_status(),
-                                  chain_take_device_status()};
+                                  chain_take_device_status(), rmma_take_device_status()};
     unsigned int first = 0;
     for (unsigned int w : words)
         if (!first) first = w;

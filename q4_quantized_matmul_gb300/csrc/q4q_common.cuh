@@ -187,6 +187,51 @@ __device__ __forceinline__ float swiglu_f32(float gate, float up) {
     return __fmul_rn(silu_f32(gate), up);
 }
 
+// ------------------------------------------------------- operand unpacking --
+
+// Q4_0 nibble word (elements e0..e7 at bits 4e) -> 8 fp16 values (e - 8) in the
+// order [e0, e4, e1, e5, e2, e6, e3, e7]: (0x6400 | n) is the fp16 1024 + n, and
+// subtracting 1032 is exact.
+__device__ __forceinline__ uint4 nibbles_to_f16x8(uint32_t q) {
+    const uint32_t MAGIC = 0x64006400u;
+    uint32_t h[4];
+    h[0] = (q & 0x000F000Fu) | MAGIC;
+    h[1] = ((q >> 4) & 0x000F000Fu) | MAGIC;
+    h[2] = ((q >> 8) & 0x000F000Fu) | MAGIC;
+    h[3] = ((q >> 12) & 0x000F000Fu) | MAGIC;
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));   // 1032
+    uint4 out;
+    __half2 r;
+    r = __hsub2(*reinterpret_cast<__half2*>(&h[0]), bias); out.x = *reinterpret_cast<uint32_t*>(&r);
+    r = __hsub2(*reinterpret_cast<__half2*>(&h[1]), bias); out.y = *reinterpret_cast<uint32_t*>(&r);
+    r = __hsub2(*reinterpret_cast<__half2*>(&h[2]), bias); out.z = *reinterpret_cast<uint32_t*>(&r);
+    r = __hsub2(*reinterpret_cast<__half2*>(&h[3]), bias); out.w = *reinterpret_cast<uint32_t*>(&r);
+    return out;
+}
+
+__device__ __forceinline__ uint64_t pack2(float x, float y) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+    return r;
+}
+
+__device__ __forceinline__ void unpack2(uint64_t r, float& x, float& y) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(r));
+}
+
+// two fp32 lanes at once: d = a * b, d = a * b + c (each lane rounded as fmul / fmaf)
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
 // ------------------------------------------------------------- async copy --
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -307,5 +352,43 @@ __device__ __forceinline__ void record_error(unsigned int* word, unsigned int co
 }
 
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;   // one second
+
+// What a bounded wait looks at besides its barrier: the CTA's abort flag (shared
+// memory), the call's abort word (global memory) and the time limit.
+struct Waiter {
+    volatile int* flag;
+    volatile unsigned int* word;
+    uint64_t limit_ns;
+    unsigned int* status;   // the translation unit's device status word
+};
+
+// bounded wait that also gives up as soon as another role of the CTA, or another CTA
+// of the same call, has aborted
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, const Waiter& w) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait_sleep(bar, parity, SLEEP_HINT_NS)) return true;
+        if (*w.flag) return false;
+        if (*w.word != 0) {   // another CTA of this call gave up
+            *w.flag = 1;
+            return false;
+        }
+        if (global_timer_ns() - t0 > w.limit_ns) {
+            *w.flag = 1;
+            atomicExch(const_cast<unsigned int*>(w.word), 1u);
+            record_error(w.status, DEV_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// Every lane polls the barrier itself (each gets its own acquire of the completed
+// phase, which cannot advance before this warp arrives on the matching "empty"
+// barrier); a single vote makes the verdict warp-uniform.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Waiter& w) {
+    const bool ok = mbar_try_wait(bar, parity) || wait_or_abort(bar, parity, w);
+    return __all_sync(0xffffffffu, ok);
+}
 
 }  // namespace q4q

@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/q4q.h"
@@ -95,6 +96,23 @@ bool gemv_group_supported(int n, const void* const* src0, const int64_t* ne01, i
 q4q_status gemv_mul_mat_group(int n, const void* const* src0, const int64_t* ne01, int64_t ne00, const float* src1,
                               int64_t ne11, float* const* dst, cudaStream_t stream, const DeviceInfo& info,
                               bool pdl);
+
+// A 2-D tiled tensor map (no swizzle, out-of-range elements read as zero), encoded by
+// the driver entry point q4q_mma.cu looks up; false if it is missing or rejects the
+// arguments.
+bool encode_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t dim0, uint64_t dim1,
+                   uint64_t stride1_bytes, uint32_t box0, uint32_t box1);
+
+// few-token path: warp-level MMA on registers (q4q_rmma.cu)
+unsigned int rmma_take_device_status();
+bool rmma_supported(int64_t ne00, int64_t ne01, int64_t ne11, const DeviceInfo& info);
+size_t rmma_min_workspace_bytes(int64_t ne00, int64_t ne01, int64_t ne11);
+size_t rmma_workspace_bytes(int64_t ne00, int64_t ne01, int64_t ne11, const DeviceInfo& info);
+// pdl: the activation kernel is launched with programmatic dependent launch behind
+// the work before it on the stream (the caller's Q4Q_MUL_MAT_PDL)
+q4q_status rmma_mul_mat(const void* src0, int64_t ne00, int64_t ne01, const float* src1, int64_t ne11, float* dst,
+                        void* workspace, size_t workspace_bytes, cudaStream_t stream, const DeviceInfo& info,
+                        bool pdl = false, const KernelDebug* dbg = nullptr);
 
 // the GEMM's split-K count for a shape (q4q_mma.cu)
 int mma_desired_splits(int64_t ne00, int64_t ne01, int64_t ne11, const DeviceInfo& info);

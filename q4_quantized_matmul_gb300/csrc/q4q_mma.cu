@@ -173,62 +173,7 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
     return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// What a bounded wait looks at besides its barrier: the CTA's abort flag (shared
-// memory), the call's abort word (global memory) and the time limit.
-struct Waiter {
-    volatile int* flag;
-    volatile unsigned int* word;
-    uint64_t limit_ns;
-};
 
-// bounded wait that also gives up as soon as another role of the CTA, or another CTA
-// of the same call, has aborted
-__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, const Waiter& w) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
-    while (true) {
-        if (mbar_try_wait_sleep(bar, parity, SLEEP_HINT_NS)) return true;
-        if (*w.flag) return false;
-        if (*w.word != 0) {   // another CTA of this call gave up
-            *w.flag = 1;
-            return false;
-        }
-        if (global_timer_ns() - t0 > w.limit_ns) {
-            *w.flag = 1;
-            atomicExch(const_cast<unsigned int*>(w.word), 1u);
-            record_error(&g_mma_status, DEV_TIMEOUT);
-            return false;
-        }
-    }
-}
-
-// Every lane polls the barrier itself (each gets its own acquire of the completed
-// phase, which cannot advance before this warp arrives on the matching "empty"
-// barrier); a single vote makes the verdict warp-uniform.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Waiter& w) {
-    const bool ok = mbar_try_wait(bar, parity) || wait_or_abort(bar, parity, w);
-    return __all_sync(0xffffffffu, ok);
-}
-
-// Q4_0 nibble word (elements e0..e7 at bits 4e) -> 8 fp16 values (e - 8) in the
-// order [e0, e4, e1, e5, e2, e6, e3, e7]: (0x6400 | n) is the fp16 1024 + n, and
-// subtracting 1032 is exact.
-__device__ __forceinline__ uint4 nibbles_to_f16x8(uint32_t q) {
-    const uint32_t MAGIC = 0x64006400u;
-    uint32_t h[4];
-    h[0] = (q & 0x000F000Fu) | MAGIC;
-    h[1] = ((q >> 4) & 0x000F000Fu) | MAGIC;
-    h[2] = ((q >> 8) & 0x000F000Fu) | MAGIC;
-    h[3] = ((q >> 12) & 0x000F000Fu) | MAGIC;
-    const __half2 bias = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));   // 1032
-    uint4 out;
-    __half2 r;
-    r = __hsub2(*reinterpret_cast<__half2*>(&h[0]), bias); out.x = *reinterpret_cast<uint32_t*>(&r);
-    r = __hsub2(*reinterpret_cast<__half2*>(&h[1]), bias); out.y = *reinterpret_cast<uint32_t*>(&r);
-    r = __hsub2(*reinterpret_cast<__half2*>(&h[2]), bias); out.z = *reinterpret_cast<uint32_t*>(&r);
-    r = __hsub2(*reinterpret_cast<__half2*>(&h[3]), bias); out.w = *reinterpret_cast<uint32_t*>(&r);
-    return out;
-}
 
 // Two words of Q8_0 codes (elements e0..e3, e4..e7) -> 8 fp16 values in the same
 // order [e0, e4, e1, e5, e2, e6, e3, e7]: a byte permute puts e_k and e_{k+4} in
@@ -267,28 +212,6 @@ struct MmaParams {
 };
 
 
-__device__ __forceinline__ uint64_t pack2(float x, float y) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
-    return r;
-}
-
-__device__ __forceinline__ void unpack2(uint64_t r, float& x, float& y) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(r));
-}
-
-// two fp32 lanes at once: d = a * b, d = a * b + c (each lane rounded as fmul / fmaf)
-__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-
-__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
 
 template <int NT, int WT>
 struct Cfg {
@@ -364,7 +287,7 @@ mma_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
     const uint32_t drain = slab_full + 16 * NBUF;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 16);
-    const Waiter wt{abort_flag, p.abort_word, p.limit_ns};
+    const Waiter wt{abort_flag, p.abort_word, p.limit_ns, &g_mma_status};
     float* dw_s = reinterpret_cast<float*>(smem + C::OFF_DW);
     const float* dx_s = reinterpret_cast<const float*>(smem + C::OFF_DX);
 
@@ -1018,6 +941,18 @@ q4q_status mma_mul_mat(const void* src0, int64_t ne00, int64_t ne01, const float
 }
 
 size_t mma_debug_workspace_bytes(int64_t ne00, int64_t ne11) { return mma_workspace_bytes(ne00, ne11); }
+
+bool encode_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t dim0, uint64_t dim1,
+                   uint64_t stride1_bytes, uint32_t box0, uint32_t box1) {
+    if (!get_encode()) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)dim0, (cuuint64_t)dim1};
+    const cuuint64_t strides[1] = {(cuuint64_t)stride1_bytes};
+    const cuuint32_t box[2] = {box0, box1};
+    const cuuint32_t estr[2] = {1, 1};
+    return g_encode(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 q4q_status mma_debug_isums(const void* src0, const void* src1_q8_0, int64_t ne00, int64_t ne01, int64_t ne11,
                            int32_t* out, void* workspace, size_t workspace_bytes, cudaStream_t stream,

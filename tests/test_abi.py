@@ -186,11 +186,28 @@ def test_wait_timeout_argument_errors(lib):
     assert lib.q4q_debug_wait_timeout(2 * 10 ** 9, None) == 7
 
 
+def test_path_entry_argument_errors(lib):
+    P = ctypes.c_void_p
+    fake = P(0x1000)
+    f = lib.q4q_debug_mul_mat_path
+    assert f(fake, 256, 4, fake, 1, fake, None, 0, 2, None) == 7                   # the chain is no path here
+    assert f(fake, 256, 4, fake, 1, fake, None, 0, 4, None) == 7                   # unknown path
+    assert f(fake, 48, 4, fake, 1, fake, None, 0, 0, None) == 2                    # ne00 % 32
+    assert f(fake, 256, 0, fake, 1, fake, None, 0, 3, None) == 2                   # nothing to run
+    assert f(None, 256, 4, fake, 1, fake, None, 0, 3, None) == 1
+    assert f(P(0x1008), 256, 4, fake, 1, fake, None, 0, 3, None) == 3              # src0 not 16-byte aligned
+    n = ctypes.c_size_t(7)
+    g = lib.q4q_debug_mul_mat_path_workspace_size
+    assert g(256, 4, 1, 0, ctypes.byref(n)) == 0 and n.value == 0                  # the GEMV needs none
+    assert g(256, 4, 1, 5, ctypes.byref(n)) == 7
+    assert g(256, 4, 1, 3, None) == 1
+
+
 def test_kernel_timeout_entry_argument_errors(lib):
     P = ctypes.c_void_p
     fake = P(0x1000)
     f = lib.q4q_debug_mul_mat_timeout
-    assert f(fake, 256, 4, fake, 1, fake, None, 0, 3, 10 ** 6, None) == 7          # unknown path
+    assert f(fake, 256, 4, fake, 1, fake, None, 0, 4, 10 ** 6, None) == 7          # unknown path
     assert f(fake, 256, 4, fake, 1, fake, None, 0, 0, 0, None) == 7                # limit 0
     assert f(fake, 256, 4, fake, 1, fake, None, 0, 0, 2 * 10 ** 9, None) == 7      # limit above 1 s
     assert f(fake, 48, 4, fake, 1, fake, None, 0, 0, 10 ** 6, None) == 2           # ne00 % 32

@@ -570,7 +570,8 @@ def test_mul_mat_tiny_activation_scales(q4q):
 # --------------------------------------------- the kernels' own bounded waits --
 
 @pytest.mark.parametrize("path,ne00,ne01,ne11", [(0, 4096, 1024, 1), (0, 1024, 300, 3), (0, 4096, 128256, 1),
-                                                 (1, 4096, 1024, 16), (1, 1024, 256, 130), (1, 4096, 2048, 64)])
+                                                 (1, 4096, 1024, 16), (1, 1024, 256, 130), (1, 4096, 2048, 64),
+                                                 (3, 4096, 1024, 8), (3, 1024, 300, 32), (3, 4096, 128256, 2)])
 def test_kernel_timeout_path(q4q, path, ne00, ne01, ne11):
     """A matmul kernel whose first CTA never receives its first stage (a hand-off left
     out on purpose, with every wait bounded by 5 ms): the waits run out, the device
@@ -603,7 +604,9 @@ def test_kernel_timeout_argument_errors(q4q):
     with pytest.raises(q4q.Q4QError):            # limit above one second
         q4q.q4q_debug_mul_mat_timeout(wq, 256, 64, x, 0, 2_000_000_000)
     with pytest.raises(q4q.Q4QError):            # unknown path
-        q4q.q4q_debug_mul_mat_timeout(wq, 256, 64, x, 3, 1_000_000)
+        q4q.q4q_debug_mul_mat_timeout(wq, 256, 64, x, 4, 1_000_000)
+    with pytest.raises(q4q.Q4QError):            # path 3 takes at most 32 tokens
+        q4q.q4q_debug_mul_mat_timeout(wq, 256, 64, torch.zeros((33, 256), device="cuda"), 3, 1_000_000)
     assert q4q.q4q_device_status() == 0
 
 
