@@ -24,8 +24,13 @@
 // is n q 2^-24 exactly, and the fp32 sum of a block is D = 2^-24 sum_k n_k q_k with
 // |sum| <= 32 * 15 * 127 < 2^24: exact.  (mma.sync takes fp16 subnormals as they
 // are; an all-pairs check of such operands against exact dots found no difference.)
-// Then S_b = 2^24 D - 8 sum_k q_k exactly, one fp32 FMA whose operands and result are
-// integers below 2^24; the activation kernel supplies -8 sum_k q_k per block and token.
+// The -8 offset of the nibbles enters as the MMA's C operand, -8 sum_k q_k * 2^-24 (the
+// activation kernel supplies it per block and token), so the block's MMAs leave
+// 2^-24 S_b exactly (every partial sum is an integer times 2^-24 below 1 in magnitude);
+// the activation scale is stored as d_x * 2^24, and fp32(d_w * d_x * 2^24) is exactly
+// fp32(d_w d_x) * 2^24 because the product of two fp16 values is never an fp32
+// subnormal.  Per block and token pair that leaves one packed multiply and one packed
+// FMA into the running sums.
 //
 // Roles and layout (persistent CTAs, two per SM; 4 consumer warps + 1 producer warp):
 //  * A work item is one 128-row tile and one K split of it; CTA c takes items c,
@@ -37,18 +42,18 @@
 //    rows are 36 words apart, so the 8 rows x 4 words a warp loads at once fall in 32
 //    distinct banks), the activation codes of its 8 blocks (one 2-D box of 32 fp16 x
 //    8 * NG tokens per block: 64-byte token rows, conflict-free 16-byte loads) and per
-//    block and token pair {d_x, d_x', -8 sum q, -8 sum q'}.  Each 8-element group of
-//    codes is stored in the order [0,4,1,5,2,6,3,7].
+//    block and token pair {2^24 d_x, 2^24 d_x', -8 sum q 2^-24, -8 sum q' 2^-24}.  Each
+//    8-element group of codes is stored in the order [0,4,1,5,2,6,3,7].
 //  * Consumer warp w owns rows 32w .. 32w+31 (two m16 tiles).  Lane (g, t) =
 //    (lane / 4, lane % 4) takes word t of each block's 16 nibble bytes for rows g,
 //    g+8, g+16, g+24; the four fp16 pairs it unpacks to are exactly the A fragments
 //    of two k16 MMAs against codes in the order above (the dot product does not
 //    depend on the order of K).
-//  * Per block the two MMAs start from zero; S_b is formed as above and
-//    fp32(d_w d_x) * S_b added to the running sums (packed f32x2 operations).
-//  * K splits: each warp writes its partial sums, and the last split to finish a
-//    (tile, warp) slab, found with one atomic counter per slab, adds the splits in
-//    split order and writes dst.  The result is deterministic and needs no extra launch.
+//  * Per block the two MMAs start from the offset term; fp32(d_w d_x) * S_b is added to
+//    the running sums (packed f32x2 operations).
+//  * K splits: each warp writes its partial sums to the workspace, and a reduce kernel,
+//    launched behind the GEMM with programmatic dependent launch, adds the splits in
+//    split order (one thread per 4 outputs) and writes dst: deterministic.
 // Every wait is bounded and follows the abort protocol of q4q_mma.cu (the call's abort
 // word sits in the workspace and is zeroed by the activation kernel), with this file's
 // own status word.  After the roles split no barrier spans more than one warp, so a
@@ -71,7 +76,7 @@ constexpr int RAW_BYTES = RM * RAW_ROW;    // 18432
 constexpr int CWARPS = 4;                  // consumer warps, 32 rows each
 constexpr int THREADS = (CWARPS + 1) * 32;
 constexpr int CTAS_PER_SM = 2;
-constexpr int CTRL_WORDS = 64;             // control words before the split counters (word 0: abort word)
+constexpr int CTRL_WORDS = 64;             // the call's control area in the workspace (word 0: abort word)
 constexpr int MAX_TOKENS = 32;
 constexpr int DS_PAIRS = MAX_TOKENS / 2;   // token pairs per block in the scale table
 constexpr int ACT_THREADS = 256;
@@ -91,7 +96,6 @@ struct RCfg {
     static constexpr int OFF_MISC = OFF_BAR + 2 * S * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 128;   // + alignment slack
     static constexpr int ACC = 2 * NG * 4;          // partial sums per lane
-    static constexpr int FIX_CHUNK = 4 / NG > 0 ? 4 / NG : 1;   // splits whose sums are loaded at once
 };
 
 struct RParams {
@@ -100,13 +104,13 @@ struct RParams {
     int tiles, splits, items;
     float* dst;             // [N][M]
     float* part;            // splits > 1: [tile][split][warp][lane][ACC] partial sums
-    unsigned int* cnt;      // splits > 1: [tile][warp] splits finished (zero at launch)
     unsigned int* abort_word;
     uint64_t limit_ns;      // bound of every wait
     int fault;              // test only: 1 = CTA 0 leaves out the copies of its first stage
 };
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int x, int y, uint32_t bar) {
@@ -115,12 +119,22 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int 
         ::"r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(bar) : "memory");
 }
 
-// D = A * B + C, m16n8k16, fp16 operands, fp32 accumulators (row-major A, column-major B)
-__device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+// d = A * B + c, m16n8k16, fp16 operands, fp32 accumulators (row-major A, column-major
+// B); c is the pair (c0, c1) for both row halves of the fragment
+__device__ __forceinline__ void mma_16816_c(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                            uint32_t b0, uint32_t b1, float c0, float c1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%10, %11, %10, %11};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c0), "f"(c1));
+}
+
+// d += A * B
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                           uint32_t b0, uint32_t b1) {
     asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
         "{%0, %1, %2, %3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
@@ -133,13 +147,12 @@ __device__ __forceinline__ uint4 nibbles_to_subnormals(uint32_t q) {
 
 // One K block for the warp's 32 rows and all token groups.  qw[r] is the lane's nibble
 // word of row g + 8r, dw[r] that row's block scale; bblk / dsb are the block's
-// activation codes and {dx, dx', m, m'} quads in shared memory.  acc[mt][tg] holds the
-// packed pairs (row g + 16mt, tokens 2t, 2t+1) and (row g + 16mt + 8, same tokens) of
-// token group tg.
+// activation codes and {2^24 dx, 2^24 dx', m, m'} quads in shared memory.  acc[mt][tg]
+// holds the packed pairs (row g + 16mt, tokens 2t, 2t+1) and (row g + 16mt + 8, same
+// tokens) of token group tg.
 template <int NG>
 __device__ __forceinline__ void block_mma(uint64_t (&acc)[2][NG][2], const uint32_t (&qw)[4], const float (&dw)[4],
                                           const uint8_t* bblk, const uint8_t* dsb, int g, int t) {
-    const uint64_t two24 = pack2(16777216.0f, 16777216.0f);
     uint4 h[4];
 #pragma unroll
     for (int r = 0; r < 4; ++r) h[r] = nibbles_to_subnormals(qw[r]);
@@ -148,16 +161,13 @@ __device__ __forceinline__ void block_mma(uint64_t (&acc)[2][NG][2], const uint3
         const uint4 bv = *reinterpret_cast<const uint4*>(bblk + (8 * tg + g) * 64 + 16 * t);
         const float4 ds = *reinterpret_cast<const float4*>(dsb + (4 * tg + t) * 16);
         const uint64_t dxx = pack2(ds.x, ds.y);
-        const uint64_t m8 = pack2(ds.z, ds.w);
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt) {
-            float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            mma_16816(c, h[2 * mt].x, h[2 * mt + 1].x, h[2 * mt].y, h[2 * mt + 1].y, bv.x, bv.y);
+            float c[4];   // 2^-24 S_b, exact
+            mma_16816_c(c, h[2 * mt].x, h[2 * mt + 1].x, h[2 * mt].y, h[2 * mt + 1].y, bv.x, bv.y, ds.z, ds.w);
             mma_16816(c, h[2 * mt].z, h[2 * mt + 1].z, h[2 * mt].w, h[2 * mt + 1].w, bv.z, bv.w);
-            const uint64_t i0 = ffma2(pack2(c[0], c[1]), two24, m8);   // S_b, exact
-            const uint64_t i1 = ffma2(pack2(c[2], c[3]), two24, m8);
-            acc[mt][tg][0] = ffma2(fmul2(pack2(dw[2 * mt], dw[2 * mt]), dxx), i0, acc[mt][tg][0]);
-            acc[mt][tg][1] = ffma2(fmul2(pack2(dw[2 * mt + 1], dw[2 * mt + 1]), dxx), i1, acc[mt][tg][1]);
+            acc[mt][tg][0] = ffma2(fmul2(pack2(dw[2 * mt], dw[2 * mt]), dxx), pack2(c[0], c[1]), acc[mt][tg][0]);
+            acc[mt][tg][1] = ffma2(fmul2(pack2(dw[2 * mt + 1], dw[2 * mt + 1]), dxx), pack2(c[2], c[3]), acc[mt][tg][1]);
         }
     }
 }
@@ -319,62 +329,56 @@ rmma_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
             store_outputs<NG>(p, v, row0, t);
             continue;
         }
-        // split-K: publish this split's sums; the last split of the slab adds them all
-        const size_t slab = (size_t)tile * CWARPS + warp;
-        const size_t lane_off = (size_t)lane * C::ACC;
-        float* mine = p.part + (((size_t)tile * p.splits + z) * CWARPS + warp) * (32 * C::ACC) + lane_off;
+        // split-K: this split's sums go to the workspace for the reduce kernel
+        float* mine = p.part + (((size_t)tile * p.splits + z) * CWARPS + warp) * (32 * C::ACC) + (size_t)lane * C::ACC;
 #pragma unroll
         for (int i = 0; i < C::ACC; i += 4)
             *reinterpret_cast<float4*>(mine + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-        // the warp's stores are ordered before lane 0's fence by the warp barrier; the
-        // fence makes them visible device-wide before the counter moves
-        __syncwarp();
-        unsigned int prev = 0;
-        if (lane == 0) {
-            __threadfence();
-            prev = atomicAdd(p.cnt + slab, 1u);
-            if (prev == (unsigned int)(p.splits - 1)) __threadfence();   // every split's sums are visible
+    }
+}
+
+// dst from the splits' partial sums, added in split order: one thread per 4 outputs
+// (a float4 of one lane's sums).  Launched behind the GEMM with programmatic dependent
+// launch; griddepcontrol.wait returns once the GEMM has finished and its writes are visible.
+template <int NG>
+__global__ void __launch_bounds__(256)
+rmma_reduce_kernel(const float* __restrict__ part, float* __restrict__ dst, int M, int N, int tiles, int splits) {
+    using C = RCfg<NG>;
+    pdl_wait();
+    pdl_trigger();
+    constexpr int C4 = C::ACC / 4;
+    const int64_t total = (int64_t)tiles * RM * C4;
+    for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < total; i += (int64_t)gridDim.x * 256) {
+        const int c4 = (int)(i % C4);
+        const int64_t tl = i / C4;                       // tile * 128 + warp * 32 + lane
+        const int tile = (int)(tl / RM), wl = (int)(tl % RM), warp = wl >> 5, lane = wl & 31;
+        const float* src = part + ((size_t)tile * splits * CWARPS + warp) * (32 * C::ACC) + (size_t)lane * C::ACC + 4 * c4;
+        float4 sum = __ldcg(reinterpret_cast<const float4*>(src));
+        for (int z = 1; z < splits; ++z) {
+            const float4 f = __ldcg(reinterpret_cast<const float4*>(src + (size_t)z * CWARPS * 32 * C::ACC));
+            sum.x = __fadd_rn(sum.x, f.x);
+            sum.y = __fadd_rn(sum.y, f.y);
+            sum.z = __fadd_rn(sum.z, f.z);
+            sum.w = __fadd_rn(sum.w, f.w);
         }
-        prev = __shfl_sync(0xffffffffu, prev, 0);
-        if (prev != (unsigned int)(p.splits - 1)) continue;
-        float sum[C::ACC];
+        // the 4 sums are acc[mt][tg] of that lane, c4 = mt * NG + tg
+        const int mt = c4 / NG, tg = c4 % NG, g = lane >> 2, t = lane & 3;
+        const int m0 = tile * RM + 32 * warp + 16 * mt + g, n0 = 8 * tg + 2 * t;
+        const float v[4] = {sum.x, sum.y, sum.z, sum.w};
 #pragma unroll
-        for (int i = 0; i < C::ACC; ++i) sum[i] = 0.0f;
-        // FIX_CHUNK splits' loads in flight at once, added in split order
-        for (int z0 = 0; z0 < p.splits; z0 += C::FIX_CHUNK) {
-            float4 f[C::FIX_CHUNK][C::ACC / 4];
-#pragma unroll
-            for (int j = 0; j < C::FIX_CHUNK; ++j) {
-                if (z0 + j < p.splits) {
-                    const float* src =
-                        p.part + (((size_t)tile * p.splits + z0 + j) * CWARPS + warp) * (32 * C::ACC) + lane_off;
-#pragma unroll
-                    for (int i = 0; i < C::ACC / 4; ++i) f[j][i] = __ldcg(reinterpret_cast<const float4*>(src) + i);
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < C::FIX_CHUNK; ++j) {
-                if (z0 + j < p.splits) {
-#pragma unroll
-                    for (int i = 0; i < C::ACC / 4; ++i) {
-                        sum[4 * i] = __fadd_rn(sum[4 * i], f[j][i].x);
-                        sum[4 * i + 1] = __fadd_rn(sum[4 * i + 1], f[j][i].y);
-                        sum[4 * i + 2] = __fadd_rn(sum[4 * i + 2], f[j][i].z);
-                        sum[4 * i + 3] = __fadd_rn(sum[4 * i + 3], f[j][i].w);
-                    }
-                }
-            }
+        for (int e = 0; e < 4; ++e) {
+            const int m = m0 + 8 * (e >> 1), n = n0 + (e & 1);
+            if (m < M && n < N) dst[(size_t)n * M + m] = v[e];
         }
-        store_outputs<NG>(p, sum, row0, t);
     }
 }
 
 // Activation operand of one call: per (token, block) the Q8_0 codes (the same
 // quantization as q4q_quantize_q8_0: one 4-lane group per block, 8 values a lane) as
 // fp16, odd elements divided by 16, each 8-element group in the order
-// [0,4,1,5,2,6,3,7]; per block and token pair the quad {d_x, d_x', -8 sum q,
-// -8 sum q'} (tokens from N up to the next multiple of 8 get zeros); and the call's
-// control words zeroed (abort word, split counters).
+// [0,4,1,5,2,6,3,7]; per block and token pair the quad {2^24 d_x, 2^24 d_x',
+// -8 sum q 2^-24, -8 sum q' 2^-24} (tokens from N up to the next multiple of 8 get
+// zeros); and the call's control words zeroed (its abort word).
 __global__ void __launch_bounds__(ACT_THREADS)
 act_to_rmma_kernel(const float* __restrict__ x, __half* __restrict__ bmat, float* __restrict__ ds, int K, int N,
                    unsigned int* __restrict__ ctrl, int ctrl_words) {
@@ -426,8 +430,9 @@ act_to_rmma_kernel(const float* __restrict__ x, __half* __restrict__ bmat, float
         }
         if (m < total && i == 0) {
             float* quad = ds + ((int64_t)b * DS_PAIRS + n / 2) * 4;
-            quad[n & 1] = real ? fp16_to_f32(fp16_bits(d)) : 0.0f;
-            quad[2 + (n & 1)] = real ? (float)(-8 * sq) : 0.0f;
+            // 2^24 d_x and -8 sum q * 2^-24, both exact power-of-two scalings
+            quad[n & 1] = real ? fp16_to_f32(fp16_bits(d)) * 16777216.0f : 0.0f;
+            quad[2 + (n & 1)] = real ? (float)(-8 * sq) * 0x1p-24f : 0.0f;
         }
     }
 }
@@ -444,8 +449,6 @@ size_t bmat_bytes(int64_t ne00, int64_t ne11) { return round256((size_t)ne11 * n
 
 size_t ds_bytes(int64_t ne00) { return (size_t)(ne00 / QK) * DS_PAIRS * 16; }   // a multiple of 256
 
-size_t counter_bytes(int64_t ne01) { return round256((size_t)tiles_of(ne01) * CWARPS * 4); }
-
 size_t partial_bytes(int64_t ne01, int64_t ne11, int splits) {
     return splits > 1 ? (size_t)splits * (size_t)tiles_of(ne01) * RM * 8 * ng_of(ne11) * 4 : 0;
 }
@@ -454,30 +457,22 @@ size_t partial_bytes(int64_t ne01, int64_t ne11, int splits) {
 // shared-memory plan are made for (checked against the occupancy calculator once).
 int resident_ctas(const DeviceInfo& info) { return info.sm_count * CTAS_PER_SM; }
 
-// K splits of a shape, from a latency model of the persistent launch (fitted to
-// timings of the Llama-3-8B projections at 8 and 16 tokens): items run in waves of
-// `grid`; a stage takes the larger of STAGE_US (a DRAM round trip spread over the
-// ring's stages in flight) and the active CTAs' share of HBM bandwidth; a split item
-// adds FIXUP_US (publishing its partial sums, the counter, the last split's reads).
-// On 152 SMs 4096 x 1024 then takes 16 splits, 4096 x 4096 eight, 14336 x 4096 seven,
-// 4096 x 14336 and the 1002-tile lm_head none (timed best: 8, 4, 8-32, any, 1).
-int desired_splits(int64_t ne00, int64_t ne01, const DeviceInfo& info) {
-    constexpr double STAGE_US = 0.5, FIXUP_US = 3.0, HBM_BYTES_PER_US = 6.6e6;
+// K splits of a shape.  A split costs its partial sums' traffic and the reduce
+// kernel, so only shapes whose tiles leave most resident CTAs idle are split, and then
+// into the largest power of two of items that still fits one wave, each split keeping
+// at least two stages.  Timed on GB300 (CUDA graphs, 1, 2, 4, 8 or 16 splits, 8 / 16 /
+// 32 tokens), the best counts were: 4096 x 1024 (8 tiles) 8 / 8 / 8, 4096 x 4096 (32
+// tiles) 4 / 8 / 8, 14336 x 4096 (32 tiles) 8 / 8 / 8, 4096 x 14336 (112 tiles) and
+// the 1002-tile lm_head 1 / 1 / 1 -- what this rule gives, but for 4096 x 4096 at 8
+// tokens (8: 7.2 against 6.9 us).
+int desired_splits(int64_t ne00, int64_t ne01, int64_t ne11, const DeviceInfo& info) {
+    (void)ne11;
     const int64_t nst = ne00 / KST, tiles = tiles_of(ne01), grid = resident_ctas(info);
-    int best = 1;
-    double best_cost = 0.0;
-    for (int64_t s = 1; s <= std::min<int64_t>(nst, 64); ++s) {
-        const int64_t items = tiles * s;
-        const int64_t waves = (items + grid - 1) / grid;
-        const double active = (double)std::min(items, grid);
-        const double stage = std::max(STAGE_US, active * RAW_BYTES / HBM_BYTES_PER_US);
-        const double cost = (double)waves * ((double)((nst + s - 1) / s) * stage + (s > 1 ? FIXUP_US : 0.0));
-        if (s == 1 || cost < best_cost) {
-            best_cost = cost;
-            best = (int)s;
-        }
-    }
-    return best;
+    if (tiles * 3 >= grid) return 1;
+    const int64_t most = std::min<int64_t>(grid / tiles, nst / 2);
+    int s = 1;
+    while (2 * s <= most && s < 64) s *= 2;
+    return s;
 }
 
 template <int NG>
@@ -510,6 +505,18 @@ q4q_status launch_ng(const CUtensorMap& tw, const CUtensorMap& tb, const CUtenso
         (void)cudaGetLastError();
         return Q4Q_ERR_CUDA;
     }
+    q4q_status st = launch_status();
+    if (st != Q4Q_OK || p.splits == 1) return st;
+    // the splits' sums into dst, behind the GEMM
+    const int64_t threads = (int64_t)p.tiles * RM * (C::ACC / 4);
+    cfg.gridDim = dim3((unsigned)std::max<int64_t>(1, std::min<int64_t>((threads + 255) / 256, (int64_t)info.sm_count * 4)));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    if (cudaLaunchKernelEx(&cfg, rmma_reduce_kernel<NG>, (const float*)p.part, p.dst, p.M, p.N, p.tiles, p.splits) !=
+        cudaSuccess) {
+        (void)cudaGetLastError();
+        return Q4Q_ERR_CUDA;
+    }
     return launch_status();
 }
 
@@ -530,16 +537,16 @@ bool rmma_supported(int64_t ne00, int64_t ne01, int64_t ne11, const DeviceInfo& 
 }
 
 // Workspace: the fp16 activation codes, the scale quads, the control area (abort
-// word), the split counters, then the partial sums.
+// word), then the splits' partial sums.
 size_t rmma_min_workspace_bytes(int64_t ne00, int64_t ne01, int64_t ne11) {
     (void)ne01;
     return bmat_bytes(ne00, ne11) + ds_bytes(ne00) + CTRL_WORDS * 4;
 }
 
 size_t rmma_workspace_bytes(int64_t ne00, int64_t ne01, int64_t ne11, const DeviceInfo& info) {
-    const int splits = desired_splits(ne00, ne01, info);
+    const int splits = desired_splits(ne00, ne01, ne11, info);
     return rmma_min_workspace_bytes(ne00, ne01, ne11) +
-           (splits > 1 ? counter_bytes(ne01) + partial_bytes(ne01, ne11, splits) : 0);
+           (splits > 1 ? partial_bytes(ne01, ne11, splits) : 0);
 }
 
 q4q_status rmma_mul_mat(const void* src0, int64_t ne00, int64_t ne01, const float* src1, int64_t ne11, float* dst,
@@ -548,13 +555,13 @@ q4q_status rmma_mul_mat(const void* src0, int64_t ne00, int64_t ne01, const floa
     const size_t base = rmma_min_workspace_bytes(ne00, ne01, ne11);
     if (workspace_bytes < base) return Q4Q_ERR_WORKSPACE;
     // as many K splits as wanted and as the workspace holds counters and partial sums for
-    int splits = desired_splits(ne00, ne01, info);
-    while (splits > 1 && base + counter_bytes(ne01) + partial_bytes(ne01, ne11, splits) > workspace_bytes) --splits;
+    int splits = desired_splits(ne00, ne01, ne11, info);
+    while (splits > 1 && base + partial_bytes(ne01, ne11, splits) > workspace_bytes) --splits;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     __half* bmat = reinterpret_cast<__half*>(ws);
     float* ds = reinterpret_cast<float*>(ws + bmat_bytes(ne00, ne11));
     unsigned int* ctrl = reinterpret_cast<unsigned int*>(ws + bmat_bytes(ne00, ne11) + ds_bytes(ne00));
-    const int ctrl_words = CTRL_WORDS + (splits > 1 ? (int)(counter_bytes(ne01) / 4) : 0);
+    const int ctrl_words = CTRL_WORDS;
 
     // activation kernel (programmatic dependent launch behind earlier work only when asked)
     {
@@ -596,8 +603,7 @@ q4q_status rmma_mul_mat(const void* src0, int64_t ne00, int64_t ne01, const floa
     p.splits = splits;
     p.items = p.tiles * splits;
     p.dst = dst;
-    p.cnt = splits > 1 ? ctrl + CTRL_WORDS : nullptr;
-    p.part = splits > 1 ? reinterpret_cast<float*>(ws + base + counter_bytes(ne01)) : nullptr;
+    p.part = splits > 1 ? reinterpret_cast<float*>(ws + base) : nullptr;
     p.abort_word = ctrl;
     p.limit_ns = dbg ? dbg->limit_ns : WAIT_LIMIT_NS;
     p.fault = dbg ? dbg->fault : 0;
