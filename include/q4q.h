@@ -100,13 +100,13 @@ Q4Q_API q4q_status q4q_quantize_q8_0(const float* src, void* dst, int64_t ncols,
  * (ne11 > 32) runs in
  *   B = round_up(2 * ne00 * ne11, 256) + (ne00 / 32) * round_up(ne11, 128) * 4 + 256
  * bytes (fp16 activation codes, block scales, a control word) and the warp-MMA
- * kernel (2 <= ne11 <= 32) in round_up(2 * ne00 * ne11, 256) + (ne00 / 32) * 256 + 256
- * <= B bytes; the size returned adds room for split-K (used when the output tiles
- * alone leave SMs idle: few tokens or few rows): the tensor-core path's fp32 partial
- * sums, round_up(s * ne01 * ne11 * 4, 256) for s <= ne00 / 512 splits, or the
- * warp-MMA kernel's split counters and partial sums, round_up(16 * T, 256) +
- * s * T * 128 * round_up(ne11, 8) * 4 with T = ceil(ne01 / 128) and s <= min(ne00 /
- * 256, 64).  The generic path needs (ne00 / 32) * ne11 * 34 bytes, the GEMV none. */
+ * kernel (2 <= ne11 <= 32) in round_up(2 * ne00 * n8, 256) + round_up(ne00 / 2 * n8,
+ * 256) + 256 bytes, n8 = round_up(ne11, 8); the size returned adds room for split-K
+ * (used when the output tiles alone leave SMs idle: few tokens or few rows): the
+ * tensor-core path's fp32 partial sums, round_up(s * ne01 * ne11 * 4, 256) for
+ * s <= ne00 / 512 splits, or the warp-MMA kernel's, s * T * 128 * n8 * 4 bytes for T
+ * split 128-row tiles and s <= min(ne00 / 512, 64) splits.  The generic path needs
+ * (ne00 / 32) * ne11 * 34 bytes, the GEMV none. */
 Q4Q_API q4q_status q4q_mul_mat_workspace_size(int64_t ne00, int64_t ne01, int64_t ne11, size_t* bytes);
 
 /* ggml_mul_mat(src0 Q4_0 [ne00, ne01], src1 F32 [ne10, ne11]) -> dst F32 [ne01, ne11]
@@ -410,8 +410,8 @@ Q4Q_API q4q_status q4q_debug_mul_mat_timeout(const void* src0, int64_t ne00, int
  * 1: the tensor-core GEMM (ne11 >= 8), path 3: the warp-MMA kernel (ne11 1..32).
  * Same operation, outputs and tolerance as q4q_mul_mat.  Requires ne00 % 256 == 0 and
  * 16-byte aligned src0 and src1 (else Q4Q_ERR_ALIGN / Q4Q_ERR_SHAPE); paths 1 and 3 take
- * 256-byte aligned workspace of at least their split-free minimum (the same B as the
- * tensor-core path's, see q4q_mul_mat_workspace_size; path 3 needs at most that), and
+ * 256-byte aligned workspace of at least their split-free minimum (see
+ * q4q_mul_mat_workspace_size), and
  * split K as far as the workspace given allows.  path: 0, 1 or 3, else Q4Q_ERR_ARG;
  * ne01 == 0 or ne11 == 0: Q4Q_ERR_SHAPE. */
 Q4Q_API q4q_status q4q_debug_mul_mat_path(const void* src0, int64_t ne00, int64_t ne01, const float* src1,

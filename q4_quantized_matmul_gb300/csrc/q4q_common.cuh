@@ -48,10 +48,14 @@ __device__ __forceinline__ int quant_one(float x, float d, float lo, float hi) {
 }
 
 // Block scales without a division.  amax / 8 is exactly amax * 0.125 (a power of
-// two).  For amax / 127: with C = fl(1/127), q = fl(amax * C) and the exact
+// two).  For amax / 127 this is the division by a constant known in advance of
+// N. Brisebarre, J.-M. Muller and S. K. Raina, "Accelerating correctly rounded
+// floating-point division when the divisor is known in advance", IEEE Trans.
+// Computers 53(8), 2004: with C = fl(1/127), q = fl(amax * C) and the exact
 // remainder r = fma(-q, 127, amax), fma(r, C, q) is the correctly rounded
-// quotient; this was checked against IEEE division for every positive finite
-// binary32 amax (the CPU test suite re-checks a strided sample of them).
+// quotient.  Their condition for the divisor was not relied on: the identity was
+// checked against IEEE division for every positive finite binary32 amax (the CPU
+// test suite re-checks a strided sample of them).
 __device__ __forceinline__ float scale_q4(float amax) { return __fmul_rn(amax, 0.125f); }
 
 __device__ __forceinline__ float scale_q8(float amax) {

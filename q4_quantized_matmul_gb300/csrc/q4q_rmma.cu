@@ -40,10 +40,12 @@
 //    its first S stages, then waits for the activations.
 //  * A stage holds the tile's raw Q4_0 bytes (2-D TMA box of 144 bytes x 128 rows:
 //    rows are 36 words apart, so the 8 rows x 4 words a warp loads at once fall in 32
-//    distinct banks), the activation codes of its 8 blocks (one 2-D box of 32 fp16 x
-//    8 * NG tokens per block: 64-byte token rows, conflict-free 16-byte loads) and per
-//    block and token pair {2^24 d_x, 2^24 d_x', -8 sum q 2^-24, -8 sum q' 2^-24}.  Each
-//    8-element group of codes is stored in the order [0,4,1,5,2,6,3,7].
+//    distinct banks), the activation codes of its 8 blocks ([block][8 NG tokens][32]
+//    fp16: 64-byte token rows, conflict-free 16-byte loads) and per block and token
+//    pair {2^24 d_x, 2^24 d_x', -8 sum q 2^-24, -8 sum q' 2^-24}.  The activation kernel
+//    writes codes and quads in exactly that order, so each stage's share is two
+//    contiguous 1-D bulk copies (three copies a stage in all).  Each 8-element group of
+//    codes is stored in the order [0,4,1,5,2,6,3,7].
 //  * Consumer warp w owns rows 32w .. 32w+31 (two m16 tiles).  Lane (g, t) =
 //    (lane / 4, lane % 4) takes word t of each block's 16 nibble bytes for rows g,
 //    g+8, g+16, g+24; the four fp16 pairs it unpacks to are exactly the A fragments
@@ -78,7 +80,6 @@ constexpr int THREADS = (CWARPS + 1) * 32;
 constexpr int CTAS_PER_SM = 2;
 constexpr int CTRL_WORDS = 64;             // the call's control area in the workspace (word 0: abort word)
 constexpr int MAX_TOKENS = 32;
-constexpr int DS_PAIRS = MAX_TOKENS / 2;   // token pairs per block in the scale table
 constexpr int ACT_THREADS = 256;
 
 template <int NG>
@@ -99,11 +100,16 @@ struct RCfg {
 };
 
 struct RParams {
+    const uint8_t* bmat;    // activation codes, [nb][8 NG][32] fp16 (one stage = 8 blocks, contiguous)
+    const uint8_t* ds;      // scale quads, [nb][4 NG][4] fp32 (one stage contiguous)
     int M, N;               // weight rows, tokens
     int nst;                // K stages (ne00 / 256)
-    int tiles, splits, items;
+    int tiles;              // 128-row tiles
+    int whole;              // tiles 0 .. whole-1 run whole (one item each, written to dst)
+    int splits;             // the other tiles run as `splits` items each (partial sums)
+    int items;              // whole + (tiles - whole) * splits
     float* dst;             // [N][M]
-    float* part;            // splits > 1: [tile][split][warp][lane][ACC] partial sums
+    float* part;            // split tiles: [tile - whole][split][warp][lane][ACC] partial sums
     unsigned int* abort_word;
     uint64_t limit_ns;      // bound of every wait
     int fault;              // test only: 1 = CTA 0 leaves out the copies of its first stage
@@ -186,20 +192,30 @@ __device__ __forceinline__ void store_outputs(const RParams& p, const float (&v)
             }
 }
 
+// Work item `it`: its tile, its K stages [k0, k1), and its partial-sum slot (-1: a
+// whole tile, written to dst).
+struct Item {
+    int tile, k0, k1, slot;
+};
+
+__device__ __forceinline__ Item item_of(const RParams& p, int it) {
+    if (it < p.whole) return Item{it, 0, p.nst, -1};
+    const int j = it - p.whole, z = j % p.splits;
+    return Item{p.whole + j / p.splits, z * p.nst / p.splits, (z + 1) * p.nst / p.splits, j};
+}
+
+// Stage k's activation codes and scale quads: two contiguous byte ranges of the
+// workspace, laid out by the activation kernel exactly as the stage slots hold them.
 template <int NG>
-__device__ __forceinline__ void issue_acts(const CUtensorMap* tmap_b, const CUtensorMap* tmap_ds, uint32_t sbase, int s,
-                                           int k, uint32_t bar) {
+__device__ __forceinline__ void issue_acts(const RParams& p, uint32_t sbase, int s, int k, uint32_t bar) {
     using C = RCfg<NG>;
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-        tma_load_2d(sbase + C::OFF_B + s * C::B_BYTES + j * C::B_BLOCK, tmap_b, (8 * k + j) * QK, 0, bar);
-    tma_load_2d(sbase + C::OFF_DS + s * C::DS_BYTES, tmap_ds, 0, 8 * k, bar);
+    bulk_g2s(sbase + C::OFF_B + s * C::B_BYTES, p.bmat + (size_t)k * C::B_BYTES, C::B_BYTES, bar);
+    bulk_g2s(sbase + C::OFF_DS + s * C::DS_BYTES, p.ds + (size_t)k * C::DS_BYTES, C::DS_BYTES, bar);
 }
 
 template <int NG>
 __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
-rmma_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_b,
-            const __grid_constant__ CUtensorMap tmap_ds, const RParams p) {
+rmma_kernel(const __grid_constant__ CUtensorMap tmap_w, const RParams p) {
     using C = RCfg<NG>;
     constexpr int S = C::S;
     extern __shared__ uint8_t smem_dyn[];
@@ -232,9 +248,9 @@ rmma_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
             bool acts_ready = false;
             int pend[S];          // K stage of each of the first S stages (-1: left out)
             for (int it = blockIdx.x; it < p.items && ok; it += gridDim.x) {
-                const int tile = it / p.splits, z = it % p.splits;
-                const int k1 = (z + 1) * p.nst / p.splits;
-                for (int k = z * p.nst / p.splits; k < k1; ++k) {
+                const Item item = item_of(p, it);
+                const int tile = item.tile;
+                for (int k = item.k0; k < item.k1; ++k) {
                     const int s = q % S;
                     if (q >= S) {
                         if (!acts_ready) {
@@ -242,7 +258,7 @@ rmma_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
                             pdl_wait();
                             acts_ready = true;
                             for (int i = 0; i < S; ++i)
-                                if (pend[i] >= 0) issue_acts<NG>(&tmap_b, &tmap_ds, sbase, i, pend[i], full + 8 * i);
+                                if (pend[i] >= 0) issue_acts<NG>(p, sbase, i, pend[i], full + 8 * i);
                         }
                         if (!wait_or_abort(empty + 8 * s, ((q / S) + 1) & 1, wt)) {
                             ok = false;
@@ -257,14 +273,14 @@ rmma_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
                     const uint32_t bar = full + 8 * s;
                     mbar_arrive_expect_tx(bar, C::STAGE_TX);
                     tma_load_2d(sbase + s * RAW_BYTES, &tmap_w, k * RAW_ROW, tile * RM, bar);
-                    if (acts_ready) issue_acts<NG>(&tmap_b, &tmap_ds, sbase, s, k, bar);
+                    if (acts_ready) issue_acts<NG>(p, sbase, s, k, bar);
                     else pend[s] = k;
                 }
             }
             if (!acts_ready) {   // fewer than S stages in all
                 pdl_wait();
                 for (int i = 0; i < min(q, S); ++i)
-                    if (pend[i] >= 0) issue_acts<NG>(&tmap_b, &tmap_ds, sbase, i, pend[i], full + 8 * i);
+                    if (pend[i] >= 0) issue_acts<NG>(p, sbase, i, pend[i], full + 8 * i);
             }
             // no copy may still be writing this CTA's shared memory when it exits: the
             // last S stages started are the only ones nobody may have waited for
@@ -279,14 +295,14 @@ rmma_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
     const int g = lane >> 2, t = lane & 3;
     int q = 0;
     for (int it = blockIdx.x; it < p.items; it += gridDim.x) {
-        const int tile = it / p.splits, z = it % p.splits;
-        const int k1 = (z + 1) * p.nst / p.splits;
+        const Item item = item_of(p, it);
+        const int tile = item.tile;
         uint64_t acc[2][NG][2];
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
             for (int tg = 0; tg < NG; ++tg) acc[mt][tg][0] = acc[mt][tg][1] = 0ull;
-        for (int k = z * p.nst / p.splits; k < k1; ++k, ++q) {
+        for (int k = item.k0; k < item.k1; ++k, ++q) {
             const int s = q % S;
             if (!warp_wait(full + 8 * s, (q / S) & 1, wt)) return;
             // row g of this warp's first m16 tile; rows g + 8r are 8r * 36 words further
@@ -325,24 +341,26 @@ rmma_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
                 unpack2(acc[mt][tg][1], v[o + 2], v[o + 3]);
             }
         const int row0 = tile * RM + 32 * warp + g;
-        if (p.splits == 1) {
+        if (item.slot < 0) {
             store_outputs<NG>(p, v, row0, t);
             continue;
         }
         // split-K: this split's sums go to the workspace for the reduce kernel
-        float* mine = p.part + (((size_t)tile * p.splits + z) * CWARPS + warp) * (32 * C::ACC) + (size_t)lane * C::ACC;
+        float* mine = p.part + ((size_t)item.slot * CWARPS + warp) * (32 * C::ACC) + (size_t)lane * C::ACC;
 #pragma unroll
         for (int i = 0; i < C::ACC; i += 4)
             *reinterpret_cast<float4*>(mine + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
     }
 }
 
-// dst from the splits' partial sums, added in split order: one thread per 4 outputs
+// dst rows of the split tiles (tile0 onwards) from their splits' partial sums, added in
+// split order: one thread per 4 outputs
 // (a float4 of one lane's sums).  Launched behind the GEMM with programmatic dependent
 // launch; griddepcontrol.wait returns once the GEMM has finished and its writes are visible.
 template <int NG>
 __global__ void __launch_bounds__(256)
-rmma_reduce_kernel(const float* __restrict__ part, float* __restrict__ dst, int M, int N, int tiles, int splits) {
+rmma_reduce_kernel(const float* __restrict__ part, float* __restrict__ dst, int M, int N, int tile0, int tiles,
+                   int splits) {
     using C = RCfg<NG>;
     pdl_wait();
     pdl_trigger();
@@ -351,7 +369,7 @@ rmma_reduce_kernel(const float* __restrict__ part, float* __restrict__ dst, int 
     for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < total; i += (int64_t)gridDim.x * 256) {
         const int c4 = (int)(i % C4);
         const int64_t tl = i / C4;                       // tile * 128 + warp * 32 + lane
-        const int tile = (int)(tl / RM), wl = (int)(tl % RM), warp = wl >> 5, lane = wl & 31;
+        const int tile = (int)(tl / RM), wl = (int)(tl % RM), warp = wl >> 5, lane = wl & 31;   // of the split tiles
         const float* src = part + ((size_t)tile * splits * CWARPS + warp) * (32 * C::ACC) + (size_t)lane * C::ACC + 4 * c4;
         float4 sum = __ldcg(reinterpret_cast<const float4*>(src));
         for (int z = 1; z < splits; ++z) {
@@ -363,7 +381,7 @@ rmma_reduce_kernel(const float* __restrict__ part, float* __restrict__ dst, int 
         }
         // the 4 sums are acc[mt][tg] of that lane, c4 = mt * NG + tg
         const int mt = c4 / NG, tg = c4 % NG, g = lane >> 2, t = lane & 3;
-        const int m0 = tile * RM + 32 * warp + 16 * mt + g, n0 = 8 * tg + 2 * t;
+        const int m0 = (tile0 + tile) * RM + 32 * warp + 16 * mt + g, n0 = 8 * tg + 2 * t;
         const float v[4] = {sum.x, sum.y, sum.z, sum.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -377,16 +395,17 @@ rmma_reduce_kernel(const float* __restrict__ part, float* __restrict__ dst, int 
 // quantization as q4q_quantize_q8_0: one 4-lane group per block, 8 values a lane) as
 // fp16, odd elements divided by 16, each 8-element group in the order
 // [0,4,1,5,2,6,3,7]; per block and token pair the quad {2^24 d_x, 2^24 d_x',
-// -8 sum q 2^-24, -8 sum q' 2^-24} (tokens from N up to the next multiple of 8 get
-// zeros); and the call's control words zeroed (its abort word).
+// -8 sum q 2^-24, -8 sum q' 2^-24}, both laid out block by block with 8 NG token
+// columns (tokens from N up to 8 NG get zeros); and the call's control words zeroed
+// (its abort word).
 __global__ void __launch_bounds__(ACT_THREADS)
 act_to_rmma_kernel(const float* __restrict__ x, __half* __restrict__ bmat, float* __restrict__ ds, int K, int N,
                    unsigned int* __restrict__ ctrl, int ctrl_words) {
+    const int n8 = (N + 7) / 8 * 8;   // token columns of the layout (8 NG)
     pdl_wait();      // launched behind earlier work only with the caller's PDL flag
     pdl_trigger();   // the GEMM may start its weight copies now
     const int nb = K / QK;
     for (int i = blockIdx.x * ACT_THREADS + threadIdx.x; i < ctrl_words; i += gridDim.x * ACT_THREADS) ctrl[i] = 0u;
-    const int n8 = (N + 7) / 8 * 8;
     const int64_t total = (int64_t)n8 * nb * 4;
     for (int64_t m0 = (int64_t)blockIdx.x * ACT_THREADS; m0 < total; m0 += (int64_t)gridDim.x * ACT_THREADS) {
         const int64_t m = m0 + threadIdx.x;
@@ -415,7 +434,7 @@ act_to_rmma_kernel(const float* __restrict__ x, __half* __restrict__ bmat, float
 #pragma unroll
         for (int e = 0; e < 8; ++e) sq += qv[e];
         sq = warp_sum4(sq);
-        if (real) {
+        if (m < total) {   // padding tokens get zero codes
             uint32_t hw[4];
 #pragma unroll
             for (int pp = 0; pp < 4; ++pp) {
@@ -426,10 +445,10 @@ act_to_rmma_kernel(const float* __restrict__ x, __half* __restrict__ bmat, float
                 const __half2 hv = __floats2half2_rn(f0, f1);
                 hw[pp] = *reinterpret_cast<const uint32_t*>(&hv);
             }
-            *reinterpret_cast<uint4*>(bmat + (int64_t)n * K + b * QK + i * 8) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4*>(bmat + ((int64_t)b * n8 + n) * QK + i * 8) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
         }
         if (m < total && i == 0) {
-            float* quad = ds + ((int64_t)b * DS_PAIRS + n / 2) * 4;
+            float* quad = ds + ((int64_t)b * (n8 / 2) + n / 2) * 4;
             // 2^24 d_x and -8 sum q * 2^-24, both exact power-of-two scalings
             quad[n & 1] = real ? fp16_to_f32(fp16_bits(d)) * 16777216.0f : 0.0f;
             quad[2 + (n & 1)] = real ? (float)(-8 * sq) * 0x1p-24f : 0.0f;
@@ -445,12 +464,18 @@ int ng_of(int64_t ne11) { return (int)((ne11 + 7) / 8); }
 
 int64_t tiles_of(int64_t ne01) { return (ne01 + RM - 1) / RM; }
 
-size_t bmat_bytes(int64_t ne00, int64_t ne11) { return round256((size_t)ne11 * ne00 * 2); }
+size_t bmat_bytes(int64_t ne00, int64_t ne11) { return round256((size_t)ne00 * 8 * ng_of(ne11) * 2); }
 
-size_t ds_bytes(int64_t ne00) { return (size_t)(ne00 / QK) * DS_PAIRS * 16; }   // a multiple of 256
+size_t ds_bytes(int64_t ne00, int64_t ne11) { return round256((size_t)(ne00 / QK) * 4 * ng_of(ne11) * 16); }
 
-size_t partial_bytes(int64_t ne01, int64_t ne11, int splits) {
-    return splits > 1 ? (size_t)splits * (size_t)tiles_of(ne01) * RM * 8 * ng_of(ne11) * 4 : 0;
+// Which tiles run whole and how many K splits the others take.
+struct SplitPlan {
+    int64_t whole;   // tiles 0 .. whole-1
+    int splits;      // for tiles whole .. tiles-1
+};
+
+size_t partial_bytes(int64_t ne01, int64_t ne11, const SplitPlan& sp) {
+    return sp.splits > 1 ? (size_t)sp.splits * (size_t)(tiles_of(ne01) - sp.whole) * RM * 8 * ng_of(ne11) * 4 : 0;
 }
 
 // CTAs one launch keeps resident: CTAS_PER_SM per SM, as the launch bounds and the
@@ -458,26 +483,36 @@ size_t partial_bytes(int64_t ne01, int64_t ne11, int splits) {
 int resident_ctas(const DeviceInfo& info) { return info.sm_count * CTAS_PER_SM; }
 
 // K splits of a shape.  A split costs its partial sums' traffic and the reduce
-// kernel, so only shapes whose tiles leave most resident CTAs idle are split, and then
-// into the largest power of two of items that still fits one wave, each split keeping
-// at least two stages.  Timed on GB300 (CUDA graphs, 1, 2, 4, 8 or 16 splits, 8 / 16 /
-// 32 tokens), the best counts were: 4096 x 1024 (8 tiles) 8 / 8 / 8, 4096 x 4096 (32
-// tiles) 4 / 8 / 8, 14336 x 4096 (32 tiles) 8 / 8 / 8, 4096 x 14336 (112 tiles) and
-// the 1002-tile lm_head 1 / 1 / 1 -- what this rule gives, but for 4096 x 4096 at 8
-// tokens (8: 7.2 against 6.9 us).
-int desired_splits(int64_t ne00, int64_t ne01, int64_t ne11, const DeviceInfo& info) {
-    (void)ne11;
+// kernel, so only tiles that would otherwise leave most resident CTAs idle are split:
+//  * fewer tiles than a third of the resident CTAs: every tile, into the largest power
+//    of two of items that still fits one wave, each split keeping at least two stages;
+//  * more tiles than resident CTAs: the whole waves run whole, and the last, partial
+//    wave's tiles are split so that it is about as full as the others (the 1002-tile
+//    lm_head: 912 whole tiles, then 90 tiles in 3 splits each);
+//  * otherwise none.
+// Timed on GB300 (CUDA graphs, 1, 2, 4, 8 or 16 splits of every tile, 8 / 16 / 32
+// tokens), the best counts were 4096 x 1024 (8 tiles) 8 / 8 / 8, 4096 x 4096 (32 tiles)
+// 4 / 8 / 8, 14336 x 4096 (32 tiles) 8 / 8 / 8, 4096 x 14336 (112 tiles) 1 / 1 / 1 --
+// what the first and third rules give, but for 4096 x 4096 at 8 tokens (8: 7.2 against
+// 6.9 us) -- and the lm_head 1 / 1 / 1 among uniform splits.
+SplitPlan desired_plan(int64_t ne00, int64_t ne01, const DeviceInfo& info) {
     const int64_t nst = ne00 / KST, tiles = tiles_of(ne01), grid = resident_ctas(info);
-    if (tiles * 3 >= grid) return 1;
-    const int64_t most = std::min<int64_t>(grid / tiles, nst / 2);
-    int s = 1;
-    while (2 * s <= most && s < 64) s *= 2;
-    return s;
+    if (tiles * 3 < grid) {
+        const int64_t most = std::min<int64_t>(grid / tiles, nst / 2);
+        int s = 1;
+        while (2 * s <= most && s < 64) s *= 2;
+        return SplitPlan{s > 1 ? 0 : tiles, s};
+    }
+    const int64_t rem = tiles % grid;
+    if (tiles >= grid && rem > 0) {
+        const int64_t s = std::min<int64_t>({grid / rem, nst / 2, 64});
+        if (s >= 2) return SplitPlan{tiles - rem, (int)s};
+    }
+    return SplitPlan{tiles, 1};
 }
 
 template <int NG>
-q4q_status launch_ng(const CUtensorMap& tw, const CUtensorMap& tb, const CUtensorMap& td, const RParams& p,
-                     cudaStream_t stream, const DeviceInfo& info) {
+q4q_status launch_ng(const CUtensorMap& tw, const RParams& p, cudaStream_t stream, const DeviceInfo& info) {
     using C = RCfg<NG>;
     static std::atomic<int> configured[64];
     auto kern = rmma_kernel<NG>;
@@ -501,18 +536,19 @@ q4q_status launch_ng(const CUtensorMap& tw, const CUtensorMap& tb, const CUtenso
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kern, tw, tb, td, p) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, kern, tw, p) != cudaSuccess) {
         (void)cudaGetLastError();
         return Q4Q_ERR_CUDA;
     }
     q4q_status st = launch_status();
-    if (st != Q4Q_OK || p.splits == 1) return st;
-    // the splits' sums into dst, behind the GEMM
-    const int64_t threads = (int64_t)p.tiles * RM * (C::ACC / 4);
+    if (st != Q4Q_OK || p.whole == p.tiles) return st;
+    // the split tiles' sums into dst, behind the GEMM
+    const int64_t threads = (int64_t)(p.tiles - p.whole) * RM * (C::ACC / 4);
     cfg.gridDim = dim3((unsigned)std::max<int64_t>(1, std::min<int64_t>((threads + 255) / 256, (int64_t)info.sm_count * 4)));
     cfg.blockDim = dim3(256);
     cfg.dynamicSmemBytes = 0;
-    if (cudaLaunchKernelEx(&cfg, rmma_reduce_kernel<NG>, (const float*)p.part, p.dst, p.M, p.N, p.tiles, p.splits) !=
+    if (cudaLaunchKernelEx(&cfg, rmma_reduce_kernel<NG>, (const float*)p.part, p.dst, p.M, p.N, p.whole,
+                           p.tiles - p.whole, p.splits) !=
         cudaSuccess) {
         (void)cudaGetLastError();
         return Q4Q_ERR_CUDA;
@@ -540,13 +576,11 @@ bool rmma_supported(int64_t ne00, int64_t ne01, int64_t ne11, const DeviceInfo& 
 // word), then the splits' partial sums.
 size_t rmma_min_workspace_bytes(int64_t ne00, int64_t ne01, int64_t ne11) {
     (void)ne01;
-    return bmat_bytes(ne00, ne11) + ds_bytes(ne00) + CTRL_WORDS * 4;
+    return bmat_bytes(ne00, ne11) + ds_bytes(ne00, ne11) + CTRL_WORDS * 4;
 }
 
 size_t rmma_workspace_bytes(int64_t ne00, int64_t ne01, int64_t ne11, const DeviceInfo& info) {
-    const int splits = desired_splits(ne00, ne01, ne11, info);
-    return rmma_min_workspace_bytes(ne00, ne01, ne11) +
-           (splits > 1 ? partial_bytes(ne01, ne11, splits) : 0);
+    return rmma_min_workspace_bytes(ne00, ne01, ne11) + partial_bytes(ne01, ne11, desired_plan(ne00, ne01, info));
 }
 
 q4q_status rmma_mul_mat(const void* src0, int64_t ne00, int64_t ne01, const float* src1, int64_t ne11, float* dst,
@@ -554,13 +588,14 @@ q4q_status rmma_mul_mat(const void* src0, int64_t ne00, int64_t ne01, const floa
                         bool pdl, const KernelDebug* dbg) {
     const size_t base = rmma_min_workspace_bytes(ne00, ne01, ne11);
     if (workspace_bytes < base) return Q4Q_ERR_WORKSPACE;
-    // as many K splits as wanted and as the workspace holds counters and partial sums for
-    int splits = desired_splits(ne00, ne01, ne11, info);
-    while (splits > 1 && base + partial_bytes(ne01, ne11, splits) > workspace_bytes) --splits;
+    // as many K splits as wanted and as the workspace holds partial sums for
+    SplitPlan plan = desired_plan(ne00, ne01, info);
+    while (plan.splits > 1 && base + partial_bytes(ne01, ne11, plan) > workspace_bytes) --plan.splits;
+    if (plan.splits == 1) plan.whole = tiles_of(ne01);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     __half* bmat = reinterpret_cast<__half*>(ws);
     float* ds = reinterpret_cast<float*>(ws + bmat_bytes(ne00, ne11));
-    unsigned int* ctrl = reinterpret_cast<unsigned int*>(ws + bmat_bytes(ne00, ne11) + ds_bytes(ne00));
+    unsigned int* ctrl = reinterpret_cast<unsigned int*>(ws + bmat_bytes(ne00, ne11) + ds_bytes(ne00, ne11));
     const int ctrl_words = CTRL_WORDS;
 
     // activation kernel (programmatic dependent launch behind earlier work only when asked)
@@ -586,32 +621,31 @@ q4q_status rmma_mul_mat(const void* src0, int64_t ne00, int64_t ne01, const floa
     }
 
     const int NG = ng_of(ne11);
-    CUtensorMap tw, tb, td;
+    CUtensorMap tw;
     if (!encode_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, src0, (uint64_t)(ne00 / QK * Q4_0_BYTES), (uint64_t)ne01,
-                       (uint64_t)(ne00 / QK * Q4_0_BYTES), RAW_ROW, RM) ||
-        !encode_map_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, bmat, (uint64_t)ne00, (uint64_t)ne11,
-                       (uint64_t)ne00 * 2, QK, (uint32_t)(8 * NG)) ||
-        !encode_map_2d(&td, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, ds, (uint64_t)DS_PAIRS * 4, (uint64_t)(ne00 / QK),
-                       (uint64_t)DS_PAIRS * 16, (uint32_t)(16 * NG), 8))
+                       (uint64_t)(ne00 / QK * Q4_0_BYTES), RAW_ROW, RM))
         return Q4Q_ERR_CUDA;
 
     RParams p;
+    p.bmat = reinterpret_cast<const uint8_t*>(bmat);
+    p.ds = reinterpret_cast<const uint8_t*>(ds);
     p.M = (int)ne01;
     p.N = (int)ne11;
     p.nst = (int)(ne00 / KST);
     p.tiles = (int)tiles_of(ne01);
-    p.splits = splits;
-    p.items = p.tiles * splits;
+    p.whole = (int)plan.whole;
+    p.splits = plan.splits;
+    p.items = p.whole + (p.tiles - p.whole) * p.splits;
     p.dst = dst;
-    p.part = splits > 1 ? reinterpret_cast<float*>(ws + base) : nullptr;
+    p.part = plan.splits > 1 ? reinterpret_cast<float*>(ws + base) : nullptr;
     p.abort_word = ctrl;
     p.limit_ns = dbg ? dbg->limit_ns : WAIT_LIMIT_NS;
     p.fault = dbg ? dbg->fault : 0;
     switch (NG) {
-        case 1: return launch_ng<1>(tw, tb, td, p, stream, info);
-        case 2: return launch_ng<2>(tw, tb, td, p, stream, info);
-        case 3: return launch_ng<3>(tw, tb, td, p, stream, info);
-        default: return launch_ng<4>(tw, tb, td, p, stream, info);
+        case 1: return launch_ng<1>(tw, p, stream, info);
+        case 2: return launch_ng<2>(tw, p, stream, info);
+        case 3: return launch_ng<3>(tw, p, stream, info);
+        default: return launch_ng<4>(tw, p, stream, info);
     }
 }
 

@@ -67,6 +67,14 @@ def _acts(rng, ne11, ne00):
     return x
 
 
+def _least_workspace(ne00, ne11):
+    # the warp-MMA kernel's split-free minimum: fp16 codes and scale quads for the tokens
+    # padded to a multiple of 8, then the control words
+    r256 = lambda b: (b + 255) // 256 * 256
+    n8 = (ne11 + 7) // 8 * 8
+    return r256(ne00 * n8 * 2) + r256((ne00 // 32) * (n8 // 2) * 16) + 256
+
+
 def _run(q4q, wq, ne00, ne01, x, workspace=None):
     return q4q.q4q_debug_mul_mat_path(dev(wq), ne00, ne01, dev(x), 3, workspace=workspace).cpu().numpy()
 
@@ -114,8 +122,7 @@ def test_rmma_split_counts_are_deterministic(q4q, ne00, ne01, ne11):
     x = _acts(rng, ne11, ne00)
     ref, scale = oracle.mul_mat(wq, ne00, ne01, x, nthreads=8)
     full = q4q.q4q_debug_mul_mat_path_workspace_size(ne00, ne01, ne11, 3)
-    # the warp-MMA kernel's split-free minimum: fp16 codes, scale quads, control words
-    least = (ne11 * ne00 * 2 + 255) // 256 * 256 + (ne00 // 32) * 256 + 256
+    least = _least_workspace(ne00, ne11)
     assert full > least
     wq_d, x_d = dev(wq), dev(x)
     for nbytes in (full, (full + least) // 2, least):
@@ -124,6 +131,29 @@ def test_rmma_split_counts_are_deterministic(q4q, ne00, ne01, ne11):
         b = q4q.q4q_debug_mul_mat_path(wq_d, ne00, ne01, x_d, 3, workspace=ws).cpu().numpy()
         assert_close(a, ref, scale)
         np.testing.assert_array_equal(a, b)
+    assert q4q.q4q_device_status() == 0
+
+
+@pytest.mark.parametrize("ne11", [3, 8, 32])
+def test_rmma_split_tail_tiles(q4q, ne11):
+    """More 128-row tiles than resident CTAs (on 152 SMs: 351 tiles, 304 CTAs): the
+    whole waves run whole and the last wave's tiles in K splits, summed by the reduce
+    kernel.  Every row of the split tiles and a sample of the others against the oracle,
+    with the planned workspace and with the split-free minimum."""
+    rng = np.random.default_rng([ne11, 48])
+    ne00, ne01 = 1024, 350 * 128 + 37
+    wq = oracle.quantize_q4_0(_weights(rng, ne01, ne00))
+    x = _acts(rng, ne11, ne00)
+    rows = np.unique(np.concatenate([np.arange(280 * 128, ne01), rng.choice(280 * 128, 2048, replace=False)]))
+    ref, scale = oracle.mul_mat(wq.reshape(ne01, -1)[rows], ne00, rows.size, x, nthreads=8)
+    wq_d, x_d = dev(wq), dev(x)
+    full = q4q.q4q_debug_mul_mat_path_workspace_size(ne00, ne01, ne11, 3)
+    least = _least_workspace(ne00, ne11)
+    assert full > least
+    for nbytes in (full, least):
+        ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        got = q4q.q4q_debug_mul_mat_path(wq_d, ne00, ne01, x_d, 3, workspace=ws).cpu().numpy()
+        assert_close(got[:, rows], ref, scale)
     assert q4q.q4q_device_status() == 0
 
 
