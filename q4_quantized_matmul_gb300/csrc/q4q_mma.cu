@@ -84,14 +84,6 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                        uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
-}
 
 // The same MMA with its A operand in tensor memory (M = 128 rows in the 128 lanes, K along
 // the columns, two fp16 per 32-bit column).
@@ -155,6 +147,13 @@ __device__ __forceinline__ void tmem_ld_chunk(uint32_t taddr, uint32_t (&r)[CK])
 }
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// one lane of the (converged) warp, the same on every call
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred = 0;
+    asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}" : "=r"(pred));
+    return pred != 0;
+}
 
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row atoms
 // of 1024 bytes (stride-dimension offset 1024), version bits 46..48 = 0b001.
@@ -367,11 +366,15 @@ mma_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer
-        // A single thread issues every MMA of the CTA, so its own instruction latency is
-        // on the critical path: the stage loop is unrolled over the ring, which makes every
-        // stage slot, slab buffer and barrier parity a compile-time constant, and the B
-        // descriptors of the stage slots are formed once.
-        if (lane == 0) {
+        // One thread issues every MMA of the CTA, so its own instruction latency is on the
+        // critical path.  The whole warp runs the stage loop (polls with a warp vote, forms
+        // descriptors and addresses as warp-uniform values) and one elected lane issues the
+        // MMAs and commits: 64 tokens 402 -> 383 us per Llama step against a lane-0-only
+        // issuer.  The loop is unrolled over the ring, which makes every stage slot, slab
+        // buffer and barrier parity a compile-time constant, and the B descriptors of the
+        // stage slots are formed once.
+        {
+            const bool leader = elect_one();
             constexpr uint32_t IDESC = idesc_f16(BM, NT);
             bool ok = true;
             constexpr bool PAIRWISE = C::PAIRWISE && !DEBUG;
@@ -395,22 +398,25 @@ mma_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                         const uint32_t par_e = (uint32_t)(((st / NPAIR) + 1) & 1);
                         const bool ra = mbar_try_wait(ab_full + 8 * st, par_a);
                         const bool re = i < NPAIR || mbar_try_wait(slab_empty + 8 * pr, par_e);
-                        if (!(ra && re) &&
-                            (!wait_or_abort(ab_full + 8 * st, par_a, wt) ||
-                             (i >= NPAIR && !wait_or_abort(slab_empty + 8 * pr, par_e, wt)))) {
+                        if (!__all_sync(0xffffffffu, ra && re) &&
+                            (!warp_wait(ab_full + 8 * st, par_a, wt) ||
+                             (i >= NPAIR && !warp_wait(slab_empty + 8 * pr, par_e, wt)))) {
                             ok = false;
                             break;
                         }
-                        tc_fence_after();
+                        if (leader) {
+                            tc_fence_after();
 #pragma unroll
-                        for (int j = 0; j < 2; ++j) {
+                            for (int j = 0; j < 2; ++j) {
 #pragma unroll
-                            for (int kk = 0; kk < 2; ++kk)
-                                mma_f16_tmem_a(tmem + (uint32_t)((2 * pr + j) * NT),
-                                               tmem + (uint32_t)(C::A_COL0 + st * A_COLS + 16 * j + 8 * kk),
-                                               Q4Q_BDESC(st, 64 * j + 32 * kk), IDESC, (uint32_t)kk);
+                                for (int kk = 0; kk < 2; ++kk)
+                                    mma_f16_tmem_a(tmem + (uint32_t)((2 * pr + j) * NT),
+                                                   tmem + (uint32_t)(C::A_COL0 + st * A_COLS + 16 * j + 8 * kk),
+                                                   Q4Q_BDESC(st, 64 * j + 32 * kk), IDESC, (uint32_t)kk);
+                            }
+                            mma_commit(slab_full + 8 * pr);
                         }
-                        mma_commit(slab_full + 8 * pr);
+                        __syncwarp();
                     }
                 }
             } else {
@@ -424,36 +430,40 @@ mma_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                     for (int st = 0; st < AB_STAGES; ++st) {
                         const int i = i0 + st;
                         if (i >= n_ab) break;
-                        if (!wait_or_abort(ab_full + 8 * st, par_a, wt)) { ok = false; break; }
-                        tc_fence_after();
+                        if (!warp_wait(ab_full + 8 * st, par_a, wt)) { ok = false; break; }
 #pragma unroll
                         for (int j = 0; j < 2; ++j) {
                                 const int gg = 2 * st + j;                    // slab index within the round
                             const int buf = gg % NBUF;
                             const uint32_t par_e = (uint32_t)(((gg / NBUF) + 1) & 1);
-                            if ((i0 > 0 || gg >= NBUF) && !wait_or_abort(slab_empty + 8 * buf, par_e, wt)) {
+                            if ((i0 > 0 || gg >= NBUF) && !warp_wait(slab_empty + 8 * buf, par_e, wt)) {
                                 ok = false;
                                 break;
                             }
-                            tc_fence_after();
+                            if (leader) {
+                                tc_fence_after();
 #pragma unroll
-                            for (int kk = 0; kk < 2; ++kk)
-                                mma_f16_tmem_a(tmem + (uint32_t)(buf * NT),
-                                               tmem + (uint32_t)(C::A_COL0 + st * A_COLS + 16 * j + 8 * kk),
-                                               Q4Q_BDESC(st, 64 * j + 32 * kk), IDESC, (uint32_t)kk);
-                            mma_commit(slab_full + 8 * buf);
+                                for (int kk = 0; kk < 2; ++kk)
+                                    mma_f16_tmem_a(tmem + (uint32_t)(buf * NT),
+                                                   tmem + (uint32_t)(C::A_COL0 + st * A_COLS + 16 * j + 8 * kk),
+                                                   Q4Q_BDESC(st, 64 * j + 32 * kk), IDESC, (uint32_t)kk);
+                                mma_commit(slab_full + 8 * buf);
+                            }
+                            __syncwarp();
                         }
                         if (!ok) break;
-                        mma_commit(ab_empty + 8 * st);
+                        if (leader) mma_commit(ab_empty + 8 * st);
+                        __syncwarp();
                     }
                 }
             }
 #undef Q4Q_BDESC
-            if (!ok) {
+            if (!ok && leader) {
                 // no MMA may still be reading shared memory or writing TMEM at exit
                 mma_commit(drain);
                 mbar_wait_bounded(drain, 0, p.limit_ns);
             }
+            __syncwarp();
         }
     } else if (warp >= 4 && warp < 8) {
         // ---------------- dequantizers: thread t <-> tile row t = TMEM lane t (warp 4 + q
