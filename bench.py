@@ -235,13 +235,17 @@ def run_ours(args, rank, world, local_rank):
         with torch.cuda.graph(g, stream=stream):
             step(c)
         graphs.append(g)
-    multi = torch.cuda.CUDAGraph()          # one step per weight copy, in order
+    # one step per weight copy, in order, args.graph_rounds times over (a decode token
+    # chains hundreds of launches in one graph; PDL does not reach across graph launches)
+    rounds = max(1, args.graph_rounds)
+    multi = torch.cuda.CUDAGraph()
     with torch.cuda.graph(multi, stream=stream):
-        for c in range(copies):
-            step(c)
+        for _ in range(rounds):
+            for c in range(copies):
+                step(c)
     torch.cuda.synchronize()
 
-    graph_steps = copies if ne11 < 8 else 1
+    graph_steps = copies * rounds if ne11 < 8 else 1
 
     def run_steps(multi_graph, single_graphs, k_steps):
         """Exactly k_steps steps: whole multi-step graphs, then single steps."""
@@ -252,7 +256,7 @@ def run_ours(args, rank, world, local_rank):
         for _ in range(k_steps // graph_steps):
             multi_graph.replay()
         for k in range(k_steps % graph_steps):
-            single_graphs[k].replay()
+            single_graphs[k % copies].replay()
 
     def barrier():
         if world > 1:
@@ -357,8 +361,9 @@ def run_ours(args, rank, world, local_rank):
         egraphs.append(g)
     emulti = torch.cuda.CUDAGraph()
     with torch.cuda.graph(emulti, stream=stream):
-        for c in range(copies):
-            e2e_step(c)
+        for _ in range(rounds):
+            for c in range(copies):
+                e2e_step(c)
     with torch.cuda.stream(stream):
         for k in range(args.warmup):
             egraphs[k % copies].replay()
@@ -409,8 +414,8 @@ def run_ours(args, rank, world, local_rank):
             "q4_0_weight_bytes_per_step": wbytes,
             "l2_policy": "inputs larger than L2: %d rotating copies of the Q4_0 weights (%.0f MB, L2 %.0f MB)" % (
                 copies, copies * wbytes / 1e6, l2 / 1e6),
-            "launch": "%d q4q_mul_mat calls per step; CUDA graphs of %d consecutive steps (one per weight copy), "
-                      "programmatic dependent launch between all calls of a graph" % (nmat, copies)
+            "launch": "%d q4q_mul_mat calls per step; CUDA graphs of %d consecutive steps (the %d weight copies in "
+                      "turn), programmatic dependent launch between all calls of a graph" % (nmat, graph_steps, copies)
                       if ne11 < 8 else "%d q4q_mul_mat calls per step, one CUDA graph per step" % nmat,
             "graph_steps": graph_steps,
             "parallelism": "replicas" if world > 1 else "single GPU",
@@ -1092,6 +1097,8 @@ def main():
     ap.add_argument("--batched-tokens", type=int, default=512,
                     help="also measure the tensor-core path on the Llama-3-8B set at this many tokens (0 = skip)")
     ap.add_argument("--matrices", default="", help="comma-separated indices: only those matrices of the set")
+    ap.add_argument("--graph-rounds", type=int, default=2,
+                    help="decode steps: rounds over the weight copies captured in one CUDA graph")
     ap.add_argument("--sweep-tokens", default="2,4,7,8,16,32,64",
                     help="token counts of the batched-shape sweep (empty = skip)")
     ap.add_argument("--next-rows", type=int, default=1,
