@@ -679,7 +679,7 @@ def measure_token_sweep(dev, stream, shapes, wq, tokens):
         ops = sum(2.0 * k * n * ne11 for k, n in shapes)
         t_bytes = wbytes / (hbm * 1e3)             # us
         t_ops = ops / (bf16 * 1e6)                 # us
-        path = ("GEMV or warp-MMA kernel by shape" if 2 <= ne11 <= 5 else "warp-MMA kernel" if ne11 <= 32
+        path = ("GEMV (q, k, v, o) and warp-MMA kernel" if 2 <= ne11 <= 3 else "warp-MMA kernel" if ne11 <= 32
                 else "tensor-core GEMM")
         rows.append({"ne11": ne11, "us_per_step": round(us, 1), "weights_gb_s": round(wbytes / us / 1e3, 1),
                      "int8_equiv_tops": round(ops / us / 1e6, 1), "path": path,

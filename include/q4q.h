@@ -117,8 +117,8 @@ Q4Q_API q4q_status q4q_mul_mat_workspace_size(int64_t ne00, int64_t ne01, int64_
  * (results differ from a serial sum by rounding only).
  * src0: device, 2-byte aligned; src1 / dst: device, 4-byte aligned.
  * Paths (ne00 % 256 == 0 and 16-byte aligned src0 / src1 for all but the generic):
- *   ne11 = 1, and 2..5 on matrices small enough that it is faster: a fused GEMV
- *     that streams the weights once (no workspace);
+ *   ne11 = 1, and 2..3 on matrices of at most 2^24 weights (where it is faster): a
+ *     fused GEMV that streams the weights once (no workspace);
  *   2 <= ne11 <= 32 otherwise: the warp-MMA kernel (an activation kernel, then
  *     per-warp mma.sync on nibbles unpacked in registers), given at least its
  *     split-free minimum of 256-byte aligned workspace (else the GEMV below 8

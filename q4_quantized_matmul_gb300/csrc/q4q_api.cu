@@ -2,7 +2,8 @@
 //
 // ggml_mul_mat(Q4_0 src0 [ne00, ne01], F32 src1 [ne10, ne11]) -> F32 [ne01, ne11]
 // ("llama.cpp 深度解读" §3 "量化矩阵乘法 — 核心算子").  Paths:
-//   ne11 < 8 where the GEMV is the faster one (see prefer_gemv) -> fused GEMV (q4q_gemv.cu)
+//   ne11 = 1, or 2..3 on matrices of at most 2^24 weights (prefer_gemv)
+//                                                          -> fused GEMV (q4q_gemv.cu)
 //   2 <= ne11 <= 32, ne00 % 256 == 0, 16-byte aligned src0/src1, and a workspace
 //   of at least q4q_mul_mat_workspace_size's minimum        -> warp-MMA kernel (q4q_rmma.cu)
 //   ne11 < 8, ne00 % 256 == 0, 16-byte aligned src0/src1  -> fused GEMV (q4q_gemv.cu)
@@ -61,15 +62,13 @@ constexpr int64_t RMMA_MIN_TOKENS = 2;
 constexpr int64_t RMMA_MAX_TOKENS = 32;
 
 // Below 8 tokens the GEMV, which needs no activation kernel and no split-K, beats the
-// warp-MMA kernel's fixed cost on small matrices (CUDA-graph timings of the Llama-3-8B
-// projections with PDL: 4096 x 1024 at 2 / 3 / 4 / 5 / 7 tokens took 6.3 / 8.3 / 8.4 /
-// 10.3 / 12.4 us on the GEMV and 10.3 us on the warp-MMA kernel; 4096 x 4096 8.4 /
-// 10.3 / 12.4 against 10.4-11.6; 4096 x 128256 at 2 tokens 69.7 against 63.8).
+// warp-MMA kernel's fixed cost on small matrices at 2 or 3 tokens, and nowhere else
+// (chains of 8 calls with PDL in CUDA graphs, us per call, GEMV / warp-MMA:
+// 4096 x 1024 at 2 / 3 / 4 / 5 / 7 tokens 3.8 / 4.6 / 5.9 / 6.0 / 8.2 against 5.7;
+// 4096 x 4096 5.4 / 5.9 / 8.0 / 9.0 / 12.3 against 7.0; 4096 x 14336 at 2 tokens 12.1
+// against 11.9; 14336 x 4096 14.0 against 13.4; 4096 x 128256 63.6 against 52.1).
 bool prefer_gemv(int64_t ne00, int64_t ne01, int64_t ne11) {
-    const int64_t w = ne00 * ne01;
-    if (ne11 < 2) return true;
-    if (ne11 == 2) return w < (1ll << 27);
-    return ne11 <= 5 && w * ne11 < (1ll << 26);
+    return ne11 < 2 || (ne11 <= 3 && ne00 * ne01 <= (1ll << 24));
 }
 
 bool use_rmma(const void* src0, int64_t ne00, int64_t ne01, const float* src1, int64_t ne11, const DeviceInfo& info) {
