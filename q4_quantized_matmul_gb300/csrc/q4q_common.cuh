@@ -194,22 +194,26 @@ __device__ __forceinline__ float swiglu_f32(float gate, float up) {
 // ------------------------------------------------------- operand unpacking --
 
 // Q4_0 nibble word (elements e0..e7 at bits 4e) -> 8 fp16 values (e - 8) in the
-// order [e0, e4, e1, e5, e2, e6, e3, e7]: (0x6400 | n) is the fp16 1024 + n, and
-// subtracting 1032 is exact.
+// order [e0, e4, e1, e5, e2, e6, e3, e7].  A low nibble n OR-ed into 0x6400 is the
+// fp16 1024 + n, and subtracting 1032 is exact; a high nibble left in place gives
+// 1024 + 16 n, and (1024 + 16 n) / 16 - 72 = n - 8 is one exact HFMA2.
 __device__ __forceinline__ uint4 nibbles_to_f16x8(uint32_t q) {
     const uint32_t MAGIC = 0x64006400u;
+    const uint32_t q8 = q >> 8;
     uint32_t h[4];
-    h[0] = (q & 0x000F000Fu) | MAGIC;
-    h[1] = ((q >> 4) & 0x000F000Fu) | MAGIC;
-    h[2] = ((q >> 8) & 0x000F000Fu) | MAGIC;
-    h[3] = ((q >> 12) & 0x000F000Fu) | MAGIC;
-    const __half2 bias = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));   // 1032
+    h[0] = (q & 0x000F000Fu) | MAGIC;    // {1024 + e0, 1024 + e4}
+    h[1] = (q & 0x00F000F0u) | MAGIC;    // {1024 + 16 e1, 1024 + 16 e5}
+    h[2] = (q8 & 0x000F000Fu) | MAGIC;   // {1024 + e2, 1024 + e6}
+    h[3] = (q8 & 0x00F000F0u) | MAGIC;   // {1024 + 16 e3, 1024 + 16 e7}
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));       // 1032
+    const __half2 sixteenth = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));  // 1/16
+    const __half2 m72 = __halves2half2(__ushort_as_half(0xD480), __ushort_as_half(0xD480));        // -72
     uint4 out;
     __half2 r;
     r = __hsub2(*reinterpret_cast<__half2*>(&h[0]), bias); out.x = *reinterpret_cast<uint32_t*>(&r);
-    r = __hsub2(*reinterpret_cast<__half2*>(&h[1]), bias); out.y = *reinterpret_cast<uint32_t*>(&r);
+    r = __hfma2(*reinterpret_cast<__half2*>(&h[1]), sixteenth, m72); out.y = *reinterpret_cast<uint32_t*>(&r);
     r = __hsub2(*reinterpret_cast<__half2*>(&h[2]), bias); out.z = *reinterpret_cast<uint32_t*>(&r);
-    r = __hsub2(*reinterpret_cast<__half2*>(&h[3]), bias); out.w = *reinterpret_cast<uint32_t*>(&r);
+    r = __hfma2(*reinterpret_cast<__half2*>(&h[3]), sixteenth, m72); out.w = *reinterpret_cast<uint32_t*>(&r);
     return out;
 }
 
