@@ -608,37 +608,42 @@ __device__ __forceinline__ void gemv_body(const uint8_t* __restrict__ w, const u
 
 
 // The kernels share one body and one signature (w2 is unused unless dual; the
-// group kernel takes its pointers from p.grp).
+// group kernel takes its pointers from p.grp).  With one or two register-resident
+// activation pairs a lane (K <= 4096 at one token) three CTAs fit in an SM's registers
+// (69 of them a thread, none spilled), so that a decode chain's next kernel can start a
+// CTA beside this one's two and prefetch its weights (see plan_gemv).
+constexpr int gemv_min_ctas(int ppl) { return (ppl >= 1 && ppl <= 2) ? 3 : (ppl <= 3 ? 2 : 1); }
+
 template <int T, int LPR, int PPL, int CL>
-__global__ void __launch_bounds__(THREADS, PPL <= 3 ? 2 : 1)
+__global__ void __launch_bounds__(THREADS, gemv_min_ctas(PPL))
 gemv_q4_0_kernel(const uint8_t* __restrict__ w, const uint8_t* __restrict__ w2, const float* __restrict__ x,
                  float* __restrict__ dst, const GemvParams p) {
     gemv_body<WQ4_0, T, LPR, PPL, CL, M_SINGLE>(w, w2, x, dst, p);
 }
 
 template <int T, int LPR, int PPL, int CL>
-__global__ void __launch_bounds__(THREADS, PPL <= 3 ? 2 : 1)
+__global__ void __launch_bounds__(THREADS, gemv_min_ctas(PPL))
 gemv_q4_0_swiglu_kernel(const uint8_t* __restrict__ w, const uint8_t* __restrict__ w2, const float* __restrict__ x,
                         float* __restrict__ dst, const GemvParams p) {
     gemv_body<WQ4_0, T, LPR, PPL, CL, M_DUAL>(w, w2, x, dst, p);
 }
 
 template <int T, int LPR, int PPL, int CL>
-__global__ void __launch_bounds__(THREADS, PPL <= 3 ? 2 : 1)
+__global__ void __launch_bounds__(THREADS, gemv_min_ctas(PPL))
 gemv_q8_0_kernel(const uint8_t* __restrict__ w, const uint8_t* __restrict__ w2, const float* __restrict__ x,
                  float* __restrict__ dst, const GemvParams p) {
     gemv_body<WQ8_0, T, LPR, PPL, CL, M_SINGLE>(w, w2, x, dst, p);
 }
 
 template <int T, int LPR, int PPL, int CL>
-__global__ void __launch_bounds__(THREADS, PPL <= 3 ? 2 : 1)
+__global__ void __launch_bounds__(THREADS, gemv_min_ctas(PPL))
 gemv_q4_0_epi_kernel(const uint8_t* __restrict__ w, const uint8_t* __restrict__ w2, const float* __restrict__ x,
                      float* __restrict__ dst, const GemvParams p) {
     gemv_body<WQ4_0, T, LPR, PPL, CL, M_EPI>(w, w2, x, dst, p);
 }
 
 template <int T, int LPR, int PPL, int CL>
-__global__ void __launch_bounds__(THREADS, PPL <= 3 ? 2 : 1)
+__global__ void __launch_bounds__(THREADS, gemv_min_ctas(PPL))
 gemv_q4_0_group_kernel(const uint8_t* __restrict__ w, const uint8_t* __restrict__ w2, const float* __restrict__ x,
                        float* __restrict__ dst, const GemvParams p) {
     gemv_body<WQ4_0, T, LPR, PPL, CL, M_GROUP>(w, w2, x, dst, p);
@@ -718,9 +723,15 @@ bool plan_gemv(int64_t ne00, int64_t ne01, int64_t ne11, const DeviceInfo& info,
     if (!small) {
         // rows per unit: aim at ~16 KB stages, but keep >= 2 units per SM when the matrix
         // allows.  Small stages let two CTAs share an SM with >= 3 stages each (16
-        // consumer warps): K = 4096 rows of 2304 bytes stage 8 at a time, 5 stages per
-        // CTA; timed on the Llama-3-8B decode set, 32 KB stages (one CTA per SM, 6
-        // stages) were 1.5% slower.
+        // consumer warps): K = 4096 rows of 2304 bytes stage 8 at a time; timed on the
+        // Llama-3-8B decode set, 32 KB stages (one CTA per SM, 6 stages) were 1.5% slower.
+        // With one or two register-resident activation pairs a lane the ring stops at 4
+        // stages (77 KB a CTA at K = 4096): two such CTAs leave room on the SM for a small
+        // matrix's CTA (the next q projection of a decode chain, 68 KB), which then
+        // prefetches its weights under PDL, while a third CTA of the same kernel does not
+        // fit, so a freed SM never takes three of them.  Timed against 5 stages (same box,
+        // Llama decode step as PDL-chained graphs): 86.8 -> 86.0 us a step, the lm_head
+        // alone 50.5 -> 47.4 us.
         const int64_t rp_bytes = (int64_t)RP * urow;
         G = RP * std::max<int64_t>(1, (16384 + rp_bytes / 2) / rp_bytes);
         while (G > 8 && (ne01 + G - 1) / G < 2 * sms) G = std::max<int64_t>(8, G / 2);
@@ -729,6 +740,7 @@ bool plan_gemv(int64_t ne00, int64_t ne01, int64_t ne11, const DeviceInfo& info,
             stage = ((g * urow) + 127) / 128 * 128;
             int64_t n = 0;
             if (two_per_sm) n = (std::min<int64_t>(limit, 110 * 1024) - head - act_bytes) / stage;
+            if (two_per_sm && plan->ppl_reg >= 1 && plan->ppl_reg <= 2) n = std::min<int64_t>(n, 4);
             if (n < 3) n = (limit - head - act_bytes) / stage;
             return n;
         };
@@ -741,6 +753,27 @@ bool plan_gemv(int64_t ne00, int64_t ne01, int64_t ne11, const DeviceInfo& info,
             S = stages_for(G);
         }
         if (S < 2) return false;
+        // Balance: the persistent CTAs take units round-robin, so the busiest one streams
+        // ceil(units / CTAs) units.  Among unit sizes from G/2 to G that keep the same CTAs
+        // per SM, take the one that leaves it the fewest rows, if that saves at least 5%
+        // (the 14336 -> 4096 down projection on 152 SMs: 512 units of 8 rows, 4 on the
+        // busiest CTA, 32 rows; 586 units of 7 rows, 28 rows).
+        const auto per_sm_of = [&](int64_t s, int64_t st) {
+            return (two_per_sm && head + act_bytes + std::min<int64_t>(s, MAX_STAGES) * st <= 113 * 1024) ? 2 : 1;
+        };
+        const int64_t cap = sms * per_sm_of(S, stage);
+        const auto busiest_rows = [&](int64_t g) { return ((ne01 + g - 1) / g + cap - 1) / cap * g; };
+        int64_t best = G, best_rows = busiest_rows(G);
+        for (int64_t g = G - 1; g >= std::max<int64_t>(1, G / 2); --g) {
+            const int64_t sg = stages_for(g);
+            if (sg < 2 || sms * per_sm_of(sg, stage) != cap) continue;
+            if (busiest_rows(g) * 20 <= busiest_rows(G) * 19 && busiest_rows(g) < best_rows) {
+                best = g;
+                best_rows = busiest_rows(g);
+            }
+        }
+        G = best;
+        S = stages_for(G);
         S = std::min<int64_t>(S, MAX_STAGES);
     }
     p.G = (int)G;

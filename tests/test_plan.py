@@ -85,12 +85,19 @@ def test_every_decode_shape_of_the_workloads_has_a_plan(lib):
 
 
 def test_plans_recorded_by_ncu(lib):
-    # lm_head 4096 -> 128256, 1 token: 8-row units, 5 stages, two CTAs per SM (grid 304)
+    # lm_head 4096 -> 128256, 1 token: 8-row units, 4 stages, two CTAs per SM (grid 304);
+    # two such CTAs leave room for a small matrix's CTA (the q projection, 68 KB), three
+    # do not fit
     p, _ = plan(lib, 4096, 128256, 1)
-    assert (p["G"], p["S"], p["stage"], p["grid"], p["cl"], p["lpr"], p["ppl_reg"]) == (8, 5, 18432, 304, 1, 32, 2)
-    # down 14336 -> 4096, 1 token: CTA pairs share the activation quantization
+    assert (p["G"], p["S"], p["stage"], p["grid"], p["cl"], p["lpr"], p["ppl_reg"]) == (8, 4, 18432, 304, 1, 32, 2)
+    q, _ = plan(lib, 4096, 4096, 1)
+    per_cta = 1024   # shared memory the SM reserves for every resident CTA
+    assert 2 * (p["smem"] + per_cta) + q["smem"] + per_cta <= 228 * 1024 < 3 * (p["smem"] + per_cta)
+    # down 14336 -> 4096, 1 token: CTA pairs share the activation quantization; 7-row
+    # units (586 of them, at most 4 on a CTA: 28 rows) balance the 152 CTAs better than
+    # 8-row units (512, at most 4: 32 rows)
     p, _ = plan(lib, 14336, 4096, 1)
-    assert (p["cl"], p["ppl_reg"], p["G"]) == (2, 7, 8)
+    assert (p["cl"], p["ppl_reg"], p["G"], p["units"]) == (2, 7, 7, 586)
     # the same with Q8_0 rows (15 KB): 4-row units so that three stages fit
     p, _ = plan(lib, 14336, 4096, 1, 34)
     assert (p["G"], p["S"], p["cl"]) == (4, 3, 2)
