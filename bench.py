@@ -629,20 +629,23 @@ def measure_batched(dev, stream, args):
     torch.cuda.empty_cache()
     if args.sweep_tokens:
         out["token_sweep"] = measure_token_sweep(dev, stream, shapes, wq,
-                                                 [int(t) for t in args.sweep_tokens.split(",") if t])
+                                                 [int(t) for t in args.sweep_tokens.split(",") if t],
+                                                 max(1, args.graph_rounds))
     del wq
     torch.cuda.empty_cache()
     return out
 
 
-def measure_token_sweep(dev, stream, shapes, wq, tokens):
+def measure_token_sweep(dev, stream, shapes, wq, tokens, rounds):
     """One step over the Llama-3-8B-shaped projection set (the 8 q4q_mul_mat calls) at
     each token count of `tokens`: weights resident in 4 rotating copies (more than 3 x
     L2, so every step reads them from HBM), activations N(0, 1) (seed 5), every call
-    with the workspace q4q_mul_mat_workspace_size asks for and the PDL flag, one CUDA
-    graph per weight copy.  The roofline time of a step is the larger of its Q4_0
-    weight bytes over the measured HBM bandwidth and its 2*M*N*K ops over the measured
-    dense bf16 rate; frac = that time / the measured time."""
+    with the workspace q4q_mul_mat_workspace_size asks for and the PDL flag.  As for the
+    1-token line, one CUDA graph holds `rounds` passes over the copies (rounds x 4 steps
+    in order; PDL does not reach across graph launches).  The roofline time of a step
+    is the larger of its Q4_0 weight bytes over the measured HBM bandwidth and its
+    2*M*N*K ops over the measured dense bf16 rate; frac = that time / the measured
+    time."""
     import torch
 
     import q4_quantized_matmul_gb300 as q4q
@@ -664,18 +667,24 @@ def measure_token_sweep(dev, stream, shapes, wq, tokens):
                 q4q.q4q_mul_mat(wsets[c][i], ne00, ne01, xs[ne00], dst=ds[i], workspace=ws,
                                 flags=q4q.Q4Q_MUL_MAT_PDL)
 
-        graphs = [_capture(stream, lambda c=c: step(c)) for c in range(copies)]
-        reps = 20
+        def steps():
+            for _ in range(rounds):
+                for c in range(copies):
+                    step(c)
+
+        graph = _capture(stream, steps)
+        per_graph = rounds * copies
+        reps = max(1, -(-24 // per_graph))   # graph replays timed: at least 24 steps
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
-            for k in range(3 * copies):
-                graphs[k % copies].replay()
+            for k in range(max(1, -(-12 // per_graph))):
+                graph.replay()
             e0.record(stream)
             for k in range(reps):
-                graphs[k % copies].replay()
+                graph.replay()
             e1.record(stream)
         torch.cuda.synchronize()
-        us = e0.elapsed_time(e1) * 1e3 / reps
+        us = e0.elapsed_time(e1) * 1e3 / (reps * per_graph)
         ops = sum(2.0 * k * n * ne11 for k, n in shapes)
         t_bytes = wbytes / (hbm * 1e3)             # us
         t_ops = ops / (bf16 * 1e6)                 # us
@@ -686,12 +695,13 @@ def measure_token_sweep(dev, stream, shapes, wq, tokens):
                      "roofline_us": round(max(t_bytes, t_ops), 1),
                      "roofline_bound": "hbm" if t_bytes >= t_ops else "tensor",
                      "frac": round(max(t_bytes, t_ops) / us, 4)})
-        del graphs, xs, ds, ws
+        del graph, xs, ds, ws
         torch.cuda.empty_cache()
     del wsets
     torch.cuda.empty_cache()
     return {"workload": "llama3_8b_batched shapes (8 projections, one layer + lm_head)", "rows": rows,
             "peaks": {"hbm_gb_s": hbm, "hbm_kind": hbm_kind, "bf16_tflops": bf16, "bf16_kind": bf16_kind},
+            "graph_steps": rounds * copies,
             "note": "us per step of 8 q4q_mul_mat calls; 1 token is the main line"}
 
 
@@ -1097,8 +1107,10 @@ def main():
     ap.add_argument("--batched-tokens", type=int, default=512,
                     help="also measure the tensor-core path on the Llama-3-8B set at this many tokens (0 = skip)")
     ap.add_argument("--matrices", default="", help="comma-separated indices: only those matrices of the set")
-    ap.add_argument("--graph-rounds", type=int, default=2,
-                    help="decode steps: rounds over the weight copies captured in one CUDA graph")
+    ap.add_argument("--graph-rounds", type=int, default=7,
+                    help="decode steps: rounds over the 4 weight copies captured in one CUDA graph (7: 28 "
+                         "steps, 224 launches, about one Llama-3-8B token of 32 layers x 7 projections "
+                         "+ lm_head)")
     ap.add_argument("--sweep-tokens", default="2,4,7,8,16,32,64",
                     help="token counts of the batched-shape sweep (empty = skip)")
     ap.add_argument("--next-rows", type=int, default=1,

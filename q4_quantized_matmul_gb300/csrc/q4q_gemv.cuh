@@ -715,6 +715,12 @@ bool plan_gemv(int64_t ne00, int64_t ne01, int64_t ne11, const DeviceInfo& info,
         // start (about two units each), and leaves room on the SM for the next
         // kernel's CTA, which can then prefetch its own weights under PDL.
         G = std::max<int64_t>(1, (ne01 + 2 * sms - 1) / (2 * sms));
+        // Where one unit per CTA still fits the RP row groups, take it: the busiest CTA
+        // then runs one dot pass instead of two, and under PDL the weights are in shared
+        // memory already, so only that pass is on the dependency chain (Llama-3-8B k / v:
+        // 7-row units, 147 of them, instead of 256 units of 4 rows).
+        const int64_t g1 = (ne01 + sms - 1) / sms;
+        if (g1 <= RP) G = std::max<int64_t>(1, g1);
         const int64_t units = (ne01 + G - 1) / G;
         S = std::min<int64_t>(MAX_STAGES, (units + sms - 1) / sms);
         stage = ((G * urow) + 127) / 128 * 128;
