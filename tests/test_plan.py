@@ -110,6 +110,20 @@ def test_plans_recorded_by_ncu(lib):
     assert (p["G"], p["S"], p["units"], p["grid"]) == (7, 1, 147, 147)
 
 
+def test_small_plans_run_one_pass(lib):
+    # A small matrix (at most 96 KB of weights per SM) whose rows fit one pass of the
+    # row groups on every SM gets one unit per CTA: ceil(ne01 / SMs) rows, one dot pass.
+    for ne00 in (256, 768, 1024, 3072, 4096):
+        for ne01 in (1, 7, 100, 152, 153, 768, 1000, 1024, 1216, 2304):
+            for t in (1, 2, 3):
+                p, st = plan(lib, ne00, ne01, t)
+                assert st == 0, (ne00, ne01, t)
+                rp = 256 // p["lpr"]
+                g1 = -(-ne01 // SMS)
+                if ne01 * p["row_bytes"] <= 96 * 1024 * SMS and g1 <= rp and p["ppl_reg"] <= 3:
+                    assert p["G"] == g1 and p["units"] <= p["grid"] and p["S"] == 1, (ne00, ne01, t, p)
+
+
 def test_shapes_the_gemv_does_not_take(lib):
     assert plan(lib, 800, 10, 1)[1] == 2            # ne00 % 256 != 0
     assert plan(lib, 4096, 10, 8)[1] == 2           # 8 tokens: the tensor-core path
