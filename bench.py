@@ -448,8 +448,9 @@ def run_ours(args, rank, world, local_rank):
         },
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": act_bytes,
                 "d2h_bytes_per_step": out_bytes,
-                "how": "CUDA graph per step: pinned-host -> device copy of all activations, %d q4q_mul_mat "
-                       "calls, device -> pinned-host copy of all outputs" % nmat},
+                "how": "every step: pinned-host -> device copy of all activations, %d q4q_mul_mat calls, "
+                       "device -> pinned-host copy of all outputs, in stream order; captured like the "
+                       "device-resident line (CUDA graphs of %d steps)" % (nmat, graph_steps)},
         "weight_quantize": {"gb_per_s_fp32_in": round(quant_in_bytes / (quant_ms * 1e-3) / 1e9, 1),
                             "gb_per_s_in_out": round((quant_in_bytes + quant_out_bytes) / (quant_ms * 1e-3) / 1e9, 1),
                             "frac_of_hbm": round((quant_in_bytes + quant_out_bytes) / (quant_ms * 1e-3) / 1e9 / peak,
