@@ -263,9 +263,12 @@ def test_block_isums_mma_extremes(q4q):
 # ------------------------------------------------------------------- mul_mat --
 
 # (14336, 1): a CTA pair where one CTA has no rows; (8448, 129), (2816, 50) at 7
-# tokens: pairs whose two halves of the blocks split inside a token
+# tokens: pairs whose two halves of the blocks split inside a token; (4096, 1216): one
+# full 8-row unit on each of 152 CTAs (one dot pass), (4096, 1217): one row more, two
+# units a CTA again; (768, 153): one row past one-row units
 GEMV_SHAPES = [(256, 1), (256, 3), (768, 2304), (768, 1000), (3072, 768), (4096, 1024), (14336, 64),
-               (512, 33), (1024, 4099), (14336, 1), (8448, 129), (2816, 50)]
+               (512, 33), (1024, 4099), (14336, 1), (8448, 129), (2816, 50), (4096, 1216), (4096, 1217),
+               (768, 153)]
 
 
 @pytest.mark.parametrize("ne00,ne01", GEMV_SHAPES)
