@@ -155,6 +155,20 @@ def job_throughput(bytes_per_rank_step: float, steps: int, world: int, max_ms: f
     return world * bytes_per_rank_step * steps / (max_ms * 1e-3) / 1e9
 
 
+def graph_replays(k_steps: int, graph_steps: int, rest_steps: int):
+    """The graph launches that run exactly k_steps steps: whole graphs of graph_steps
+    steps, then the remainder as one graph of rest_steps steps when it matches, else as
+    single-step graphs.  Returns a list of (kind, steps) with kind "multi", "rest" or
+    "single" (steps = steps run by that launch)."""
+    if graph_steps <= 1:
+        return [("single", 1)] * k_steps
+    out = [("multi", graph_steps)] * (k_steps // graph_steps)
+    left = k_steps % graph_steps
+    if left:
+        out += [("rest", left)] if left == rest_steps else [("single", 1)] * left
+    return out
+
+
 # --------------------------------------------------------------- the arms ---
 
 def _weights_bytes(shapes):
@@ -262,20 +276,19 @@ def run_ours(args, rank, world, local_rank):
     rest_graph = capture_rest(step)
     torch.cuda.synchronize()
 
+    rest_steps = args.steps % graph_steps if graph_steps > 1 else 0
+
     def run_steps(multi_graph, single_graphs, k_steps, rest=None):
         """Exactly k_steps steps: whole multi-step graphs, then the rest (one graph)."""
-        if graph_steps == 1:
-            for k in range(k_steps):
-                single_graphs[k % copies].replay()
-            return
-        for _ in range(k_steps // graph_steps):
-            multi_graph.replay()
-        if k_steps % graph_steps:
-            if rest is not None and k_steps == args.steps:
+        k = 0
+        for kind, _ in graph_replays(k_steps, graph_steps, rest_steps if rest is not None else -1):
+            if kind == "multi":
+                multi_graph.replay()
+            elif kind == "rest":
                 rest.replay()
             else:
-                for k in range(k_steps % graph_steps):
-                    single_graphs[k % copies].replay()
+                single_graphs[k % copies].replay()
+                k += 1
 
     def barrier():
         if world > 1:
